@@ -1,0 +1,465 @@
+#!/usr/bin/env python
+"""Throughput of the causal kernelised linear-attention forward on GB300.
+
+Default workload: B=2, H=16, N=32768, d=dv=64, bf16 q/k/v ~ N(0,1), elu+1
+feature map, normalised, causal -- one "step" is one la_forward over the
+whole batch (every step of the hot path: feature map, chunk states, chunk
+scan, intra- and inter-chunk products, normalisation).  Prints ONE JSON line
+on rank 0 with token*heads/s, the roofline fraction of the dominant kernel,
+an end-to-end figure through the C ABI with host buffers, and the fp64
+oracle timed on the host cores as a CPU baseline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(independent sequences: weak scaling, no data-path collective); the timed
+region is bracketed by barriers and the max over ranks is reported.
+`--impl reference` times the fp64 CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+import torch
+
+ROOT = Path(__file__).resolve().parent
+METRIC = "causal linear-attn fwd token·heads/s at N=32768,d=64; % of HBM/TC roofline"
+UNIT = "token*heads/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 10**6
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=None)
+    p.add_argument("--warmup", type=int, default=None)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="causal_n32768_d64_bf16")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = ROOT / "MEASURED_PEAKS.json"
+    if path.exists():
+        d = json.loads(path.read_text())
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------ clocks -----
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.dev)], stdout=self.file,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in Path(self.file.name).read_text().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        loaded = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------- workload glue ---
+def algorithmic_bytes(w) -> int:
+    """Bytes the method must move per forward launch: q, k, v in, fp32 o out
+    (the state never needs to leave the chip)."""
+    eb = torch.tensor([], dtype=w.dtype).element_size()
+    return w.BH * w.N * (2 * w.d * eb + w.dv * eb + w.dv * 4)
+
+
+def algorithmic_flops(w) -> int:
+    """4 r dv + 4 r FLOPs per token and head: rank-1 state update, read, and
+    the normaliser update and dot (r = d)."""
+    return w.BH * w.N * (4 * w.d * w.dv + 4 * w.d)
+
+
+def decode_bytes(w) -> int:
+    eb = torch.tensor([], dtype=w.dtype).element_size()
+    per = 2 * 4 * (w.d * w.dv + w.d) + (2 * w.d + w.dv) * eb + w.dv * 4
+    return w.BH * per
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_forward_sample(w, q, k, v, cores):
+    """Time the fp64 oracle on whole sequences of the workload (a bounded
+    sample); returns (token*heads/s, description, threads)."""
+    import numpy as np
+
+    import oracle
+
+    orc = oracle.load()
+    ns = min(w.BH, 2 * cores)
+    qf, kf, vf = (t.reshape(w.BH, 1, w.N, -1)[:ns].float().cpu().numpy().astype(np.float64)
+                  for t in (q, k, v))
+    gamma = w.gamma()
+    t0 = time.perf_counter()
+    orc.forward(qf.reshape(ns, 1, w.N, -1), kf.reshape(ns, 1, w.N, -1),
+                vf.reshape(ns, 1, w.N, -1), causal=w.causal, fm=w.feature_map,
+                gamma=None if gamma is None else gamma[:1].double().numpy(), nthreads=cores)
+    dt = time.perf_counter() - t0
+    return ns * w.N / dt, f"{ns} of {w.BH} sequences x {w.N} tokens (fp64 oracle)", min(ns, cores), dt
+
+
+# --------------------------------------------------------------- main ----
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from kernelised_causal_linear_gb300 import synth
+
+    w = synth.WORKLOADS[args.workload]
+    decode = w.steps > 0
+    steps = args.steps if args.steps is not None else (200 if decode else 400)
+    warmup = args.warmup if args.warmup is not None else 10
+    if warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args, w, steps, warmup, world)
+
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+
+    import kernelised_causal_linear_gb300 as la
+
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream()
+
+    if decode:
+        from kernelised_causal_linear_gb300 import prefill
+
+        S, z = prefill.prefill_decode_state(w)
+        tok = synth.decode_tokens(w, 1, device="cuda")
+        q, k, v = (t[0] for t in tok)
+        out = torch.empty((w.B, w.H, w.dv), dtype=torch.float32, device="cuda")
+
+        def step():
+            la.la_decode_step(S, z, q, k, v, out, feature_map=w.feature_map)
+
+        units_per_step = w.BH
+        bytes_per_launch = decode_bytes(w)
+    else:
+        q, k, v = synth.qkv(w, device="cuda")
+        out = torch.empty((w.B, w.H, w.N, w.dv), dtype=torch.float32, device="cuda")
+        ws = torch.empty(max(16, la.la_forward_workspace_size(w.B, w.H, w.N, w.d, w.dv, w.causal,
+                                                               w.dtype)),
+                         dtype=torch.uint8, device="cuda")
+        gamma = w.gamma()
+
+        def step():
+            la.la_forward(q, k, v, out, causal=w.causal, feature_map=w.feature_map, gamma=gamma,
+                          workspace=ws)
+
+        units_per_step = w.BH * w.N
+        bytes_per_launch = algorithmic_bytes(w)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    assert la.la_get_device_status() == 0
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        n0 = la.la_launch_count()
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        n1 = la.la_launch_count()
+        barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms_total], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / steps
+    value = units_per_step * world * steps / (ms_total / 1e3)
+    assert la.la_get_device_status() == 0
+
+    # --- end to end through the C ABI with pinned host buffers ------------
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(la, w, decode, steps, stream, world, out, locals())
+
+    # --- CPU baseline: the fp64 oracle on a bounded sample -----------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = cpu_cores()
+        if decode:
+            cpu = cpu_decode_baseline(w, S, z, cores)
+        else:
+            val, desc, used, dt = oracle_forward_sample(w, q, k, v, cores)
+            cpu = {"value": val, "unit": UNIT, "cores": used, "kind": "oracle",
+                   "sample": f"{desc}; {dt:.1f} s wall"}
+
+    achieved = bytes_per_launch / (ms_step / 1e3) / 1e9
+    line = {
+        "metric": METRIC if not decode else "batched decode step token*heads/s, d=dv=128",
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": la_path_dtype(w),
+        "data": "synthetic: seeded i.i.d. normal inputs rounded once to the input dtype",
+        "config": {
+            "workload": w.name, "B": w.B, "H": w.H, "N": w.N if not decode else 1,
+            "d": w.d, "dv": w.dv, "input_dtype": str(w.dtype).replace("torch.", ""),
+            "causal": w.causal, "feature_map": w.feature_map, "decay": w.decay,
+            "l2": f"no flush: every step moves {bytes_per_launch / 1e6:.0f} MB, more than the "
+                  f"{L2_BYTES / 1e6:.0f} MB L2",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": peaks["hbm_gbs"],
+            "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"],
+            "traffic": None,
+            "kernel": "la_forward (all launches of one call)" if not decode else "k_decode_step",
+            "peak_source": f"{peak_src} HBM copy bandwidth",
+            "algorithmic_bytes_per_launch": bytes_per_launch,
+        },
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(n1 - n0),
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def la_path_dtype(w) -> str:
+    return "f32"
+
+
+def run_e2e(la, w, decode, steps, stream, world, out, env):
+    """The same metric with host buffers: every step copies its inputs from
+    pinned host memory, runs the C-ABI call and reads the result back."""
+    if decode:
+        q, k, v = env["q"], env["k"], env["v"]
+        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        S, z = env["S"], env["z"]
+
+        def step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            la.la_decode_step(S, z, q, k, v, out, feature_map=w.feature_map)
+            hout.copy_(out, non_blocking=True)
+
+        units = w.BH
+    else:
+        q, k, v, ws = env["q"], env["k"], env["v"], env["ws"]
+        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        gamma = w.gamma()
+
+        def step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            la.la_forward(q, k, v, out, causal=w.causal, feature_map=w.feature_map, gamma=gamma,
+                          workspace=ws)
+            hout.copy_(out, non_blocking=True)
+
+        units = w.BH * w.N
+    n = max(3, min(steps, 50))
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(n):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = hout.numel() * hout.element_size()
+    return {"value": units * world * n / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n}
+
+
+def cpu_decode_baseline(w, S, z, cores):
+    import numpy as np
+
+    import oracle
+    from kernelised_causal_linear_gb300 import synth
+
+    orc = oracle.load()
+    ns = min(w.BH, 256)
+    steps = 5
+    Sh = S.reshape(w.BH, 1, w.d, w.dv)[:ns].double().cpu().numpy()
+    zh = z.reshape(w.BH, 1, w.d)[:ns].double().cpu().numpy()
+    q, k, v = synth.decode_tokens(w, steps, device="cpu")
+    qs = q.reshape(steps, w.BH, 1, w.d)[:, :ns].double().numpy()
+    ks = k.reshape(steps, w.BH, 1, w.d)[:, :ns].double().numpy()
+    vs = v.reshape(steps, w.BH, 1, w.dv)[:, :ns].double().numpy()
+    t0 = time.perf_counter()
+    for t in range(steps):
+        _, Sh, zh = orc.decode_step(Sh, zh, qs[t], ks[t], vs[t], nthreads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": ns * steps / dt, "unit": UNIT, "cores": min(cores, ns), "kind": "oracle",
+            "sample": f"{ns} of {w.BH} sequences x {steps} decode steps (fp64 oracle); "
+                      f"{dt:.1f} s wall"}
+
+
+def run_reference(args, w, steps, warmup, world):
+    """--impl reference: the fp64 oracle on the host cores, each step a
+    bounded sample of the same workload."""
+    import numpy as np
+
+    import oracle
+    from kernelised_causal_linear_gb300 import synth
+
+    orc = oracle.load()
+    cores = cpu_cores()
+    gamma = w.gamma()
+    if w.steps > 0:
+        ns = min(w.BH, 4 * cores)
+        Sh = np.zeros((ns, 1, w.d, w.dv))
+        zh = np.zeros((ns, 1, w.d))
+        q, k, v = synth.decode_tokens(w, 1, device="cpu")
+        qs, ks, vs = (t.reshape(w.BH, 1, -1)[:ns].double().numpy() for t in (q[0], k[0], v[0]))
+
+        def step():
+            nonlocal Sh, zh
+            _, Sh, zh = orc.decode_step(Sh, zh, qs, ks, vs, nthreads=cores)
+
+        units = ns
+        desc = f"{ns} of {w.BH} sequences, one decode step each (fp64 oracle)"
+    else:
+        ns = min(w.BH, cores)
+        n_tok = min(w.N, 4096)
+        q, k, v = synth.qkv(w, device="cpu", B=1, H=ns, N=n_tok)
+        qf, kf, vf = (t.double().numpy() for t in (q, k, v))
+
+        def step():
+            orc.forward(qf, kf, vf, causal=w.causal, fm=w.feature_map,
+                        gamma=None if gamma is None else np.full(ns, float(gamma[0])),
+                        nthreads=cores)
+
+        units = ns * n_tok
+        desc = f"{ns} of {w.BH} sequences x first {n_tok} of {w.N} tokens (fp64 oracle)"
+    for _ in range(warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = units * steps / dt
+    line = {
+        "impl": "reference",
+        "metric": METRIC if w.steps == 0 else "batched decode step token*heads/s, d=dv=128",
+        "value": value, "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": warmup,
+        "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dv": w.dv},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(cores, ns), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

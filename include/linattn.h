@@ -1,0 +1,171 @@
+/*
+ * linattn.h -- C ABI of the GB300 (sm_103a) causal kernelised linear
+ * attention library (liblinattn.so).
+ *
+ * The operation, in the notation of the pages it follows:
+ *
+ *   feature map   phi(x) = elu(x) + 1  (alpha = 1; positive)
+ *                 ["Linear Attention Kernel", section "Choice of phi";
+ *                  "Efficient Attention Variants", section 4]
+ *   causal state  S_t = S_{t-1} + phi(k_t) v_t^T,  z_t = z_{t-1} + phi(k_t),
+ *                 S_0 = 0, z_0 = 0, write before read (token t sees itself)
+ *   causal read   o_t = phi(q_t)^T S_t / phi(q_t)^T z_t
+ *                 ["Efficient Attention Variants", section 5, prefix-sum
+ *                  recurrence; "Linear Attention Kernel", section
+ *                  "Recurrent form"]
+ *   non-causal    S = phi(K)^T V, z = column sums of phi(K),
+ *                 o_i = phi(q_i)^T S / phi(q_i)^T z
+ *                 ["Linear Attention Kernel", section "Rewrite:
+ *                  associativity"; "Efficient Attention Variants", section 4]
+ *   scalar decay  S_t = gamma_h S_{t-1} + k_t v_t^T,  o_t = q_t^T S_t
+ *                 (RetNet; no feature map, no normaliser)
+ *                 ["Efficient Attention Variants", section 7.1]
+ *   decode step   one iteration of the causal recurrence on a stored state,
+ *                 with no KV cache ["Efficient Attention Variants",
+ *                 sections 1 and 5; "Linear Attention and SSM", eq.
+ *                 attn-linssm-recurrence]
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor arguments are DEVICE pointers on the current CUDA device,
+ *    owned by the caller, contiguous row-major, 16-byte aligned:
+ *        q, k   [B, H, N, d]     (dtype: bf16 or fp32, see la_dtype)
+ *        v      [B, H, N, dv]
+ *        out    [B, H, N, dv]    always fp32
+ *        S      [B, H, d, dv]    fp32, S[b,h,i,c] pairs key feature i with
+ *                                value channel c
+ *        z      [B, H, d]        fp32
+ *    The feature dimension r of the pages equals d.
+ *  - d and dv must each be 32, 64 or 128.  B, H >= 1.  N >= 0 (N = 0 is a
+ *    no-op).  B*H <= 2^31 - 1.
+ *  - gamma is a HOST pointer to H floats (per-head decay, 0 < gamma <= 1),
+ *    read during the call and not retained, or NULL for no decay.  For
+ *    normalised feature maps the decay weights numerator and denominator
+ *    alike (mask gamma^(t-j)).  Decay is not defined for the non-causal form.
+ *  - Every call only enqueues work on `stream` (NULL = legacy default stream)
+ *    and returns; results are ready once the stream is synchronised.  No
+ *    entry point allocates or frees memory on the compute path; scratch is
+ *    the caller's `workspace`.
+ *  - Argument errors are returned before anything is enqueued.  A status of
+ *    LA_ERR_CUDA means a launch failed (the CUDA error is left for the
+ *    caller's next runtime call).  Device-side checks (bounded waits, index
+ *    checks) never trap: they record a code in a per-device status word that
+ *    la_get_device_status() returns and clears.
+ *  - Normalised reads divide by max(phi(q)^T z, FLT_MIN); for elu+1 the
+ *    denominator is a sum of positive terms, so this only matters when every
+ *    term underflows (the numerator is then zero too and o = 0).
+ */
+#ifndef LINATTN_H
+#define LINATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LA_API __attribute__((visibility("default")))
+#else
+#define LA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; kept opaque so this header needs no CUDA headers. */
+typedef struct CUstream_st* la_stream_t;
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1,   /* NULL / misaligned pointer, bad size or enum  */
+    LA_ERR_UNSUPPORTED = 2,   /* valid request outside what is implemented   */
+    LA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed        */
+    LA_ERR_TIMEOUT = 4,       /* device: a bounded wait gave up              */
+    LA_ERR_DEVICE_CHECK = 5,  /* device: an internal consistency check failed */
+    LA_ERR_WORKSPACE = 6      /* workspace missing or smaller than required  */
+} la_status;
+
+typedef enum {
+    LA_FM_ELU1 = 0,          /* phi = elu + 1, normalised read               */
+    LA_FM_IDENTITY_NORM = 1, /* phi = identity, normalised read (the pages'
+                                hand-worked examples give features directly) */
+    LA_FM_NONE = 2           /* phi = identity, unnormalised (RetNet)        */
+} la_feature_map;
+
+typedef enum {
+    LA_BF16 = 0,             /* q, k, v are bfloat16                          */
+    LA_FP32 = 1              /* q, k, v are float                             */
+} la_dtype;
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+LA_API int la_version(void);
+
+/* Static description of a status code; never NULL. */
+LA_API const char* la_status_string(la_status status);
+
+/*
+ * Bytes of device workspace la_forward needs for these sizes (0 for N = 0).
+ * The workspace holds per-chunk fp32 states and the chunk-scan flags; its
+ * contents on entry do not matter and on exit are unspecified.
+ */
+LA_API size_t la_forward_workspace_size(int64_t B, int64_t H, int64_t N, int d, int dv, int causal,
+                                 int dtype);
+
+/*
+ * Forward over B*H independent sequences of N tokens.
+ *   causal = 1 : o_t reads the prefix state S_t (j <= t).
+ *   causal = 0 : every o_i reads the full-sequence state (gamma must be NULL).
+ *   feature_map: la_feature_map.  dtype: la_dtype of q, k, v.
+ *   workspace  : device buffer of at least la_forward_workspace_size() bytes,
+ *                16-byte aligned, owned by the caller; must not be used by
+ *                another call that runs concurrently.
+ * Returns LA_OK once the work is enqueued on `stream`.
+ */
+LA_API la_status la_forward(const void* q, const void* k, const void* v, float* out, int64_t B,
+                     int64_t H, int64_t N, int d, int dv, int causal, int feature_map,
+                     const float* gamma, int dtype, void* workspace, size_t workspace_bytes,
+                     la_stream_t stream);
+
+/* Bytes of device workspace la_state needs (0 for N = 0). */
+LA_API size_t la_state_workspace_size(int64_t B, int64_t H, int64_t N, int d, int dv, int dtype);
+
+/*
+ * Final state of the causal recurrence after N tokens, starting from
+ * S_0 = 0, z_0 = 0:  S [B,H,d,dv] and z [B,H,d] (fp32, overwritten).  This is
+ * the prefill that hands a prompt to la_decode_step.  With N = 0 the outputs
+ * are set to zero.  z is required for every feature map (for LA_FM_NONE it
+ * receives the undecayed-or-decayed key sum and is simply unused by reads).
+ */
+LA_API la_status la_state(const void* k, const void* v, float* S, float* z, int64_t B, int64_t H,
+                   int64_t N, int d, int dv, int feature_map, const float* gamma, int dtype,
+                   void* workspace, size_t workspace_bytes, la_stream_t stream);
+
+/*
+ * One decode step for B*H sequences, one new token each:
+ *   S <- gamma S + phi(k) v^T ;  z <- gamma z + phi(k) ;  o = phi(q)^T S / phi(q)^T z
+ * (o = phi(q)^T S for LA_FM_NONE).  S [B,H,d,dv] and z [B,H,d] are updated in
+ * place; q, k [B,H,d] and v [B,H,dv] are in `dtype`; out [B,H,dv] is fp32.
+ * Needs no workspace.
+ */
+LA_API la_status la_decode_step(float* S, float* z, const void* q, const void* k, const void* v,
+                         float* out, int64_t B, int64_t H, int d, int dv, int feature_map,
+                         const float* gamma, int dtype, la_stream_t stream);
+
+/*
+ * Diagnostic: total number of kernels this library has launched in this
+ * process (all devices, all threads).  The difference across a region counts
+ * the library's launches inside it.
+ */
+LA_API uint64_t la_launch_count(void);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's status
+ * word: LA_OK, LA_ERR_TIMEOUT or LA_ERR_DEVICE_CHECK (or LA_ERR_CUDA if the
+ * synchronisation itself failed).
+ */
+LA_API la_status la_get_device_status(la_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LINATTN_H */

@@ -1,0 +1,196 @@
+"""Thin ctypes binding of liblinattn.so with the C ABI's own names.
+
+Only argument marshalling happens here: tensors become device pointers and
+sizes, enums become ints, and a non-zero status becomes an exception.  Every
+step of the computation runs in the library's CUDA kernels.  There is no
+fallback: if the library has not been built, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+from . import build as _build
+
+LIB_PATH: Path = _build.LIB
+
+if not LIB_PATH.exists():
+    raise ImportError(
+        f"liblinattn.so not found at {LIB_PATH}; build it first with "
+        "`python -c 'import __graft_entry__ as g; g.build()'` "
+        "(kernelised_causal_linear_gb300.build.build())")
+
+_lib = ctypes.CDLL(str(LIB_PATH))
+
+LA_OK = 0
+STATUS_NAMES = {0: "LA_OK", 1: "LA_ERR_INVALID_ARG", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_CUDA",
+                4: "LA_ERR_TIMEOUT", 5: "LA_ERR_DEVICE_CHECK", 6: "LA_ERR_WORKSPACE"}
+FEATURE_MAPS = {"elu1": 0, "identity_norm": 1, "none": 2}
+DTYPES = {torch.bfloat16: 0, torch.float32: 1}
+
+_vp, _i64, _i, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+_fp = ctypes.POINTER(ctypes.c_float)
+
+_lib.la_version.restype = _i
+_lib.la_version.argtypes = []
+_lib.la_status_string.restype = ctypes.c_char_p
+_lib.la_status_string.argtypes = [_i]
+_lib.la_forward_workspace_size.restype = _sz
+_lib.la_forward_workspace_size.argtypes = [_i64, _i64, _i64, _i, _i, _i, _i]
+_lib.la_state_workspace_size.restype = _sz
+_lib.la_state_workspace_size.argtypes = [_i64, _i64, _i64, _i, _i, _i]
+_lib.la_forward.restype = _i
+_lib.la_forward.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _i, _i, _fp, _i, _vp,
+                            _sz, _vp]
+_lib.la_state.restype = _i
+_lib.la_state.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _i, _fp, _i, _vp, _sz,
+                          _vp]
+_lib.la_decode_step.restype = _i
+_lib.la_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _i, _i, _fp, _i,
+                                _vp]
+_lib.la_launch_count.restype = ctypes.c_uint64
+_lib.la_launch_count.argtypes = []
+_lib.la_get_device_status.restype = _i
+_lib.la_get_device_status.argtypes = [_vp]
+
+
+class LinAttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {la_status_string(code)}")
+
+
+def la_version() -> int:
+    return _lib.la_version()
+
+
+def la_status_string(code: int) -> str:
+    return _lib.la_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str) -> None:
+    if code != LA_OK:
+        raise LinAttnError(code, where)
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def _gamma_arg(gamma, H: int):
+    if gamma is None:
+        return None, None
+    g = torch.as_tensor(gamma, dtype=torch.float32, device="cpu").contiguous().reshape(-1)
+    if g.numel() != H:
+        raise ValueError(f"gamma must have H={H} entries, got {g.numel()}")
+    return ctypes.cast(g.data_ptr(), _fp), g  # keep g alive for the call
+
+
+def _fm(feature_map) -> int:
+    return FEATURE_MAPS[feature_map] if isinstance(feature_map, str) else int(feature_map)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype not in DTYPES:
+        raise TypeError(f"unsupported input dtype {t.dtype}; use bfloat16 or float32")
+    return DTYPES[t.dtype]
+
+
+def _dev_ptr(t: torch.Tensor | None, name: str) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def la_forward_workspace_size(B, H, N, d, dv, causal=True, dtype=torch.bfloat16) -> int:
+    return int(_lib.la_forward_workspace_size(B, H, N, d, dv, int(bool(causal)),
+                                              DTYPES[dtype]))
+
+
+def la_state_workspace_size(B, H, N, d, dv, dtype=torch.bfloat16) -> int:
+    return int(_lib.la_state_workspace_size(B, H, N, d, dv, DTYPES[dtype]))
+
+
+def la_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor | None = None,
+               *, causal: bool = True, feature_map="elu1", gamma=None,
+               workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """q, k: [B,H,N,d]; v: [B,H,N,dv] (bf16 or fp32, CUDA) -> out [B,H,N,dv] fp32.
+
+    ``workspace`` may be passed to reuse scratch across calls (a uint8 CUDA
+    tensor of at least la_forward_workspace_size() bytes); otherwise one is
+    allocated by PyTorch for this call.
+    """
+    B, H, N, d = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=torch.float32, device=q.device)
+    need = la_forward_workspace_size(B, H, N, d, dv, causal, q.dtype) if q.dtype in DTYPES else 0
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    gp, _keep = _gamma_arg(gamma, H)
+    code = _lib.la_forward(_dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                           _dev_ptr(out, "out"), B, H, N, d, dv, int(bool(causal)),
+                           _fm(feature_map), gp, _dtype(q), _dev_ptr(workspace, "workspace"),
+                           workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(code, "la_forward")
+    return out
+
+
+def la_state(k: torch.Tensor, v: torch.Tensor, S: torch.Tensor | None = None,
+             z: torch.Tensor | None = None, *, feature_map="elu1", gamma=None,
+             workspace: torch.Tensor | None = None, stream=None):
+    """State after the N tokens of k [B,H,N,d], v [B,H,N,dv] -> (S [B,H,d,dv], z [B,H,d])."""
+    B, H, N, d = k.shape
+    dv = v.shape[-1]
+    if S is None:
+        S = torch.empty((B, H, d, dv), dtype=torch.float32, device=k.device)
+    if z is None:
+        z = torch.empty((B, H, d), dtype=torch.float32, device=k.device)
+    need = la_state_workspace_size(B, H, N, d, dv, k.dtype) if k.dtype in DTYPES else 0
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=k.device)
+    gp, _keep = _gamma_arg(gamma, H)
+    code = _lib.la_state(_dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(S, "S"), _dev_ptr(z, "z"),
+                         B, H, N, d, dv, _fm(feature_map), gp, _dtype(k),
+                         _dev_ptr(workspace, "workspace"),
+                         workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(code, "la_state")
+    return S, z
+
+
+def la_decode_step(S: torch.Tensor, z: torch.Tensor, q: torch.Tensor, k: torch.Tensor,
+                   v: torch.Tensor, out: torch.Tensor | None = None, *, feature_map="elu1",
+                   gamma=None, stream=None) -> torch.Tensor:
+    """One token per sequence: q, k [B,H,d], v [B,H,dv]; S, z updated in place."""
+    B, H, d = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=torch.float32, device=q.device)
+    gp, _keep = _gamma_arg(gamma, H)
+    code = _lib.la_decode_step(_dev_ptr(S, "S"), _dev_ptr(z, "z"), _dev_ptr(q, "q"),
+                               _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(out, "out"), B, H, d,
+                               dv, _fm(feature_map), gp, _dtype(q), _stream_handle(stream))
+    _check(code, "la_decode_step")
+    return out
+
+
+def la_launch_count() -> int:
+    return int(_lib.la_launch_count())
+
+
+def la_get_device_status(stream=None) -> int:
+    return int(_lib.la_get_device_status(_stream_handle(stream)))
+
+
+# raw handle, for callers that want the C functions directly (tests of the ABI)
+raw = _lib

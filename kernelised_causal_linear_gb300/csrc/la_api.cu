@@ -1,0 +1,232 @@
+// la_api.cu -- the C ABI of liblinattn.so: argument checks, dispatch, status.
+//
+// Every entry point validates its arguments before anything is enqueued and
+// never allocates: scratch is the caller's workspace, and the only
+// library-owned device object is the per-device status word below, a static
+// __device__ variable that exists as soon as the module is loaded.
+#include <atomic>
+#include <math.h>
+#include <mutex>
+
+#include "la_internal.cuh"
+
+namespace la {
+__device__ int g_device_status;  // LA_OK, or the first device-side error code
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mu;
+int* g_status_ptr[kMaxDevices];
+
+// Device address of the status word for the current device (looked up once).
+int* status_ptr()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    std::lock_guard<std::mutex> lk(g_status_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess)
+            return nullptr;
+        g_status_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+bool dim_ok(int x) { return x == 32 || x == 64 || x == 128; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+la_status check_sizes(int64_t B, int64_t H, int64_t N, int d, int dv, int fm, int dtype)
+{
+    if (B < 1 || H < 1 || N < 0 || d < 1 || dv < 1)
+        return LA_ERR_INVALID_ARG;
+    if (fm != LA_FM_ELU1 && fm != LA_FM_IDENTITY_NORM && fm != LA_FM_NONE)
+        return LA_ERR_INVALID_ARG;
+    if (dtype != LA_BF16 && dtype != LA_FP32)
+        return LA_ERR_INVALID_ARG;
+    if (!dim_ok(d) || !dim_ok(dv))
+        return LA_ERR_UNSUPPORTED;
+    if (B > INT32_MAX / H)
+        return LA_ERR_UNSUPPORTED;
+    return LA_OK;
+}
+
+// Fill the by-value decay table; NULL gamma means no decay.
+la_status make_gamma(const float* gamma, int64_t H, GammaTable* t)
+{
+    t->has_decay = 0;
+    t->H = (int)(H < kMaxGammaHeads ? H : kMaxGammaHeads);
+    if (!gamma)
+        return LA_OK;
+    if (H > kMaxGammaHeads)
+        return LA_ERR_UNSUPPORTED;
+    for (int64_t h = 0; h < H; ++h) {
+        const float gm = gamma[h];
+        if (!(gm > 0.0f && gm <= 1.0f))
+            return LA_ERR_INVALID_ARG;
+        t->g[h] = gm;
+        t->log2g[h] = (float)log2((double)gm);
+    }
+    t->has_decay = 1;
+    return LA_OK;
+}
+
+la_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+
+}  // namespace
+}  // namespace la
+
+using namespace la;
+
+extern "C" {
+
+int la_version(void) { return 100; }  // 0.1.0
+
+const char* la_status_string(la_status s)
+{
+    switch (s) {
+    case LA_OK: return "LA_OK: success";
+    case LA_ERR_INVALID_ARG: return "LA_ERR_INVALID_ARG: invalid argument (pointer, size, enum or gamma)";
+    case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED: valid request outside what is implemented";
+    case LA_ERR_CUDA: return "LA_ERR_CUDA: a CUDA runtime call or kernel launch failed";
+    case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT: a bounded device-side wait gave up";
+    case LA_ERR_DEVICE_CHECK: return "LA_ERR_DEVICE_CHECK: a device-side consistency check failed";
+    case LA_ERR_WORKSPACE: return "LA_ERR_WORKSPACE: workspace missing or too small";
+    }
+    return "unknown la_status";
+}
+
+size_t la_forward_workspace_size(int64_t B, int64_t H, int64_t N, int d, int dv, int causal,
+                                 int dtype)
+{
+    if (check_sizes(B, H, N, d, dv, LA_FM_ELU1, dtype) != LA_OK)
+        return 0;
+    return simt_forward_workspace(B * H, N, d, dv, causal);
+}
+
+size_t la_state_workspace_size(int64_t B, int64_t H, int64_t N, int d, int dv, int dtype)
+{
+    if (check_sizes(B, H, N, d, dv, LA_FM_ELU1, dtype) != LA_OK)
+        return 0;
+    return simt_state_workspace(B * H, N, d, dv);
+}
+
+la_status la_forward(const void* q, const void* k, const void* v, float* out, int64_t B,
+                     int64_t H, int64_t N, int d, int dv, int causal, int feature_map,
+                     const float* gamma, int dtype, void* workspace, size_t workspace_bytes,
+                     la_stream_t stream)
+{
+    la_status st = check_sizes(B, H, N, d, dv, feature_map, dtype);
+    if (st != LA_OK)
+        return st;
+    if (causal != 0 && causal != 1)
+        return LA_ERR_INVALID_ARG;
+    if (!causal && gamma)
+        return LA_ERR_UNSUPPORTED;  // decay is defined only for the causal form
+    GammaTable gt;
+    if ((st = make_gamma(gamma, H, &gt)) != LA_OK)
+        return st;
+    if (N == 0)
+        return LA_OK;
+    if (!q || !k || !v || !out)
+        return LA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return LA_ERR_INVALID_ARG;
+    const size_t need = simt_forward_workspace(B * H, N, d, dv, causal);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace))
+        return LA_ERR_WORKSPACE;
+
+    FwdArgs a{};
+    a.q = q, a.k = k, a.v = v, a.out = out;
+    a.B = B, a.H = H, a.N = N, a.d = d, a.dv = dv;
+    a.causal = causal, a.fm = feature_map, a.dtype = dtype;
+    a.gamma = &gt;
+    a.ws = workspace, a.ws_bytes = workspace_bytes;
+    a.status = status_ptr();
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    return from_cuda(simt_forward(a));
+}
+
+la_status la_state(const void* k, const void* v, float* S, float* z, int64_t B, int64_t H,
+                   int64_t N, int d, int dv, int feature_map, const float* gamma, int dtype,
+                   void* workspace, size_t workspace_bytes, la_stream_t stream)
+{
+    la_status st = check_sizes(B, H, N, d, dv, feature_map, dtype);
+    if (st != LA_OK)
+        return st;
+    GammaTable gt;
+    if ((st = make_gamma(gamma, H, &gt)) != LA_OK)
+        return st;
+    if (!S || !z || !aligned16(S) || !aligned16(z))
+        return LA_ERR_INVALID_ARG;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (N == 0) {
+        cudaError_t e = cudaMemsetAsync(S, 0, sizeof(float) * (size_t)(B * H) * d * dv, cs);
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(z, 0, sizeof(float) * (size_t)(B * H) * d, cs);
+        return from_cuda(e);
+    }
+    if (!k || !v || !aligned16(k) || !aligned16(v))
+        return LA_ERR_INVALID_ARG;
+    const size_t need = simt_state_workspace(B * H, N, d, dv);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace))
+        return LA_ERR_WORKSPACE;
+
+    FwdArgs a{};
+    a.k = k, a.v = v;
+    a.B = B, a.H = H, a.N = N, a.d = d, a.dv = dv;
+    a.causal = 1, a.fm = feature_map, a.dtype = dtype;
+    a.gamma = &gt;
+    a.ws = workspace, a.ws_bytes = workspace_bytes;
+    a.S_out = S, a.z_out = z;
+    a.status = status_ptr();
+    a.stream = cs;
+    return from_cuda(simt_state(a));
+}
+
+la_status la_decode_step(float* S, float* z, const void* q, const void* k, const void* v,
+                         float* out, int64_t B, int64_t H, int d, int dv, int feature_map,
+                         const float* gamma, int dtype, la_stream_t stream)
+{
+    la_status st = check_sizes(B, H, 1, d, dv, feature_map, dtype);
+    if (st != LA_OK)
+        return st;
+    GammaTable gt;
+    if ((st = make_gamma(gamma, H, &gt)) != LA_OK)
+        return st;
+    if (!S || !z || !q || !k || !v || !out)
+        return LA_ERR_INVALID_ARG;
+    if (!aligned16(S) || !aligned16(z) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+        !aligned16(out))
+        return LA_ERR_INVALID_ARG;
+    DecodeArgs a{};
+    a.S = S, a.z = z, a.q = q, a.k = k, a.v = v, a.out = out;
+    a.BH = B * H, a.H = H, a.d = d, a.dv = dv, a.fm = feature_map, a.dtype = dtype;
+    a.gamma = &gt;
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    return from_cuda(decode_step(a));
+}
+
+uint64_t la_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+la_status la_get_device_status(la_stream_t stream)
+{
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return LA_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess)
+        return LA_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess)
+            return LA_ERR_CUDA;
+    }
+    return static_cast<la_status>(v);
+}
+
+}  // extern "C"
