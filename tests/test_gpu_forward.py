@@ -136,7 +136,7 @@ def test_state_matches_oracle(orc):
         Sr, zr = orc.state(to_np(k), to_np(v), fm=w.feature_map,
                            gamma=None if g is None else g.double().numpy())
         assert rel_err_rows(S, Sr) <= 1e-5
-        assert rel_err_rows(z[..., None], zr[..., None]) <= 1e-5
+        assert rel_err_rows(z, zr) <= 1e-5
 
 
 def test_output_guard_band():
