@@ -81,7 +81,9 @@ typedef enum {
     LA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed        */
     LA_ERR_TIMEOUT = 4,       /* device: a bounded wait gave up              */
     LA_ERR_DEVICE_CHECK = 5,  /* device: an internal consistency check failed */
-    LA_ERR_WORKSPACE = 6      /* workspace missing or smaller than required  */
+    LA_ERR_WORKSPACE = 6,     /* workspace missing or smaller than required  */
+    LA_ERR_TOO_LARGE = 7      /* la_forward_noalloc: the sizes need more
+                                 scratch than its fixed device array holds   */
 } la_status;
 
 typedef enum {
@@ -149,6 +151,35 @@ LA_API la_status la_state(const void* k, const void* v, float* S, float* z, int6
 LA_API la_status la_decode_step(float* S, float* z, const void* q, const void* k, const void* v,
                          float* out, int64_t B, int64_t H, int d, int dv, int feature_map,
                          const float* gamma, int dtype, la_stream_t stream);
+
+/*
+ * la_forward without a workspace argument, for callers that cannot allocate
+ * device memory (the pages have no counterpart: this is a deployment
+ * convenience).  Typical such callers are a plugin running inside a host
+ * application whose memory pool owns all device memory and forbids other
+ * allocations, and latency-critical serving code that must not call
+ * cudaMalloc / cudaFree because those calls can synchronise the whole device.
+ *
+ * Scratch comes from a fixed array of LA_NOALLOC_SCRATCH_BYTES compiled into
+ * the library's device image; every GPU that loads the library keeps that
+ * much memory reserved until the process exits.  Requests whose
+ * la_forward_workspace_size() exceeds it return LA_ERR_TOO_LARGE before
+ * anything is enqueued.  Nothing is allocated or freed by this call.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture.  All calls share the one array and it keeps
+ * the previous call's contents (the forward clears what must start at zero
+ * itself), so two calls whose work overlaps on the GPU -- on different
+ * streams, or from different host threads -- race on it and give wrong
+ * results: serialise them.  All other arguments and results are exactly
+ * those of la_forward.
+ */
+#define LA_NOALLOC_SCRATCH_BYTES (32u << 20)
+LA_API la_status la_forward_noalloc(const void* q, const void* k, const void* v, float* out,
+                                    int64_t B, int64_t H, int64_t N, int d, int dv, int causal,
+                                    int feature_map, const float* gamma, int dtype,
+                                    la_stream_t stream);
 
 /*
  * Diagnostic: total number of kernels this library has launched in this

@@ -26,7 +26,8 @@ _lib = ctypes.CDLL(str(LIB_PATH))
 
 LA_OK = 0
 STATUS_NAMES = {0: "LA_OK", 1: "LA_ERR_INVALID_ARG", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_CUDA",
-                4: "LA_ERR_TIMEOUT", 5: "LA_ERR_DEVICE_CHECK", 6: "LA_ERR_WORKSPACE"}
+                4: "LA_ERR_TIMEOUT", 5: "LA_ERR_DEVICE_CHECK", 6: "LA_ERR_WORKSPACE",
+                7: "LA_ERR_TOO_LARGE"}
 FEATURE_MAPS = {"elu1": 0, "identity_norm": 1, "none": 2}
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 
@@ -50,6 +51,9 @@ _lib.la_state.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _i, _fp,
 _lib.la_decode_step.restype = _i
 _lib.la_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _i, _i, _fp, _i,
                                 _vp]
+_lib.la_forward_noalloc.restype = _i
+_lib.la_forward_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _i, _i, _fp,
+                                    _i, _vp]
 _lib.la_launch_count.restype = ctypes.c_uint64
 _lib.la_launch_count.argtypes = []
 _lib.la_get_device_status.restype = _i
@@ -143,6 +147,25 @@ def la_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Ten
                            _fm(feature_map), gp, _dtype(q), _dev_ptr(workspace, "workspace"),
                            workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(code, "la_forward")
+    return out
+
+
+def la_forward_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
+                       *, causal: bool = True, feature_map="elu1", gamma=None,
+                       stream=None) -> torch.Tensor:
+    """la_forward with no workspace argument and no allocation anywhere: for
+    callers that cannot allocate device memory (their host application owns
+    all of it, or they must not risk the device-wide synchronisation of
+    cudaMalloc / cudaFree).  Scratch comes from a fixed device array inside the
+    library; ``out`` must be given, since creating it would allocate.  Calls
+    that overlap on the GPU share that array and race."""
+    B, H, N, d = q.shape
+    dv = v.shape[-1]
+    gp, _keep = _gamma_arg(gamma, H)
+    code = _lib.la_forward_noalloc(_dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                                   _dev_ptr(out, "out"), B, H, N, d, dv, int(bool(causal)),
+                                   _fm(feature_map), gp, _dtype(q), _stream_handle(stream))
+    _check(code, "la_forward_noalloc")
     return out
 
 

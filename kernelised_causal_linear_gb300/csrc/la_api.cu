@@ -97,6 +97,8 @@ const char* la_status_string(la_status s)
     case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT: a bounded device-side wait gave up";
     case LA_ERR_DEVICE_CHECK: return "LA_ERR_DEVICE_CHECK: a device-side consistency check failed";
     case LA_ERR_WORKSPACE: return "LA_ERR_WORKSPACE: workspace missing or too small";
+    case LA_ERR_TOO_LARGE:
+        return "LA_ERR_TOO_LARGE: sizes need more scratch than la_forward_noalloc's fixed array";
     }
     return "unknown la_status";
 }

@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings_and_version(lib):
     lib.la_status_string.restype = ctypes.c_char_p
-    for code in range(7):
+    for code in range(8):
         s = lib.la_status_string(code).decode()
         assert s.startswith("LA_")
     assert lib.la_version() >= 100
