@@ -305,7 +305,8 @@ def main():
             "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"],
             "traffic": None,
-            "kernel": "la_forward (all launches of one call)" if not decode else "k_decode_step",
+            "kernel": ("k_fwd_tc64" if la_path_dtype(w) == "bf16" else "la_forward (all launches)")
+                      if not decode else "k_decode_step",
             "peak_source": f"{peak_src} HBM copy bandwidth",
             "algorithmic_bytes_per_launch": bytes_per_launch,
         },
@@ -322,7 +323,15 @@ def main():
 
 
 def la_path_dtype(w) -> str:
-    return "f32"
+    """Arithmetic type of the path that runs: bf16 tensor-core operands with
+    fp32 accumulation on the tcgen05 kernel, fp32 on the CUDA-core paths."""
+    if w.steps > 0:
+        return "f32"
+    import kernelised_causal_linear_gb300 as la
+
+    path = la.la_forward_path(w.B, w.H, w.N, w.d, w.dv, w.causal, w.feature_map, w.decay,
+                              w.dtype)
+    return "bf16" if path == "tcgen05" else "f32"
 
 
 def run_e2e(la, w, decode, steps, stream, world, out, env):

@@ -127,6 +127,15 @@ LA_API la_status la_forward(const void* q, const void* k, const void* v, float* 
                      const float* gamma, int dtype, void* workspace, size_t workspace_bytes,
                      la_stream_t stream);
 
+/*
+ * Diagnostic: the kernel path la_forward takes for these arguments --
+ * "tcgen05" (the tensor-core single-pass kernel: bf16, d = dv = 64, causal,
+ * no decay) or "simt" (CUDA cores, fp32, every other case); "invalid" for
+ * arguments la_forward would reject.  has_decay: 1 if gamma will be non-NULL.
+ */
+LA_API const char* la_forward_path(int64_t B, int64_t H, int64_t N, int d, int dv, int causal,
+                                   int feature_map, int has_decay, int dtype);
+
 /* Bytes of device workspace la_state needs (0 for N = 0). */
 LA_API size_t la_state_workspace_size(int64_t B, int64_t H, int64_t N, int d, int dv, int dtype);
 

@@ -54,6 +54,8 @@ _lib.la_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _i
 _lib.la_forward_noalloc.restype = _i
 _lib.la_forward_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _i, _i, _fp,
                                     _i, _vp]
+_lib.la_forward_path.restype = ctypes.c_char_p
+_lib.la_forward_path.argtypes = [_i64, _i64, _i64, _i, _i, _i, _i, _i, _i]
 _lib.la_launch_count.restype = ctypes.c_uint64
 _lib.la_launch_count.argtypes = []
 _lib.la_get_device_status.restype = _i
@@ -205,6 +207,12 @@ def la_decode_step(S: torch.Tensor, z: torch.Tensor, q: torch.Tensor, k: torch.T
                                dv, _fm(feature_map), gp, _dtype(q), _stream_handle(stream))
     _check(code, "la_decode_step")
     return out
+
+
+def la_forward_path(B, H, N, d, dv, causal=True, feature_map="elu1", has_decay=False,
+                    dtype=torch.bfloat16) -> str:
+    return _lib.la_forward_path(B, H, N, d, dv, int(bool(causal)), _fm(feature_map),
+                                int(bool(has_decay)), DTYPES[dtype]).decode()
 
 
 def la_launch_count() -> int:

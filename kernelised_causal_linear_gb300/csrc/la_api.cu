@@ -103,12 +103,34 @@ const char* la_status_string(la_status s)
     return "unknown la_status";
 }
 
+// Which kernel path serves a forward: the tcgen05 kernel where it applies,
+// else the CUDA-core path.
+static bool use_tc(int64_t N, int d, int dv, int causal, int has_decay, int dtype)
+{
+    FwdArgs a{};
+    GammaTable g{};
+    g.has_decay = has_decay;
+    a.N = N, a.d = d, a.dv = dv, a.causal = causal, a.dtype = dtype, a.gamma = &g;
+    return tc_forward_eligible(a);
+}
+
 size_t la_forward_workspace_size(int64_t B, int64_t H, int64_t N, int d, int dv, int causal,
                                  int dtype)
 {
-    if (check_sizes(B, H, N, d, dv, LA_FM_ELU1, dtype) != LA_OK)
+    if (check_sizes(B, H, N, d, dv, LA_FM_ELU1, dtype) != LA_OK || N == 0)
         return 0;
-    return simt_forward_workspace(B * H, N, d, dv, causal);
+    size_t n = simt_forward_workspace(B * H, N, d, dv, causal);
+    if (use_tc(N, d, dv, causal, 0, dtype))  // gamma unknown here: cover both paths
+        n = n > tc_forward_workspace(B * H, N) ? n : tc_forward_workspace(B * H, N);
+    return n;
+}
+
+const char* la_forward_path(int64_t B, int64_t H, int64_t N, int d, int dv, int causal,
+                            int feature_map, int has_decay, int dtype)
+{
+    if (check_sizes(B, H, N, d, dv, feature_map, dtype) != LA_OK)
+        return "invalid";
+    return use_tc(N, d, dv, causal, has_decay, dtype) ? "tcgen05" : "simt";
 }
 
 size_t la_state_workspace_size(int64_t B, int64_t H, int64_t N, int d, int dv, int dtype)
@@ -139,10 +161,6 @@ la_status la_forward(const void* q, const void* k, const void* v, float* out, in
         return LA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return LA_ERR_INVALID_ARG;
-    const size_t need = simt_forward_workspace(B * H, N, d, dv, causal);
-    if (!workspace || workspace_bytes < need || !aligned16(workspace))
-        return LA_ERR_WORKSPACE;
-
     FwdArgs a{};
     a.q = q, a.k = k, a.v = v, a.out = out;
     a.B = B, a.H = H, a.N = N, a.d = d, a.dv = dv;
@@ -151,7 +169,12 @@ la_status la_forward(const void* q, const void* k, const void* v, float* out, in
     a.ws = workspace, a.ws_bytes = workspace_bytes;
     a.status = status_ptr();
     a.stream = reinterpret_cast<cudaStream_t>(stream);
-    return from_cuda(simt_forward(a));
+    const bool tc = tc_forward_eligible(a);
+    const size_t need = tc ? tc_forward_workspace(B * H, N)
+                           : simt_forward_workspace(B * H, N, d, dv, causal);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace))
+        return LA_ERR_WORKSPACE;
+    return from_cuda(tc ? tc_forward(a) : simt_forward(a));
 }
 
 la_status la_state(const void* k, const void* v, float* S, float* z, int64_t B, int64_t H,

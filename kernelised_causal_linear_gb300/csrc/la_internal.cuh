@@ -91,6 +91,11 @@ size_t simt_state_workspace(int64_t BH, int64_t N, int d, int dv);
 cudaError_t simt_forward(const FwdArgs& a);
 cudaError_t simt_state(const FwdArgs& a);
 
+// tcgen05 / TMA single-pass causal forward (bf16, d = dv = 64, no decay)
+bool tc_forward_eligible(const FwdArgs& a);
+size_t tc_forward_workspace(int64_t BH, int64_t N);
+cudaError_t tc_forward(const FwdArgs& a);
+
 struct DecodeArgs {
     float* S;
     float* z;
