@@ -98,7 +98,7 @@ struct Misc {
     int abort;
     int pad[3];
     int list[kMaxList];
-    float zprev[kD];
+    alignas(16) float zprev[kD];
     float dzpart[4][kD];
 };
 static_assert(sizeof(Misc) <= 2048, "misc");
@@ -235,6 +235,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_fwd_tc64(const __grid_constant_
         }
         if (!ok)
             atomicExch(&ms->abort, 1);
+        if (tid == 0)
+            bulk_wait_read<0>();  // the previous output tile has left the staging buffer
 
         // ---- feature map in place, ragged rows zeroed, column sums of phi(K)
         {
@@ -302,30 +304,36 @@ __global__ void __launch_bounds__(kThreads, 2) k_fwd_tc64(const __grid_constant_
             mma_bar = -1;
         tc_fence_after();
 
-        // ---- publish the aggregate: dS^T rows (warps 0,1), dz (warps 2,3)
-        float dz_mine = 0.f;
+        // ---- dS^T (tensor-memory lanes 0..63 -> warps 0,1) and dz into a shared
+        // copy (the output staging buffer is idle until the epilogue), then the
+        // whole CTA writes the aggregate slot with coalesced stores
+        float* sDS = reinterpret_cast<float*>(sO);  // [64][64] then z[64]
         float* agg = slot_base + static_cast<size_t>(my_slot) * kSlotFloats;
         if (warp < 2) {
-            float ds[kD];
-            uint32_t r[16];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
+                uint32_t r[16];
                 tmem_ld16(tS + 16 * q, r);
                 tmem_ld_wait();
+                float4* d4 = reinterpret_cast<float4*>(sDS + tid * kD + 16 * q);
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    ds[16 * q + j] = __uint_as_float(r[j]);
+                for (int u = 0; u < 4; ++u)
+                    d4[u] = make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                                        __uint_as_float(r[4 * u + 2]),
+                                        __uint_as_float(r[4 * u + 3]));
             }
-            float4* dst = reinterpret_cast<float4*>(agg + tid * kD);
-#pragma unroll
-            for (int q = 0; q < 16; ++q)
-                __stcg(dst + q, make_float4(ds[4 * q], ds[4 * q + 1], ds[4 * q + 2], ds[4 * q + 3]));
         } else {
             const int i = tid - 64;
-            dz_mine = ms->dzpart[0][i] + ms->dzpart[1][i] + ms->dzpart[2][i] + ms->dzpart[3][i];
-            __stcg(agg + kD * kD + i, dz_mine);
+            sDS[kD * kD + i] =
+                ms->dzpart[0][i] + ms->dzpart[1][i] + ms->dzpart[2][i] + ms->dzpart[3][i];
         }
-        __threadfence();
+        __syncthreads();
+        {
+            const float4* src = reinterpret_cast<const float4*>(sDS);
+            float4* dst = reinterpret_cast<float4*>(agg);
+            for (int f = tid; f < kStateFloats / 4; f += kThreads)
+                __stcg(dst + f, src[f]);
+        }
 
         // ---- P: causal mask, row sums, bf16 hi/lo re-packed in place
         float den = 0.f;
@@ -360,10 +368,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_fwd_tc64(const __grid_constant_
         tc_fence_before();
         __syncthreads();
 
-        // ---- flag the aggregate, MMA 2 (P V), look-back
+        // ---- flag the aggregate, MMA 2 (P V), look-back over the predecessors
         if (tid == 0) {
-            tc_fence_after();
+            __threadfence();
             st_release(flag_base + my_slot, (static_cast<unsigned>(c + 1) << 2) | 1u);
+            tc_fence_after();
             const uint32_t id_pv = idesc_bf16_f32(128, 64, false, true);
 #pragma unroll
             for (int k = 0; k < 8; ++k)
@@ -375,54 +384,84 @@ __global__ void __launch_bounds__(kThreads, 2) k_fwd_tc64(const __grid_constant_
                             sdesc_sw128(smem_addr(sV) + 2048 * k, 16, 1024), id_pv, 1);
             mma_commit(&ms->bar[3]);
             mma_bar = 3, mma_par = ph;
-
+        }
+        if (warp == 0) {
+            // Lane l watches chunk base - l.  The list collects, newest first, the
+            // aggregates back to the nearest inclusive prefix (or the sequence start).
+            // Window of W lanes: with a wrapping ring only R-1 slots behind this
+            // chunk are distinct from its own.  A slot that holds another epoch
+            // (older: not yet written; newer: reused after a later inclusive
+            // prefix made it unnecessary) reads as not ready.
+            const int W = p.R >= p.nchunk ? 32 : min(32, p.R - 1);
+            const unsigned active = W >= 32 ? 0xffffffffu : ((1u << W) - 1u);
             int n = 0;
-            for (int pc = c - 1; pc >= 0 && n >= 0; --pc) {
-                const unsigned want = static_cast<unsigned>(pc + 1);
-                const int sl = pc % p.R;
-                unsigned f = ld_acquire(flag_base + sl);
-                uint64_t start = 0;
-                while ((f >> 2) != want || (f & 3u) == 0u) {
-                    if ((f >> 2) > want) {  // slot reused too early: never expected
+            int base = c - 1;
+            uint64_t start = 0;
+            const unsigned full = 0xffffffffu;
+            while (base >= 0) {
+                const int pc = base - lane;
+                bool ready = true, incl = true;
+                if (lane >= W) {
+                    ready = incl = false;
+                } else if (pc >= 0) {
+                    const unsigned f = ld_acquire(flag_base + pc % p.R);
+                    ready = (f >> 2) == static_cast<unsigned>(pc + 1) && (f & 3u) != 0u;
+                    incl = ready && (f & 3u) == 2u;
+                }
+                const unsigned mi = __ballot_sync(full, incl) & active;
+                const unsigned mr = __ballot_sync(full, ready) & active;
+                if (mi) {
+                    const int ls = __ffs(mi) - 1;
+                    const unsigned need = ls == 0 ? 0u : ((1u << ls) - 1u);
+                    if ((mr & need) == need) {
+                        if (n + ls + 1 > kMaxList) {
+                            n = -2;
+                            break;
+                        }
+                        if (lane < ls)
+                            ms->list[n + lane] = (pc % p.R) << 1;
+                        if (lane == ls && pc >= 0)
+                            ms->list[n + lane] = ((pc % p.R) << 1) | 1;
+                        n += ls + (base - ls >= 0 ? 1 : 0);
+                        break;
+                    }
+                } else if (mr == active) {
+                    if (n + W > kMaxList) {
                         n = -2;
                         break;
                     }
-                    const uint64_t now = globaltimer();
-                    if (!start)
-                        start = now;
-                    else if (now - start > kLookbackNs) {
-                        n = -1;
-                        break;
-                    }
-                    __nanosleep(100);
-                    f = ld_acquire(flag_base + sl);
+                    if (lane < W)
+                        ms->list[n + lane] = (pc % p.R) << 1;
+                    n += W;
+                    base -= W;
+                    start = 0;
+                    continue;
                 }
+                const uint64_t now = globaltimer();
+                if (!start)
+                    start = now;
+                else if (now - start > kLookbackNs) {
+                    n = -1;
+                    break;
+                }
+                __nanosleep(64);
+            }
+            if (lane == 0) {
+                ms->nlist = n;
                 if (n < 0)
-                    break;
-                const bool incl = (f & 3u) == 2u;
-                if (n >= kMaxList) {
-                    n = -2;
-                    break;
+                    set_status(p.status, n == -1 ? LA_ERR_TIMEOUT : LA_ERR_DEVICE_CHECK);
+                // K, V are free once P V is done: start the next chunk's K, V
+                if (mbar_wait(&ms->bar[3], ph, kPollLimit)) {
+                    mma_bar = -1;
+                    if (ms->next < p.total) {
+                        issue_loads(p, sm, ms, ms->next, true, false, pol);
+                        kv_pending = true;
+                    }
+                } else {
+                    ms->nlist = -1;
+                    set_status(p.status, LA_ERR_TIMEOUT);
                 }
-                ms->list[n++] = (sl << 1) | (incl ? 1 : 0);
-                if (incl)
-                    break;
             }
-            ms->nlist = n;
-            if (n < 0)
-                set_status(p.status, n == -1 ? LA_ERR_TIMEOUT : LA_ERR_DEVICE_CHECK);
-            // K, V are free once P V is done: start the next chunk's K, V
-            if (mbar_wait(&ms->bar[3], ph, kPollLimit)) {
-                mma_bar = -1;
-                if (ms->next < p.total) {
-                    issue_loads(p, sm, ms, ms->next, true, false, pol);
-                    kv_pending = true;
-                }
-            } else {
-                ms->nlist = -1;
-                set_status(p.status, LA_ERR_TIMEOUT);
-            }
-            bulk_wait_read<0>();  // the previous output tile has left the staging buffer
         }
         __syncthreads();
         const int nlist = ms->nlist;
@@ -431,69 +470,62 @@ __global__ void __launch_bounds__(kThreads, 2) k_fwd_tc64(const __grid_constant_
             break;
         }
 
-        // ---- S_prev, z_prev: nearest inclusive prefix, then later aggregates in order
-        if (warp < 2) {
-            float sp[kD];
+        // ---- S_prev, z_prev: the nearest inclusive prefix plus the later
+        // aggregates in chunk order (a fixed left-to-right fp32 sum).  Thread t
+        // owns float4 words t + 128 m of the state; threads 0..15 also z.
+        {
+            float4 acc[9];
 #pragma unroll
-            for (int j = 0; j < kD; ++j)
-                sp[j] = 0.f;
+            for (int m = 0; m < 9; ++m)
+                acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int e = nlist - 1; e >= 0; --e) {
                 const int ent = ms->list[e];
                 const float4* src = reinterpret_cast<const float4*>(
                     slot_base + static_cast<size_t>(ent >> 1) * kSlotFloats +
-                    ((ent & 1) ? kStateFloats : 0) + tid * kD);
+                    ((ent & 1) ? kStateFloats : 0));
+                float4 x[9];
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const float4 x = __ldcg(src + q);
-                    sp[4 * q] += x.x, sp[4 * q + 1] += x.y, sp[4 * q + 2] += x.z, sp[4 * q + 3] += x.w;
+                for (int m = 0; m < 8; ++m)
+                    x[m] = __ldcg(src + tid + 128 * m);
+                x[8] = tid < 16 ? __ldcg(src + 1024 + tid) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int m = 0; m < 9; ++m) {
+                    acc[m].x += x[m].x, acc[m].y += x[m].y;
+                    acc[m].z += x[m].z, acc[m].w += x[m].w;
                 }
             }
-            // S_prev^T row `tid` as bf16 hi/lo (K-major B operand of phi(Q) S_prev)
+            const float4* ds4 = reinterpret_cast<const float4*>(sDS);
+            float4* inc = reinterpret_cast<float4*>(agg + kStateFloats);
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-                uint4 h, l;
-                split2(sp[8 * cc + 0], sp[8 * cc + 1], h.x, l.x);
-                split2(sp[8 * cc + 2], sp[8 * cc + 3], h.y, l.y);
-                split2(sp[8 * cc + 4], sp[8 * cc + 5], h.z, l.z);
-                split2(sp[8 * cc + 6], sp[8 * cc + 7], h.w, l.w);
-                *reinterpret_cast<uint4*>(sShi + sw128_off(tid, cc)) = h;
-                *reinterpret_cast<uint4*>(sSlo + sw128_off(tid, cc)) = l;
+            for (int m = 0; m < 8; ++m) {
+                const int f = tid + 128 * m;
+                const int row = f >> 4, col4 = f & 15;  // S_prev^T row (value channel), 4 features
+                uint2 h, l;
+                split2(acc[m].x, acc[m].y, h.x, l.x);
+                split2(acc[m].z, acc[m].w, h.y, l.y);
+                const uint32_t off = sw128_off(row, col4 >> 1) + (col4 & 1) * 8;
+                *reinterpret_cast<uint2*>(sShi + off) = h;
+                *reinterpret_cast<uint2*>(sSlo + off) = l;
+                const float4 d = ds4[f];
+                __stcg(inc + f, make_float4(acc[m].x + d.x, acc[m].y + d.y, acc[m].z + d.z,
+                                            acc[m].w + d.w));
             }
-            // inclusive prefix = S_prev + dS (dS^T row re-read from tensor memory)
-            float4* inc = reinterpret_cast<float4*>(agg + kStateFloats + tid * kD);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t r[16];
-                tmem_ld16(tS + 16 * q, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    __stcg(inc + 4 * q + u,
-                           make_float4(sp[16 * q + 4 * u] + __uint_as_float(r[4 * u]),
-                                       sp[16 * q + 4 * u + 1] + __uint_as_float(r[4 * u + 1]),
-                                       sp[16 * q + 4 * u + 2] + __uint_as_float(r[4 * u + 2]),
-                                       sp[16 * q + 4 * u + 3] + __uint_as_float(r[4 * u + 3])));
+            if (tid < 16) {
+                reinterpret_cast<float4*>(ms->zprev)[tid] = acc[8];
+                const float4 d = ds4[1024 + tid];
+                __stcg(inc + 1024 + tid, make_float4(acc[8].x + d.x, acc[8].y + d.y,
+                                                     acc[8].z + d.z, acc[8].w + d.w));
             }
-        } else {
-            const int i = tid - 64;
-            float zp = 0.f;
-            for (int e = nlist - 1; e >= 0; --e) {
-                const int ent = ms->list[e];
-                zp += __ldcg(slot_base + static_cast<size_t>(ent >> 1) * kSlotFloats +
-                             ((ent & 1) ? kStateFloats : 0) + kD * kD + i);
-            }
-            ms->zprev[i] = zp;
-            __stcg(agg + kStateFloats + kD * kD + i, zp + dz_mine);
         }
-        __threadfence();
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
 
         // ---- flag the inclusive prefix, MMA 3 (phi(Q) S_prev, hi and lo)
         if (tid == 0) {
-            tc_fence_after();
+            __threadfence();
             st_release(flag_base + my_slot, (static_cast<unsigned>(c + 1) << 2) | 2u);
+            tc_fence_after();
             if (nlist > 0) {
                 const uint32_t id_in = idesc_bf16_f32(128, 64, false, false);
 #pragma unroll
