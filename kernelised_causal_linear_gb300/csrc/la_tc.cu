@@ -18,37 +18,45 @@
 // is the only intermediate; "Efficient Attention Variants", section 5: the
 // prefix state S_t, z_t and the normalised read).
 //
-// Chunks are taken in ticket order (chunk-major over the B*H sequences) by one
-// persistent CTA per SM.  The state entering a chunk comes from a decoupled
-// look-back over a small ring of per-chunk slots in global memory (it stays in
-// L2): each chunk publishes its aggregate (dS_c, dz_c) as soon as its first
-// MMAs finish, then its inclusive prefix.  The look-back starts from the
-// nearest inclusive prefix and adds the later aggregates in chunk order, so
-// every prefix is the same left-to-right fp32 sum whatever the timing: the
-// results are bitwise reproducible.
+// Chunks are grouped into segments of L consecutive chunks of one sequence.
+// One persistent CTA per SM takes segments in ticket order (segment-major over
+// the B*H sequences) and runs each in two phases:
+//   A  the segment's aggregate: K, V of every chunk (kept in L2 with an
+//      evict-last hint), phi(K), dS accumulated on the tensor cores, dz;
+//      published at once to a ring of per-segment slots in global memory;
+//   C  the outputs: Q, K, V again (K, V from L2), with the running state
+//      S_prev = S_in + the segment's earlier chunks carried in tensor memory.
+// Between them a decoupled look-back over the predecessors' slots gives S_in,
+// the state before the segment, and publishes the segment's inclusive prefix.
+// Phase A of segment j+1 runs before phase C of segment j, so the look-back
+// of segment j is hidden behind it.  The look-back starts from the nearest
+// inclusive prefix and adds later aggregates in segment order, so every
+// prefix is the same left-to-right fp32 sum whatever the timing: results are
+// bitwise reproducible.
 //
-// The CTA is warp-specialised; chunks flow through rings of shared-memory
-// stages and double-buffered tensor memory, synchronised by mbarriers:
-//   warp 0      producer: tickets, TMA loads of Q and of K, V
-//   warp 1      MMA issuer: scores + chunk state, P V, phi(Q) S_prev
-//   warp 2      look-back over the predecessors' flags (needs only the ticket,
-//               so it runs ahead of the chunk's own arithmetic)
-//   warps 4-7   feature map in place, column sums of phi(K); P: causal mask,
-//               row sums, bf16 hi/lo re-pack in tensor memory
-//   warps 8-11  chunk state out of tensor memory, aggregate and inclusive
-//               prefix publishing, S_prev hi/lo for the tensor cores
-//   warps 12-15 epilogue: denominator, output tile by TMA store
+// The CTA is warp-specialised; work flows through rings of shared-memory
+// stages and tensor-memory buffers, synchronised by mbarriers:
+//   warp 0      producer: segment tickets, TMA loads
+//   warp 1      MMA issuer: segment aggregate, scores, chunk state, P V,
+//               phi(Q) S_prev
+//   warps 2-3   look-back over the predecessors' slots, S_in, inclusive prefix
+//   warps 4-7   phi(K) in place and its column sums (phases A and C); P:
+//               causal mask, row sums, bf16 hi/lo re-pack in tensor memory
+//   warps 8-11  segment aggregate out of tensor memory and published; running
+//               state S_prev as bf16 hi/lo for the tensor cores, z_prev
+//   warps 12-15 phi(Q) in place (one chunk ahead), epilogue: denominator,
+//               output tile by TMA store
 //
 // Precision: phi(Q), phi(K) and V enter the MMAs as bf16 (phi rounded once);
 // P and S_prev are fp32 and enter as a bf16 hi/lo pair (two MMAs each), so
-// their rounding is ~2^-17 relative; denominators stay in fp32.
+// their rounding is ~2^-17 relative; states and denominators stay fp32.
 //
 // Operands: Q, K, V chunks arrive by TMA in the 128-byte swizzled layout.
-// The scores MMA reads Q and K K-major; the chunk-state MMA reads [V | phi(K)]
-// as an MN-major A of 128 rows (the second 64 rows are discarded) against
-// phi(K) MN-major, giving dS^T in lanes 0..63; P's hi/lo parts sit in tensor
-// memory as the A operand of P V; S_prev^T hi/lo sit in shared memory
-// K-major for phi(Q) S_prev.
+// The scores MMA reads Q and K K-major; the state MMAs read [V | phi(K)] as an
+// MN-major A of 128 rows (the second 64 rows are discarded) against phi(K)
+// MN-major, giving dS^T in lanes 0..63; P's hi/lo parts sit in tensor memory
+// as the A operand of P V; S_prev^T hi/lo sit in shared memory K-major for
+// phi(Q) S_prev.
 //
 // Every wait is bounded (%globaltimer); on expiry the CTA records
 // LA_ERR_TIMEOUT, every role leaves its loop, the CTA drains its own TMA loads,
@@ -71,8 +79,8 @@ constexpr int kC = 128;        // tokens per chunk
 constexpr int kD = 64;         // d = dv
 constexpr int kThreads = 512;  // 16 warps
 constexpr int NQ = 3;          // Q stages
-constexpr int NKV = 2;         // K,V stages
-constexpr int NT = 4;          // ticket ring
+constexpr int NKV = 3;         // K,V stages
+constexpr int NS = 4;          // segment-ticket ring
 constexpr int kStateFloats = kD * kD + kD;         // S^T (dv x d) then z (d)
 constexpr int kSlotFloats = 2 * kStateFloats;      // aggregate, inclusive
 constexpr int kMaxList = 128;                      // look-back entries
@@ -83,46 +91,54 @@ constexpr uint32_t OFF_Q = 0;                          // NQ x (128 x 64 bf16)
 constexpr uint32_t OFF_KV = OFF_Q + NQ * 16384;        // NKV x (V then K)
 constexpr uint32_t OFF_S = OFF_KV + NKV * 32768;       // 2 x (S^T hi, S^T lo)
 constexpr uint32_t OFF_O = OFF_S + 2 * 16384;          // output staging 2 x 16 KiB
-constexpr uint32_t OFF_DS = OFF_O + 32768;             // dS^T, dz fp32 copy
-constexpr uint32_t OFF_MISC = OFF_DS + 17408;
-constexpr uint32_t kMiscBytes = 6144;
+constexpr uint32_t OFF_MISC = OFF_O + 32768;
+constexpr uint32_t kMiscBytes = 8192;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + kMiscBytes + 1024;  // + alignment slack
 
 // tensor memory columns
-constexpr uint32_t TM_P = 0;      // scores fp32, 128 columns
-constexpr uint32_t TM_PHL = 128;  // P hi (128..191), P lo (192..255), bf16 pairs
-constexpr uint32_t TM_O = 256;    // 2 x 64: output accumulators
-constexpr uint32_t TM_DS = 384;   // 2 x 64: dS^T (lanes 0..63)
+constexpr uint32_t TM_P = 0;       // scores fp32, 128 columns
+constexpr uint32_t TM_PHL = 128;   // P hi (128..191), P lo (192..255), bf16 pairs
+constexpr uint32_t TM_O = 256;     // 2 x 64: output accumulators
+constexpr uint32_t TM_SRUN = 384;  // running S_prev^T (lanes 0..63)
+constexpr uint32_t TM_DSEG = 448;  // segment aggregate dS^T (lanes 0..63)
 
 struct TcParams {
     CUtensorMap mq, mk, mv, mo;
     int64_t N;
     int BH;
-    int nchunk;
+    int nchunk;   // chunks per sequence
+    int L;        // chunks per segment
+    int nseg;     // segments per sequence
     int R;        // ring slots per sequence
-    int total;    // BH * nchunk
+    int total;    // BH * nseg segment tickets
     int fm;
     unsigned* counter;
     unsigned* flags;
     float* slots;
+    float* sin_scratch;  // per CTA: 2 x S_in
     int* status;
 };
 
 struct Misc {
-    uint64_t tick_full[NT], tick_empty[NT];
-    uint64_t q_full[NQ], q_empty[NQ];
-    uint64_t kv_full[NKV], kv_empty[NKV];
-    uint64_t phi_done[2], mma1_done[2], p_ready[2], pv_done[2], ds_free[2], s_ready[2];
-    uint64_t o_done[2], o_free[2], list_full[2], list_empty[2], epi_done[2];
+    uint64_t seg_full[NS], seg_empty[NS];
+    uint64_t q_full[NQ], q_empty[NQ], q_phi[NQ];
+    uint64_t kv_full[NKV], kv_empty[NKV], kv_phi[NKV];
+    uint64_t mma1_done[2], p_ready[2], pv_done[2], srun_read[2], o_done[2], o_free[2];
+    uint64_t epi_done[2], dzc_ready[2];
+    uint64_t dseg_done, dseg_free, dzseg_ready[2], agg_pub[2], sin_ready[2], sin_free[2];
     uint64_t drain;
     uint32_t tmem;
     int abort;
-    int ticket[NT];
-    int nlist[2];
-    int list[2][kMaxList];
+    int seg_ticket[NS];
+    int nlist;
+    int list[kMaxList];
     float den[2][kC];
     alignas(16) float zprev[2][kD];
-    float dzpart[2][4][kD];
+    float zrun[kD];
+    float dzc[2][4][kD];     // per C chunk: column sums of phi(K), one row per warp
+    float dza[4][kD];        // per A chunk: the same
+    float dzacc[kD];         // running column sums over the current A segment
+    float dzseg[2][kD];
 };
 static_assert(sizeof(Misc) <= kMiscBytes, "misc");
 
@@ -130,9 +146,9 @@ static_assert(sizeof(Misc) <= kMiscBytes, "misc");
 // in builds with LA_TC_TRACE defined, never in the library as shipped.
 #ifdef LA_TC_TRACE
 __device__ unsigned long long* g_tc_trace;
-#define TC_TRACE(i, ev)                                                                  \
-    do {                                                                                 \
-        if (g_tc_trace && (i) < 64)                                                      \
+#define TC_TRACE(i, ev)                                                                       \
+    do {                                                                                      \
+        if (g_tc_trace && (i) < 64)                                                           \
             g_tc_trace[(static_cast<size_t>(blockIdx.x) * 64 + (i)) * 16 + (ev)] = clock64(); \
     } while (0)
 #else
@@ -160,9 +176,9 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p)
     return v;
 }
 
-__device__ __forceinline__ void named_bar(int id)
+__device__ __forceinline__ void named_bar(int id, int count)
 {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(128) : "memory");
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Bounded wait that also gives up as soon as another role has aborted.
@@ -186,16 +202,16 @@ __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile i
     }
 }
 
-// A 128-thread group waits through one leader; bar.red hands every thread
-// the same verdict, so the group never splits on an abort.
-__device__ __forceinline__ bool group_ok(int ok, int barid)
+// A thread group waits through one leader; bar.red hands every thread the
+// same verdict, so the group never splits on an abort.
+__device__ __forceinline__ bool group_ok(int ok, int barid, int count)
 {
     int res;
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %1, 0;\n\t"
-        "bar.red.and.pred p, %2, 128, p;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        "bar.red.and.pred p, %2, %3, p;\n\tselp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(res)
-        : "r"(ok), "r"(barid)
+        : "r"(ok), "r"(barid), "r"(count)
         : "memory");
     return res != 0;
 }
@@ -212,13 +228,12 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity)
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// elu(x)+1 on two packed bf16, rounded back to bf16
+// elu(x)+1 on two packed bf16, rounded back to bf16: max(x,0) + exp(min(x,0))
 __device__ __forceinline__ uint32_t phi2(uint32_t w)
 {
-    float a = bf_lo(w), b = bf_hi(w);
-    a = a > 0.f ? a + 1.f : __expf(a);
-    b = b > 0.f ? b + 1.f : __expf(b);
-    return pack_bf16x2(a, b);
+    const float a = bf_lo(w), b = bf_hi(w);
+    return pack_bf16x2(fmaxf(a, 0.f) + __expf(fminf(a, 0.f)),
+                       fmaxf(b, 0.f) + __expf(fminf(b, 0.f)));
 }
 
 // split two fp32 into packed bf16 hi and lo parts
@@ -226,6 +241,75 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
 {
     hi = pack_bf16x2(a, b);
     lo = pack_bf16x2(a - bf_lo(hi), b - bf_hi(hi));
+}
+
+// Feature map in place on a 128 x 64 bf16 tile (128-byte swizzle) by 128
+// threads; rows >= valid become zero.  With zsum, also the column sums of the
+// result: zsum[warp][64] (rows of this warp's threads only).
+__device__ __forceinline__ void phi_tile(unsigned char* tile, int t, int valid, bool elu,
+                                         float (*zsum)[kD])
+{
+    const int cc = t & 7, r0 = t >> 3;
+    uint4 x[8];
+#pragma unroll
+    for (int mm = 0; mm < 8; ++mm)
+        x[mm] = *reinterpret_cast<const uint4*>(tile + sw128_off(r0 + 16 * mm, cc));
+#pragma unroll
+    for (int mm = 0; mm < 8; ++mm) {
+        const int r = r0 + 16 * mm;
+        if (r >= valid)
+            x[mm] = make_uint4(0, 0, 0, 0);
+        else if (elu)
+            x[mm] = make_uint4(phi2(x[mm].x), phi2(x[mm].y), phi2(x[mm].z), phi2(x[mm].w));
+        if (r >= valid || elu)
+            *reinterpret_cast<uint4*>(tile + sw128_off(r, cc)) = x[mm];
+    }
+    if (zsum) {
+        float zp[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            zp[e] = 0.f;
+#pragma unroll
+        for (int mm = 0; mm < 8; ++mm) {
+            zp[0] += bf_lo(x[mm].x), zp[1] += bf_hi(x[mm].x);
+            zp[2] += bf_lo(x[mm].y), zp[3] += bf_hi(x[mm].y);
+            zp[4] += bf_lo(x[mm].z), zp[5] += bf_hi(x[mm].z);
+            zp[6] += bf_lo(x[mm].w), zp[7] += bf_hi(x[mm].w);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            zp[e] += __shfl_xor_sync(0xffffffffu, zp[e], 8);
+            zp[e] += __shfl_xor_sync(0xffffffffu, zp[e], 16);
+        }
+        if ((t & 31) < 8)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                zsum[(t >> 5) & 3][8 * cc + e] = zp[e];
+    }
+}
+
+// Segment helpers
+struct Seg {
+    int t;       // ticket
+    int s;       // sequence
+    int c0;      // first chunk
+    int n;       // chunks in this segment
+};
+
+__device__ __forceinline__ Seg seg_of(const TcParams& p, int t)
+{
+    Seg g;
+    g.t = t;
+    const int gi = t / p.BH;
+    g.s = t % p.BH;
+    g.c0 = gi * p.L;
+    g.n = min(p.L, p.nchunk - g.c0);
+    return g;
+}
+
+__device__ __forceinline__ int chunk_valid(const TcParams& p, int c)
+{
+    return static_cast<int>(min(static_cast<int64_t>(kC), p.N - static_cast<int64_t>(c) * kC));
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant__ TcParams p)
@@ -251,6 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
         tma_prefetch_desc(&p.mv);
         tma_prefetch_desc(&p.mo);
     }
+    if (tid < kD)
+        m->dzacc[tid] = 0.f;
     if (warp == 0) {
         tmem_alloc(&m->tmem, 512);
         tmem_relinquish();
@@ -264,38 +350,59 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
     if (warp == 0) {
         // ------------------------------------------------------ producer --
         if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
+            const uint64_t keep = policy_evict_last();
+            const uint64_t stream = policy_evict_first();
             int q_last[NQ], kv_last[NKV];
             for (int j = 0; j < NQ; ++j)
                 q_last[j] = -1;
             for (int j = 0; j < NKV; ++j)
                 kv_last[j] = -1;
-            for (int i = 0;; ++i) {
-                const int t = static_cast<int>(atomicAdd(p.counter, 1u));
-                const int ts = i % NT;
-                if (i >= NT && !bwait(&m->tick_empty[ts], ((i / NT) & 1) ^ 1, abort))
-                    break;
-                m->ticket[ts] = t;
-                mbar_arrive(&m->tick_full[ts]);
-                TC_TRACE(i, 0);
-                if (t >= p.total)
-                    break;
-                const int c = t / p.BH, s = t % p.BH;
-                const int qs = i % NQ, ks = i % NKV;
-                if (i >= NQ && !bwait(&m->q_empty[qs], ((i / NQ) & 1) ^ 1, abort))
-                    break;
-                mbar_arrive_expect_tx(&m->q_full[qs], kC * kD * 2);
-                tma_load_3d(sm + OFF_Q + qs * 16384, &p.mq, 0, c * kC, s, &m->q_full[qs], pol);
-                q_last[qs] = i / NQ;
-                TC_TRACE(i, 1);
-                if (i >= NKV && !bwait(&m->kv_empty[ks], ((i / NKV) & 1) ^ 1, abort))
-                    break;
+            int kvi = 0, ci = 0, prev = -1;
+            bool ok = true;
+            auto load_kv = [&](const Seg& g, int c, uint64_t pol) -> bool {
+                const int ks = kvi % NKV;
+                if (kvi >= NKV && !bwait(&m->kv_empty[ks], ((kvi / NKV) & 1) ^ 1, abort))
+                    return false;
                 mbar_arrive_expect_tx(&m->kv_full[ks], 2 * kC * kD * 2);
                 unsigned char* kv = sm + OFF_KV + ks * 32768;
-                tma_load_3d(kv + 16384, &p.mk, 0, c * kC, s, &m->kv_full[ks], pol);
-                tma_load_3d(kv, &p.mv, 0, c * kC, s, &m->kv_full[ks], pol);
-                kv_last[ks] = i / NKV;
-                TC_TRACE(i, 2);
+                tma_load_3d(kv + 16384, &p.mk, 0, c * kC, g.s, &m->kv_full[ks], pol);
+                tma_load_3d(kv, &p.mv, 0, c * kC, g.s, &m->kv_full[ks], pol);
+                kv_last[ks] = kvi / NKV;
+                ++kvi;
+                return true;
+            };
+            for (int j = 0; ok; ++j) {
+                const int t = static_cast<int>(atomicAdd(p.counter, 1u));
+                const int ss = j % NS;
+                if (j >= NS && !bwait(&m->seg_empty[ss], ((j / NS) & 1) ^ 1, abort))
+                    break;
+                m->seg_ticket[ss] = t;
+                mbar_arrive(&m->seg_full[ss]);
+                if (t < p.total) {
+                    const Seg g = seg_of(p, t);
+                    for (int k = 0; k < g.n && ok; ++k)
+                        ok = load_kv(g, g.c0 + k, keep);
+                }
+                if (prev >= 0 && ok) {
+                    const Seg g = seg_of(p, prev);
+                    for (int k = 0; k < g.n && ok; ++k) {
+                        const int qs = ci % NQ;
+                        if (ci >= NQ && !bwait(&m->q_empty[qs], ((ci / NQ) & 1) ^ 1, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&m->q_full[qs], kC * kD * 2);
+                        tma_load_3d(sm + OFF_Q + qs * 16384, &p.mq, 0, (g.c0 + k) * kC, g.s,
+                                    &m->q_full[qs], stream);
+                        q_last[qs] = ci / NQ;
+                        TC_TRACE(ci, 0);
+                        ++ci;
+                        ok = load_kv(g, g.c0 + k, stream);
+                    }
+                }
+                if (t >= p.total)
+                    break;
+                prev = t;
             }
             if (*abort) {  // let every load this thread issued land before exit
                 for (int j = 0; j < NQ; ++j)
@@ -313,429 +420,529 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
             const uint32_t id_st = idesc_bf16_f32(128, 64, true, true);
             const uint32_t id_pv = idesc_bf16_f32(128, 64, false, true);
             const uint32_t id_in = idesc_bf16_f32(128, 64, false, false);
-            bool issued = false;
-            // MMA 1 of chunk i: scores into TM_P, chunk state into TM_DS[b]
-            auto mma1 = [&](int i) -> int {  // 1 issued, 0 no such chunk, -1 abort
-                const int ts = i % NT;
-                if (!bwait(&m->tick_full[ts], (i / NT) & 1, abort))
-                    return -1;
-                if (m->ticket[ts] >= p.total)
-                    return 0;
-                const int b = i & 1;
-                if (!bwait(&m->phi_done[b], (i >> 1) & 1, abort))
-                    return -1;
-                if (i >= 2 && !bwait(&m->ds_free[b], ((i >> 1) & 1) ^ 1, abort))
-                    return -1;
-                tc_fence_after();
-                const uint32_t q = smem_addr(sm + OFF_Q + (i % NQ) * 16384);
-                const uint32_t v = smem_addr(sm + OFF_KV + (i % NKV) * 32768);
+            bool issued = false, ok = true;
+            int kvi = 0, ci = 0, prev = -1, nsegA = 0;
+            // [V | phi(K)]^T phi(K) of the K,V stage `ks` accumulated into d
+            auto state_mma = [&](uint32_t d, int ks, bool acc) {
+                const uint32_t v = smem_addr(sm + OFF_KV + ks * 32768);
                 const uint32_t k = v + 16384;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ss(tm + TM_P, sdesc_sw128(q + 32 * kk, 16, 1024),
-                                sdesc_sw128(k + 32 * kk, 16, 1024), id_sc, kk > 0);
-#pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16_ss(tm + TM_DS + 64 * b, sdesc_sw128(v + 2048 * kk, 16384, 1024),
-                                sdesc_sw128(k + 2048 * kk, 16, 1024), id_st, kk > 0);
-                mma_commit(&m->mma1_done[b]);
-                TC_TRACE(i, 7);
-                issued = true;
-                return 1;
+                    mma_bf16_ss(d, sdesc_sw128(v + 2048 * kk, 16384, 1024),
+                                sdesc_sw128(k + 2048 * kk, 16, 1024), id_st, acc || kk > 0);
             };
-            int r = mma1(0);
-            for (int i = 0; r == 1; ++i) {
-                const int b = i & 1;
-                if (!bwait(&m->p_ready[b], (i >> 1) & 1, abort))
+            for (int j = 0; ok; ++j) {
+                const int ss = j % NS;
+                if (!bwait(&m->seg_full[ss], (j / NS) & 1, abort))
                     break;
-                if (i >= 2 && !bwait(&m->o_free[b], ((i >> 1) & 1) ^ 1, abort))
+                const int t = m->seg_ticket[ss];
+                if (t < p.total) {  // phase A: the segment aggregate
+                    const Seg g = seg_of(p, t);
+                    if (nsegA >= 1 && !bwait(&m->dseg_free, (nsegA - 1) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    for (int k = 0; k < g.n; ++k) {
+                        const int ks = kvi % NKV;
+                        if (!bwait(&m->kv_phi[ks], (kvi / NKV) & 1, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        state_mma(tm + TM_DSEG, ks, k > 0);
+                        mma_commit(&m->kv_empty[ks]);
+                        issued = true;
+                        ++kvi;
+                    }
+                    if (!ok)
+                        break;
+                    mma_commit(&m->dseg_done);
+                    
+                    ++nsegA;
+                }
+                if (prev >= 0) {  // phase C of the previous segment
+                    const Seg g = seg_of(p, prev);
+                    for (int k = 0; k < g.n && ok; ++k, ++ci, ++kvi) {
+                        const int b = ci & 1, qs = ci % NQ, ks = kvi % NKV;
+                        if (!bwait(&m->q_phi[qs], (ci / NQ) & 1, abort) ||
+                            !bwait(&m->kv_phi[ks], (kvi / NKV) & 1, abort) ||
+                            !bwait(&m->srun_read[b], (ci >> 1) & 1, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t q = smem_addr(sm + OFF_Q + qs * 16384);
+                        const uint32_t kk0 = smem_addr(sm + OFF_KV + ks * 32768) + 16384;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ss(tm + TM_P, sdesc_sw128(q + 32 * kk, 16, 1024),
+                                        sdesc_sw128(kk0 + 32 * kk, 16, 1024), id_sc, kk > 0);
+                        state_mma(tm + TM_SRUN, ks, true);
+                        mma_commit(&m->mma1_done[b]);
+                        TC_TRACE(ci, 7);
+                        issued = true;
+                        if (!bwait(&m->p_ready[b], (ci >> 1) & 1, abort) ||
+                            (ci >= 2 && !bwait(&m->o_free[b], ((ci >> 1) & 1) ^ 1, abort))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        TC_TRACE(ci, 14);
+                        const uint32_t v = smem_addr(sm + OFF_KV + ks * 32768);
+                        const uint32_t o = tm + TM_O + 64 * b;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_bf16_ts(o, tm + TM_PHL + 8 * kk,
+                                        sdesc_sw128(v + 2048 * kk, 16, 1024), id_pv, kk > 0);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_bf16_ts(o, tm + TM_PHL + 64 + 8 * kk,
+                                        sdesc_sw128(v + 2048 * kk, 16, 1024), id_pv, 1);
+                        mma_commit(&m->pv_done[b]);
+                        mma_commit(&m->kv_empty[ks]);
+                        TC_TRACE(ci, 8);
+                        const uint32_t sh = smem_addr(sm + OFF_S + b * 16384);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ss(o, sdesc_sw128(q + 32 * kk, 16, 1024),
+                                        sdesc_sw128(sh + 32 * kk, 16, 1024), id_in, 1);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ss(o, sdesc_sw128(q + 32 * kk, 16, 1024),
+                                        sdesc_sw128(sh + 8192 + 32 * kk, 16, 1024), id_in, 1);
+                        mma_commit(&m->o_done[b]);
+                        TC_TRACE(ci, 9);
+                    }
+                }
+                if (t >= p.total)
                     break;
-                tc_fence_after();
-                const uint32_t v = smem_addr(sm + OFF_KV + (i % NKV) * 32768);
-                const uint32_t o = tm + TM_O + 64 * b;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16_ts(o, tm + TM_PHL + 8 * kk, sdesc_sw128(v + 2048 * kk, 16, 1024),
-                                id_pv, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16_ts(o, tm + TM_PHL + 64 + 8 * kk,
-                                sdesc_sw128(v + 2048 * kk, 16, 1024), id_pv, 1);
-                mma_commit(&m->pv_done[b]);
-                mma_commit(&m->kv_empty[i % NKV]);
-                TC_TRACE(i, 8);
-                r = mma1(i + 1);
-                if (r < 0)
-                    break;
-                if (!bwait(&m->s_ready[b], (i >> 1) & 1, abort))
-                    break;
-                tc_fence_after();
-                const uint32_t q = smem_addr(sm + OFF_Q + (i % NQ) * 16384);
-                const uint32_t sh = smem_addr(sm + OFF_S + b * 16384);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ss(o, sdesc_sw128(q + 32 * kk, 16, 1024),
-                                sdesc_sw128(sh + 32 * kk, 16, 1024), id_in, 1);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ss(o, sdesc_sw128(q + 32 * kk, 16, 1024),
-                                sdesc_sw128(sh + 8192 + 32 * kk, 16, 1024), id_in, 1);
-                mma_commit(&m->o_done[b]);
-                TC_TRACE(i, 9);
+                prev = t;
             }
             if (issued && *abort) {  // every MMA issued here retires before tensor memory is freed
                 mma_commit(&m->drain);
                 drain_wait(&m->drain, 0);
             }
         }
-    } else if (warp == 2) {
-        // ----------------------------------------------------- look-back --
+    } else if (warp == 2 || warp == 3) {
+        // ------------------------------------ look-back, S_in (warps 2-3) --
+        const int tl = tid - 64;  // 0..63
+        const bool lead = tl == 0;
         const unsigned full = 0xffffffffu;
-        for (int i = 0;; ++i) {
-            const int ts = i % NT;
-            int ok = 1;
-            if (lane == 0)
-                ok = bwait(&m->tick_full[ts], (i / NT) & 1, abort);
-            if (!__shfl_sync(full, ok, 0))
+        for (int j = 0;; ++j) {
+            const int ss = j % NS;
+            if (!group_ok(!lead || bwait(&m->seg_full[ss], (j / NS) & 1, abort), 4, 64))
                 break;
-            const int t = m->ticket[ts];
+            const int t = m->seg_ticket[ss];
             if (t >= p.total)
                 break;
-            const int b = i & 1;
-            if (lane == 0 && i >= 2)
-                ok = bwait(&m->list_empty[b], ((i >> 1) & 1) ^ 1, abort);
-            if (!__shfl_sync(full, ok, 0))
+            const Seg g = seg_of(p, t);
+            const int gi = t / p.BH;
+            if (!group_ok(!lead || j < 2 || bwait(&m->sin_free[j & 1], ((j >> 1) & 1) ^ 1, abort),
+                          4, 64))
                 break;
-            const int c = t / p.BH, s = t % p.BH;
-            if (lane == 0)
-                TC_TRACE(i, 10);
-            const unsigned* flag_base = p.flags + static_cast<size_t>(s) * p.R;
-            // Lane l watches chunk base - l.  With a wrapping ring only R-1 slots
-            // behind this chunk are distinct from its own; a slot that holds
-            // another epoch (older: not yet written; newer: reused once a later
-            // inclusive prefix made it unnecessary) reads as not ready.
-            const int W = p.R >= p.nchunk ? 32 : min(32, p.R - 1);
-            const unsigned active = W >= 32 ? 0xffffffffu : ((1u << W) - 1u);
-            int* list = m->list[b];
-            int n = 0, base = c - 1;
-            uint64_t start = 0;
-            while (base >= 0) {
-                const int pc = base - lane;
-                bool ready = true, incl = true;
-                if (lane >= W) {
-                    ready = incl = false;
-                } else if (pc >= 0) {
-                    const unsigned f = ld_acquire(flag_base + pc % p.R);
-                    ready = (f >> 2) == static_cast<unsigned>(pc + 1) && (f & 3u) != 0u;
-                    incl = ready && (f & 3u) == 2u;
-                }
-                const unsigned mi = __ballot_sync(full, incl) & active;
-                const unsigned mr = __ballot_sync(full, ready) & active;
-                if (mi) {
-                    const int ls = __ffs(mi) - 1;
-                    const unsigned need = ls == 0 ? 0u : ((1u << ls) - 1u);
-                    if ((mr & need) == need) {
-                        if (n + ls + 1 > kMaxList) {
+            const unsigned* flag_base = p.flags + static_cast<size_t>(g.s) * p.R;
+            float* slot_base = p.slots + static_cast<size_t>(g.s) * p.R * kSlotFloats;
+            if (warp == 2) {
+                // Lane l watches segment base - l.  With a wrapping ring only R-1
+                // slots behind this segment are distinct from its own; a slot
+                // holding another epoch reads as not ready.
+                const int W = p.R >= p.nseg ? 32 : min(32, p.R - 1);
+                const unsigned active = W >= 32 ? 0xffffffffu : ((1u << W) - 1u);
+                int n = 0, base = gi - 1;
+                uint64_t start = 0;
+                while (base >= 0) {
+                    const int pg = base - lane;
+                    bool ready = true, incl = true;
+                    if (lane >= W) {
+                        ready = incl = false;
+                    } else if (pg >= 0) {
+                        const unsigned f = ld_acquire(flag_base + pg % p.R);
+                        ready = (f >> 2) == static_cast<unsigned>(pg + 1) && (f & 3u) != 0u;
+                        incl = ready && (f & 3u) == 2u;
+                    }
+                    const unsigned mi = __ballot_sync(full, incl) & active;
+                    const unsigned mr = __ballot_sync(full, ready) & active;
+                    if (mi) {
+                        const int ls = __ffs(mi) - 1;
+                        const unsigned need = ls == 0 ? 0u : ((1u << ls) - 1u);
+                        if ((mr & need) == need) {
+                            if (n + ls + 1 > kMaxList) {
+                                n = -2;
+                                break;
+                            }
+                            if (lane < ls)
+                                m->list[n + lane] = (pg % p.R) << 1;
+                            if (lane == ls && pg >= 0)
+                                m->list[n + lane] = ((pg % p.R) << 1) | 1;
+                            n += ls + (base - ls >= 0 ? 1 : 0);
+                            break;
+                        }
+                    } else if (mr == active) {
+                        if (n + W > kMaxList) {
                             n = -2;
                             break;
                         }
-                        if (lane < ls)
-                            list[n + lane] = (pc % p.R) << 1;
-                        if (lane == ls && pc >= 0)
-                            list[n + lane] = ((pc % p.R) << 1) | 1;
-                        n += ls + (base - ls >= 0 ? 1 : 0);
+                        if (lane < W)
+                            m->list[n + lane] = (pg % p.R) << 1;
+                        n += W;
+                        base -= W;
+                        start = 0;
+                        continue;
+                    }
+                    const uint64_t now = globaltimer();
+                    if (!start)
+                        start = now;
+                    if (__any_sync(full, now - start > kWaitNs || *abort)) {
+                        n = -1;
                         break;
                     }
-                } else if (mr == active) {
-                    if (n + W > kMaxList) {
-                        n = -2;
-                        break;
-                    }
-                    if (lane < W)
-                        list[n + lane] = (pc % p.R) << 1;
-                    n += W;
-                    base -= W;
-                    start = 0;
-                    continue;
+                    __nanosleep(32);
                 }
-                const uint64_t now = globaltimer();
-                if (!start)
-                    start = now;
-                if (__any_sync(full, now - start > kWaitNs || *abort)) {
-                    n = -1;
-                    break;
-                }
-                __nanosleep(32);
-            }
-            __syncwarp();
-            if (n < 0) {
                 if (lane == 0) {
-                    set_status(p.status, n == -1 ? LA_ERR_TIMEOUT : LA_ERR_DEVICE_CHECK);
-                    *abort = 1;
-                }
-                break;
-            }
-            if (lane == 0) {
-                m->nlist[b] = n;
-                mbar_arrive(&m->list_full[b]);
-                TC_TRACE(i, 11);
-            }
-        }
-    } else if (warp >= 4 && warp < 8) {
-        // --------------------------------- feature map, P (warps 4-7) --
-        const int ta = tid - 128, wa = warp - 4;
-        const bool lead = ta == 0;
-        for (int i = 0;; ++i) {
-            const int ts = i % NT;
-            if (!group_ok(!lead || bwait(&m->tick_full[ts], (i / NT) & 1, abort), 1))
-                break;
-            const int t = m->ticket[ts];
-            if (t >= p.total)
-                break;
-            const int c = t / p.BH;
-            const int valid = static_cast<int>(min(static_cast<int64_t>(kC),
-                                                   p.N - static_cast<int64_t>(c) * kC));
-            const int b = i & 1;
-            if (!group_ok(!lead || (bwait(&m->q_full[i % NQ], (i / NQ) & 1, abort) &&
-                                    bwait(&m->kv_full[i % NKV], (i / NKV) & 1, abort) &&
-                                    (i < 2 || bwait(&m->ds_free[b], ((i >> 1) & 1) ^ 1, abort))),
-                          1))
-                break;
-            unsigned char* sQ = sm + OFF_Q + (i % NQ) * 16384;
-            unsigned char* sK = sm + OFF_KV + (i % NKV) * 32768 + 16384;
-            if (lead)
-                TC_TRACE(i, 3);
-            {
-                const int cc = ta & 7;
-                float zp[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    zp[e] = 0.f;
-#pragma unroll 2
-                for (int mm = 0; mm < 8; ++mm) {
-                    const int r = (ta >> 3) + 16 * mm;
-                    const uint32_t off = sw128_off(r, cc);
-                    uint4* pq = reinterpret_cast<uint4*>(sQ + off);
-                    uint4* pk = reinterpret_cast<uint4*>(sK + off);
-                    uint4 xq = *pq, xk = *pk;
-                    if (r >= valid) {
-                        xq = make_uint4(0, 0, 0, 0);
-                        xk = make_uint4(0, 0, 0, 0);
-                        *pq = xq;
-                        *pk = xk;
-                    } else if (elu) {
-                        xq = make_uint4(phi2(xq.x), phi2(xq.y), phi2(xq.z), phi2(xq.w));
-                        xk = make_uint4(phi2(xk.x), phi2(xk.y), phi2(xk.z), phi2(xk.w));
-                        *pq = xq;
-                        *pk = xk;
+                    
+                    m->nlist = n;
+                    if (n < 0) {
+                        set_status(p.status, n == -1 ? LA_ERR_TIMEOUT : LA_ERR_DEVICE_CHECK);
+                        *abort = 1;
                     }
-                    zp[0] += bf_lo(xk.x), zp[1] += bf_hi(xk.x);
-                    zp[2] += bf_lo(xk.y), zp[3] += bf_hi(xk.y);
-                    zp[4] += bf_lo(xk.z), zp[5] += bf_hi(xk.z);
-                    zp[6] += bf_lo(xk.w), zp[7] += bf_hi(xk.w);
                 }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    zp[e] += __shfl_xor_sync(0xffffffffu, zp[e], 8);
-                    zp[e] += __shfl_xor_sync(0xffffffffu, zp[e], 16);
-                }
-                if (lane < 8)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        m->dzpart[b][wa][8 * cc + e] = zp[e];
             }
-            fence_proxy_async_smem();
-            named_bar(1);
-            if (ta == 0) {
-                mbar_arrive(&m->phi_done[b]);
-                TC_TRACE(i, 4);
-            }
-
-            // P: causal mask, row sums, bf16 hi/lo into TM_PHL
-            if (!group_ok(!lead || (bwait(&m->mma1_done[b], (i >> 1) & 1, abort) &&
-                                    (i < 1 || bwait(&m->pv_done[(i - 1) & 1],
-                                                    ((i - 1) >> 1) & 1, abort)) &&
-                                    (i < 2 || bwait(&m->epi_done[b], ((i >> 1) & 1) ^ 1, abort))),
-                          1))
+            named_bar(4, 64);
+            const int nlist = m->nlist;
+            if (nlist < 0)
                 break;
-            tc_fence_after();
-            if (lead)
-                TC_TRACE(i, 5);
-            float rs = 0.f;
+            // S_in: the nearest inclusive prefix plus the later aggregates in
+            // segment order; thread tl owns float4 words tl + 64 u, u = 0..16.
+            float4 acc[17];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t v0[16], v1[16];
-                tmem_ld16(tm + TM_P + lane_off + 32 * q, v0);
-                tmem_ld16(tm + TM_P + lane_off + 32 * q + 16, v1);
-                tmem_ld_wait();
-                uint32_t hi[16], lo[16];
-#pragma unroll
-                for (int mm = 0; mm < 16; ++mm) {
-                    const int j = 32 * q + 2 * mm;
-                    const uint32_t wa0 = mm < 8 ? v0[2 * mm] : v1[2 * mm - 16];
-                    const uint32_t wa1 = mm < 8 ? v0[2 * mm + 1] : v1[2 * mm - 15];
-                    const float a = j <= ta ? __uint_as_float(wa0) : 0.f;
-                    const float bb = j + 1 <= ta ? __uint_as_float(wa1) : 0.f;
-                    rs += a + bb;
-                    split2(a, bb, hi[mm], lo[mm]);
-                }
-                tmem_st16(tm + TM_PHL + lane_off + 16 * q, hi);
-                tmem_st16(tm + TM_PHL + lane_off + 64 + 16 * q, lo);
-            }
-            tmem_st_wait();
-            m->den[b][ta] = rs;
-            tc_fence_before();
-            named_bar(1);
-            if (ta == 0) {
-                mbar_arrive(&m->p_ready[b]);
-                TC_TRACE(i, 6);
-            }
-        }
-    } else if (warp >= 8 && warp < 12) {
-        // ------------------------------ chunk state, prefixes (warps 8-11) --
-        const int tb = tid - 256, wb = warp - 8;
-        float* sDS = reinterpret_cast<float*>(sm + OFF_DS);
-        const bool lead = tb == 0;
-        for (int i = 0;; ++i) {
-            const int ts = i % NT;
-            if (!group_ok(!lead || bwait(&m->tick_full[ts], (i / NT) & 1, abort), 2))
-                break;
-            const int t = m->ticket[ts];
-            if (t >= p.total)
-                break;
-            const int c = t / p.BH, s = t % p.BH;
-            const int b = i & 1;
-            float* slot_base = p.slots + static_cast<size_t>(s) * p.R * kSlotFloats;
-            unsigned* flag = p.flags + static_cast<size_t>(s) * p.R + (c % p.R);
-            float* agg = slot_base + static_cast<size_t>(c % p.R) * kSlotFloats;
-            if (!group_ok(!lead || (bwait(&m->phi_done[b], (i >> 1) & 1, abort) &&
-                                    bwait(&m->mma1_done[b], (i >> 1) & 1, abort)),
-                          2))
-                break;
-            tc_fence_after();
-            if (lead)
-                TC_TRACE(i, 12);
-            if (wb < 2) {  // dS^T rows = tensor-memory lanes 0..63
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t r[16];
-                    tmem_ld16(tm + TM_DS + 64 * b + lane_off + 16 * q, r);
-                    tmem_ld_wait();
-                    float4* d4 = reinterpret_cast<float4*>(sDS + tb * kD + 16 * q);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        d4[u] = make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
-                                            __uint_as_float(r[4 * u + 2]),
-                                            __uint_as_float(r[4 * u + 3]));
-                }
-            } else {
-                const int j = tb - 64;
-                sDS[kD * kD + j] = m->dzpart[b][0][j] + m->dzpart[b][1][j] + m->dzpart[b][2][j] +
-                                   m->dzpart[b][3][j];
-            }
-            tc_fence_before();
-            named_bar(2);
-            if (tb == 0)
-                mbar_arrive(&m->ds_free[b]);
-            {  // the aggregate, coalesced
-                const float4* src = reinterpret_cast<const float4*>(sDS);
-                float4* dst = reinterpret_cast<float4*>(agg);
-                for (int f = tb; f < kStateFloats / 4; f += 128)
-                    __stcg(dst + f, src[f]);
-            }
-            named_bar(2);
-            if (tb == 0) {
-                __threadfence();
-                st_release(flag, (static_cast<unsigned>(c + 1) << 2) | 1u);
-                TC_TRACE(i, 13);
-            }
-
-            // S_prev, z_prev: the nearest inclusive prefix plus the later
-            // aggregates in chunk order; thread tb owns float4 words tb + 128 j
-            // of the state, threads 0..15 also the z words.
-            if (!group_ok(!lead || bwait(&m->list_full[b], (i >> 1) & 1, abort), 2))
-                break;
-            const int nlist = m->nlist[b];
-            float4 acc[9];
-#pragma unroll
-            for (int j = 0; j < 9; ++j)
-                acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int u = 0; u < 17; ++u)
+                acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int e = nlist - 1; e >= 0; --e) {
-                const int ent = m->list[b][e];
+                const int ent = m->list[e];
                 const float4* src = reinterpret_cast<const float4*>(
                     slot_base + static_cast<size_t>(ent >> 1) * kSlotFloats +
                     ((ent & 1) ? kStateFloats : 0));
-                float4 x[9];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    x[j] = __ldcg(src + tb + 128 * j);
-                x[8] = tb < 16 ? __ldcg(src + 1024 + tb) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int j = 0; j < 9; ++j) {
-                    acc[j].x += x[j].x, acc[j].y += x[j].y;
-                    acc[j].z += x[j].z, acc[j].w += x[j].w;
+                for (int u = 0; u < 17; ++u) {
+                    const int f = tl + 64 * u;
+                    if (f < kStateFloats / 4) {
+                        const float4 x = __ldcg(src + f);
+                        acc[u].x += x.x, acc[u].y += x.y, acc[u].z += x.z, acc[u].w += x.w;
+                    }
                 }
             }
-            if (!group_ok(!lead || i < 2 ||
-                              (bwait(&m->o_done[b], ((i >> 1) & 1) ^ 1, abort) &&
-                               bwait(&m->epi_done[b], ((i >> 1) & 1) ^ 1, abort)),
-                          2))
-                break;
-            unsigned char* sShi = sm + OFF_S + b * 16384;
-            unsigned char* sSlo = sShi + 8192;
-            const float4* ds4 = reinterpret_cast<const float4*>(sDS);
-            float4* inc = reinterpret_cast<float4*>(agg + kStateFloats);
+            float4* sin = reinterpret_cast<float4*>(
+                p.sin_scratch + (static_cast<size_t>(blockIdx.x) * 2 + (j & 1)) * kStateFloats);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int f = tb + 128 * j;
-                const int row = f >> 4, col4 = f & 15;  // S_prev^T row, 4 features
-                uint2 h, l;
-                split2(acc[j].x, acc[j].y, h.x, l.x);
-                split2(acc[j].z, acc[j].w, h.y, l.y);
-                const uint32_t off = sw128_off(row, col4 >> 1) + (col4 & 1) * 8;
-                *reinterpret_cast<uint2*>(sShi + off) = h;
-                *reinterpret_cast<uint2*>(sSlo + off) = l;
-                const float4 d = ds4[f];
-                __stcg(inc + f, make_float4(acc[j].x + d.x, acc[j].y + d.y, acc[j].z + d.z,
-                                            acc[j].w + d.w));
+            for (int u = 0; u < 17; ++u) {
+                const int f = tl + 64 * u;
+                if (f < kStateFloats / 4)
+                    __stcg(sin + f, acc[u]);
             }
-            if (tb < 16) {
-                reinterpret_cast<float4*>(m->zprev[b])[tb] = acc[8];
-                const float4 d = ds4[1024 + tb];
-                __stcg(inc + 1024 + tb, make_float4(acc[8].x + d.x, acc[8].y + d.y,
-                                                    acc[8].z + d.z, acc[8].w + d.w));
+            // the inclusive prefix needs this segment's own aggregate
+            if (!group_ok(!lead || bwait(&m->agg_pub[j & 1], (j >> 1) & 1, abort), 4, 64))
+                break;
+            const int my = gi % p.R;
+            const float4* agg =
+                reinterpret_cast<const float4*>(slot_base + static_cast<size_t>(my) * kSlotFloats);
+            float4* inc = reinterpret_cast<float4*>(slot_base + static_cast<size_t>(my) * kSlotFloats +
+                                                    kStateFloats);
+#pragma unroll
+            for (int u = 0; u < 17; ++u) {
+                const int f = tl + 64 * u;
+                if (f < kStateFloats / 4) {
+                    const float4 a = __ldcg(agg + f);
+                    __stcg(inc + f, make_float4(acc[u].x + a.x, acc[u].y + a.y, acc[u].z + a.z,
+                                                acc[u].w + a.w));
+                }
             }
-            fence_proxy_async_smem();
-            named_bar(2);
-            if (tb == 0) {
-                mbar_arrive(&m->list_empty[b]);
-                mbar_arrive(&m->s_ready[b]);
+            named_bar(4, 64);
+            if (lead) {
                 __threadfence();
-                st_release(flag, (static_cast<unsigned>(c + 1) << 2) | 2u);
-                TC_TRACE(i, 14);
+                st_release(const_cast<unsigned*>(flag_base) + my,
+                           (static_cast<unsigned>(gi + 1) << 2) | 2u);
+                mbar_arrive(&m->sin_ready[j & 1]);
+                
             }
         }
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------ P (warps 4-7) ----
+        const int ta = tid - 128;
+        const bool lead = ta == 0;
+        int ci = 0, prev = -1;
+        for (int j = 0;; ++j) {
+            const int ss = j % NS;
+            if (!group_ok(!lead || bwait(&m->seg_full[ss], (j / NS) & 1, abort), 1, 128))
+                break;
+            const int t = m->seg_ticket[ss];
+            bool ok = true;
+            if (prev >= 0) {  // phase C of the previous segment
+                const Seg g = seg_of(p, prev);
+                for (int k = 0; k < g.n; ++k, ++ci) {
+                    const int b = ci & 1;
+                    // P: causal mask, row sums, bf16 hi/lo into TM_PHL
+                    if (!group_ok(!lead ||
+                                      (bwait(&m->mma1_done[b], (ci >> 1) & 1, abort) &&
+                                       (ci < 1 || bwait(&m->pv_done[(ci - 1) & 1],
+                                                        ((ci - 1) >> 1) & 1, abort)) &&
+                                       (ci < 2 ||
+                                        bwait(&m->epi_done[b], ((ci >> 1) & 1) ^ 1, abort))),
+                                  1, 128)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lead)
+                        TC_TRACE(ci, 3);
+                    float rs = 0.f;
+                    const bool upper_zero = ta < 64;  // rows 0..63: keys 64..127 are masked
+                    uint32_t v[2][32];
+                    tmem_ld16(tm + TM_P + lane_off, *reinterpret_cast<uint32_t(*)[16]>(v[0]));
+                    tmem_ld16(tm + TM_P + lane_off + 16,
+                              *reinterpret_cast<uint32_t(*)[16]>(v[0] + 16));
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t* cur = v[q & 1];
+                        if (q < 3 && !(upper_zero && q >= 1)) {
+                            tmem_ld16(tm + TM_P + lane_off + 32 * (q + 1),
+                                      *reinterpret_cast<uint32_t(*)[16]>(v[(q + 1) & 1]));
+                            tmem_ld16(tm + TM_P + lane_off + 32 * (q + 1) + 16,
+                                      *reinterpret_cast<uint32_t(*)[16]>(v[(q + 1) & 1] + 16));
+                        }
+                        uint32_t hi[16], lo[16];
+                        if (upper_zero && q >= 2) {
+#pragma unroll
+                            for (int mm = 0; mm < 16; ++mm)
+                                hi[mm] = lo[mm] = 0u;
+                        } else {
+#pragma unroll
+                            for (int mm = 0; mm < 16; ++mm) {
+                                const int jj = 32 * q + 2 * mm;
+                                const float a = jj <= ta ? __uint_as_float(cur[2 * mm]) : 0.f;
+                                const float bb =
+                                    jj + 1 <= ta ? __uint_as_float(cur[2 * mm + 1]) : 0.f;
+                                rs += a + bb;
+                                split2(a, bb, hi[mm], lo[mm]);
+                            }
+                        }
+                        tmem_st16(tm + TM_PHL + lane_off + 16 * q, hi);
+                        tmem_st16(tm + TM_PHL + lane_off + 64 + 16 * q, lo);
+                        tmem_ld_wait();
+                    }
+                    tmem_st_wait();
+                    if (lead)
+                        TC_TRACE(ci, 10);
+                    m->den[b][ta] = rs;
+                    tc_fence_before();
+                    named_bar(1, 128);
+                    if (lead) {
+                        mbar_arrive(&m->p_ready[b]);
+                        TC_TRACE(ci, 6);
+                    }
+                }
+            }
+            if (!ok || t >= p.total)
+                break;
+            prev = t;
+        }
+    } else if (warp >= 8 && warp < 12) {
+        // ------------- phi(K), segment aggregate, S_prev (warps 8-11) ------
+        const int tb = tid - 256, wb = warp - 8;
+        const bool lead = tb == 0;
+        int kvi = 0, ci = 0, prev = -1, nsegA = 0;
+        for (int j = 0;; ++j) {
+            const int ss = j % NS;
+            if (!group_ok(!lead || bwait(&m->seg_full[ss], (j / NS) & 1, abort), 2, 128))
+                break;
+            const int t = m->seg_ticket[ss];
+            bool ok = true;
+            if (t < p.total) {  // phase A of segment j: phi(K), dz, then the aggregate
+                const Seg g = seg_of(p, t);
+                const int gi = t / p.BH;
+                for (int k = 0; k < g.n; ++k, ++kvi) {
+                    const int ks = kvi % NKV;
+                    if (!group_ok(!lead || bwait(&m->kv_full[ks], (kvi / NKV) & 1, abort), 2,
+                                  128)) {
+                        ok = false;
+                        break;
+                    }
+                    phi_tile(sm + OFF_KV + ks * 32768 + 16384, tb, chunk_valid(p, g.c0 + k), elu,
+                             m->dza);
+                    fence_proxy_async_smem();
+                    named_bar(2, 128);
+                    if (tb < kD)
+                        m->dzacc[tb] += m->dza[0][tb] + m->dza[1][tb] + m->dza[2][tb] +
+                                        m->dza[3][tb];
+                    if (lead)
+                        mbar_arrive(&m->kv_phi[ks]);
+                    named_bar(2, 128);
+                }
+                if (!ok ||
+                    !group_ok(!lead || bwait(&m->dseg_done, nsegA & 1, abort), 2, 128))
+                    break;
+                tc_fence_after();
+                float* agg = p.slots + (static_cast<size_t>(g.s) * p.R + gi % p.R) * kSlotFloats;
+                if (wb < 2) {  // dS^T rows = tensor-memory lanes 0..63
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t r[16];
+                        tmem_ld16(tm + TM_DSEG + lane_off + 16 * q, r);
+                        tmem_ld_wait();
+                        float4* d4 = reinterpret_cast<float4*>(agg + tb * kD + 16 * q);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            __stcg(d4 + u, make_float4(__uint_as_float(r[4 * u]),
+                                                       __uint_as_float(r[4 * u + 1]),
+                                                       __uint_as_float(r[4 * u + 2]),
+                                                       __uint_as_float(r[4 * u + 3])));
+                    }
+                } else {
+                    __stcg(agg + kD * kD + (tb - 64), m->dzacc[tb - 64]);
+                    m->dzacc[tb - 64] = 0.f;
+                }
+                tc_fence_before();
+                named_bar(2, 128);
+                if (lead) {
+                    mbar_arrive(&m->dseg_free);
+                    __threadfence();
+                    st_release(p.flags + static_cast<size_t>(g.s) * p.R + gi % p.R,
+                               (static_cast<unsigned>(gi + 1) << 2) | 1u);
+                    mbar_arrive(&m->agg_pub[j & 1]);
+                    
+                }
+                ++nsegA;
+            }
+            if (prev >= 0 && ok) {  // phase C of segment j-1: phi(K), running state
+                const Seg g = seg_of(p, prev);
+                const int jp = j - 1;
+                for (int k = 0; k < g.n; ++k, ++ci, ++kvi) {
+                    const int b = ci & 1, ks = kvi % NKV;
+                    if (!group_ok(!lead || bwait(&m->kv_full[ks], (kvi / NKV) & 1, abort), 2,
+                                  128)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lead)
+                        TC_TRACE(ci, 11);
+                    phi_tile(sm + OFF_KV + ks * 32768 + 16384, tb, chunk_valid(p, g.c0 + k), elu,
+                             m->dzc[b]);
+                    fence_proxy_async_smem();
+                    named_bar(2, 128);
+                    if (lead) {
+                        mbar_arrive(&m->kv_phi[ks]);
+                        TC_TRACE(ci, 2);
+                    }
+                    // S_prev, z_prev of chunk ci
+                    if (!group_ok(!lead || ci < 2 ||
+                                      (bwait(&m->o_done[b], ((ci >> 1) & 1) ^ 1, abort) &&
+                                       bwait(&m->epi_done[b], ((ci >> 1) & 1) ^ 1, abort)),
+                                  2, 128) ||
+                        !group_ok(!lead || ci < 1 ||
+                                      bwait(&m->mma1_done[(ci - 1) & 1], ((ci - 1) >> 1) & 1,
+                                            abort),
+                                  2, 128) ||
+                        !group_ok(!lead || k > 0 ||
+                                      bwait(&m->sin_ready[jp & 1], (jp >> 1) & 1, abort),
+                                  2, 128)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    unsigned char* sShi = sm + OFF_S + b * 16384;
+                    unsigned char* sSlo = sShi + 8192;
+                    if (wb < 2) {  // S_prev^T row tb: tensor-memory lane tb
+                        float sp[kD];
+                        if (k == 0) {  // segment start: S_in from the look-back
+                            const float4* src = reinterpret_cast<const float4*>(
+                                p.sin_scratch +
+                                (static_cast<size_t>(blockIdx.x) * 2 + (jp & 1)) * kStateFloats +
+                                tb * kD);
+#pragma unroll
+                            for (int u = 0; u < 16; ++u) {
+                                const float4 x = __ldcg(src + u);
+                                sp[4 * u] = x.x, sp[4 * u + 1] = x.y, sp[4 * u + 2] = x.z,
+                                       sp[4 * u + 3] = x.w;
+                            }
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                uint32_t r[16];
+#pragma unroll
+                                for (int u = 0; u < 16; ++u)
+                                    r[u] = __float_as_uint(sp[16 * q + u]);
+                                tmem_st16(tm + TM_SRUN + lane_off + 16 * q, r);
+                            }
+                            tmem_st_wait();
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                uint32_t r[16];
+                                tmem_ld16(tm + TM_SRUN + lane_off + 16 * q, r);
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int u = 0; u < 16; ++u)
+                                    sp[16 * q + u] = __uint_as_float(r[u]);
+                            }
+                        }
+#pragma unroll
+                        for (int cc = 0; cc < 8; ++cc) {
+                            uint4 h, l;
+                            split2(sp[8 * cc + 0], sp[8 * cc + 1], h.x, l.x);
+                            split2(sp[8 * cc + 2], sp[8 * cc + 3], h.y, l.y);
+                            split2(sp[8 * cc + 4], sp[8 * cc + 5], h.z, l.z);
+                            split2(sp[8 * cc + 6], sp[8 * cc + 7], h.w, l.w);
+                            *reinterpret_cast<uint4*>(sShi + sw128_off(tb, cc)) = h;
+                            *reinterpret_cast<uint4*>(sSlo + sw128_off(tb, cc)) = l;
+                        }
+                    } else {  // z_prev
+                        const int i = tb - 64;
+                        float z;
+                        if (k == 0)
+                            z = __ldcg(p.sin_scratch +
+                                       (static_cast<size_t>(blockIdx.x) * 2 + (jp & 1)) *
+                                           kStateFloats +
+                                       kD * kD + i);
+                        else
+                            z = m->zrun[i] + m->dzc[(ci - 1) & 1][0][i] +
+                                m->dzc[(ci - 1) & 1][1][i] + m->dzc[(ci - 1) & 1][2][i] +
+                                m->dzc[(ci - 1) & 1][3][i];
+                        m->zrun[i] = z;
+                        m->zprev[b][i] = z;
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    named_bar(2, 128);
+                    if (lead) {
+                        if (k == 0)
+                            mbar_arrive(&m->sin_free[jp & 1]);
+                        mbar_arrive(&m->srun_read[b]);
+                        TC_TRACE(ci, 4);
+                    }
+                }
+            }
+            if (!ok || t >= p.total)
+                break;
+            prev = t;
+        }
     } else if (warp >= 12) {
-        // ------------------------------------------ epilogue (warps 12-15) --
+        // ------------------------------ phi(Q), epilogue (warps 12-15) -----
         const int tcx = tid - 384;
+        const bool lead = tcx == 0;
         const uint64_t pol = policy_evict_first();
         unsigned char* sO = sm + OFF_O;
-        const bool lead = tcx == 0;
-        for (int i = 0;; ++i) {
-            const int ts = i % NT;
-            if (!group_ok(!lead || bwait(&m->tick_full[ts], (i / NT) & 1, abort), 3))
-                break;
-            const int t = m->ticket[ts];
-            if (t >= p.total)
-                break;
-            const int c = t / p.BH, s = t % p.BH;
-            const int b = i & 1, qs = i % NQ;
-            if (!group_ok(!lead || (bwait(&m->p_ready[b], (i >> 1) & 1, abort) &&
-                                    bwait(&m->s_ready[b], (i >> 1) & 1, abort) &&
-                                    bwait(&m->o_done[b], (i >> 1) & 1, abort)),
-                          3))
-                break;
+        int ci = 0, prev = -1;
+        // the epilogue of a chunk runs after phi(Q) of the next one
+        int pend_ci = -1, pend_c = 0, pend_s = 0, pend_last = 0, pend_ss = 0;
+        auto epilogue = [&]() -> bool {
+            const int cj = pend_ci, b = cj & 1, qs = cj % NQ;
+            if (!group_ok(!lead || (bwait(&m->p_ready[b], (cj >> 1) & 1, abort) &&
+                                    bwait(&m->srun_read[b], (cj >> 1) & 1, abort) &&
+                                    bwait(&m->o_done[b], (cj >> 1) & 1, abort)),
+                          3, 128))
+                return false;
             tc_fence_after();
+            if (lead)
+                TC_TRACE(cj, 5);
             float den = 0.f;
             if (norm) {
                 den = m->den[b][tcx];
@@ -756,40 +963,84 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 }
             }
             const float inv = norm ? 1.0f / fmaxf(den, FLT_MIN) : 1.0f;
-            if (tcx == 0)
+            if (lead)
                 bulk_wait_read<0>();  // the previous tile has left the staging buffer
-            named_bar(3);
+            named_bar(3, 128);
+            uint32_t r[4][16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                tmem_ld16(tm + TM_O + 64 * b + lane_off + 16 * q, r[q]);
+            tmem_ld_wait();
+            if (lead)
+                TC_TRACE(cj, 13);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                uint32_t r[16];
-                tmem_ld16(tm + TM_O + 64 * b + lane_off + 16 * q, r);
-                tmem_ld_wait();
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int col4 = 4 * q + u;
-                    const float4 o = make_float4(__uint_as_float(r[4 * u]) * inv,
-                                                 __uint_as_float(r[4 * u + 1]) * inv,
-                                                 __uint_as_float(r[4 * u + 2]) * inv,
-                                                 __uint_as_float(r[4 * u + 3]) * inv);
+                    const float4 o = make_float4(__uint_as_float(r[q][4 * u]) * inv,
+                                                 __uint_as_float(r[q][4 * u + 1]) * inv,
+                                                 __uint_as_float(r[q][4 * u + 2]) * inv,
+                                                 __uint_as_float(r[q][4 * u + 3]) * inv);
                     *reinterpret_cast<float4*>(sO + (col4 >> 3) * 16384 +
                                                sw128_off(tcx, col4 & 7)) = o;
                 }
             }
             tc_fence_before();
             fence_proxy_async_smem();
-            named_bar(3);
-            if (tcx == 0) {
+            named_bar(3, 128);
+            if (lead) {
                 mbar_arrive(&m->o_free[b]);
                 mbar_arrive(&m->q_empty[qs]);
                 mbar_arrive(&m->epi_done[b]);
-                mbar_arrive(&m->tick_empty[ts]);
-                tma_store_3d(&p.mo, sO, 0, c * kC, s, pol);
-                tma_store_3d(&p.mo, sO + 16384, 32, c * kC, s, pol);
+                if (pend_last)
+                    mbar_arrive(&m->seg_empty[pend_ss]);
+                tma_store_3d(&p.mo, sO, 0, pend_c * kC, pend_s, pol);
+                tma_store_3d(&p.mo, sO + 16384, 32, pend_c * kC, pend_s, pol);
                 bulk_commit();
-                TC_TRACE(i, 15);
+                TC_TRACE(cj, 15);
             }
+            pend_ci = -1;
+            return true;
+        };
+        bool ok = true;
+        for (int j = 0; ok; ++j) {
+            const int ss = j % NS;
+            if (!group_ok(!lead || bwait(&m->seg_full[ss], (j / NS) & 1, abort), 3, 128))
+                break;
+            const int t = m->seg_ticket[ss];
+            if (prev >= 0) {
+                const Seg g = seg_of(p, prev);
+                for (int k = 0; k < g.n; ++k, ++ci) {
+                    const int qs = ci % NQ;
+                    if (!group_ok(!lead || bwait(&m->q_full[qs], (ci / NQ) & 1, abort), 3, 128)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lead)
+                        TC_TRACE(ci, 12);
+                    phi_tile(sm + OFF_Q + qs * 16384, tcx, chunk_valid(p, g.c0 + k), elu, nullptr);
+                    fence_proxy_async_smem();
+                    named_bar(3, 128);
+                    if (lead) {
+                        mbar_arrive(&m->q_phi[qs]);
+                        TC_TRACE(ci, 1);
+                    }
+                    if (pend_ci >= 0 && !epilogue()) {
+                        ok = false;
+                        break;
+                    }
+                    pend_ci = ci, pend_c = g.c0 + k, pend_s = g.s;
+                    pend_last = k == g.n - 1, pend_ss = (j - 1) % NS;
+                }
+            }
+            if (t >= p.total)
+                break;
+            prev = t;
         }
-        if (tcx == 0)
+        if (ok && pend_ci >= 0)
+            epilogue();
+        if (lead)
             bulk_wait<0>();
     }
 
@@ -838,10 +1089,12 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esz,
 
 struct TcGeom {
     int G;       // CTAs
-    int R;       // ring slots per sequence
+    int L;       // chunks per segment
     int nchunk;
-    int total;
-    size_t flags_off, slots_off, bytes;
+    int nseg;
+    int R;       // ring slots per sequence
+    int total;   // segment tickets
+    size_t flags_off, slots_off, sin_off, bytes;
 };
 
 int sm_count()
@@ -856,20 +1109,28 @@ int sm_count()
 TcGeom tc_geom(int64_t BH, int64_t N, int sms)
 {
     TcGeom g{};
+    if (sms <= 0)
+        sms = 148;
     g.nchunk = (int)((N + kC - 1) / kC);
-    g.total = (int)(BH * g.nchunk);
-    int G = sms > 0 ? sms : 148;
+    const int64_t chunks = BH * g.nchunk;
+    // about a dozen segments per CTA keeps the tail short; long segments make
+    // the look-back rare
+    g.L = (int)std::max<int64_t>(1, std::min<int64_t>(8, chunks / ((int64_t)sms * 12)));
+    g.nseg = (g.nchunk + g.L - 1) / g.L;
+    g.total = (int)(BH * g.nseg);
+    int G = sms;
     G = (int)std::min<int64_t>(G, g.total);
     G = (int)std::min<int64_t>(G, BH * 20);  // bounds the ring and the look-back list
     if (G < 1)
         G = 1;
     g.G = G;
-    // tickets a CTA holds at once: the ring plus one being placed
-    const int64_t per_seq = ((NT + 1) * (int64_t)G + BH - 1) / BH + 2;
-    g.R = (int)std::min<int64_t>(per_seq, g.nchunk);
+    // segment tickets a CTA holds at once: the ring plus one being placed
+    const int64_t per_seq = ((NS + 1) * (int64_t)G + BH - 1) / BH + 2;
+    g.R = (int)std::min<int64_t>(per_seq, g.nseg);
     g.flags_off = 256;
     g.slots_off = (g.flags_off + sizeof(unsigned) * (size_t)BH * g.R + 255) & ~(size_t)255;
-    g.bytes = g.slots_off + sizeof(float) * (size_t)BH * g.R * kSlotFloats;
+    g.sin_off = g.slots_off + sizeof(float) * (size_t)BH * g.R * kSlotFloats;
+    g.bytes = g.sin_off + sizeof(float) * (size_t)G * 2 * kStateFloats;
     return g;
 }
 
@@ -903,12 +1164,15 @@ cudaError_t tc_forward(const FwdArgs& a)
     p.N = a.N;
     p.BH = (int)BH;
     p.nchunk = g.nchunk;
+    p.L = g.L;
+    p.nseg = g.nseg;
     p.R = g.R;
     p.total = g.total;
     p.fm = a.fm;
     p.counter = reinterpret_cast<unsigned*>(ws);
     p.flags = reinterpret_cast<unsigned*>(ws + g.flags_off);
     p.slots = reinterpret_cast<float*>(ws + g.slots_off);
+    p.sin_scratch = reinterpret_cast<float*>(ws + g.sin_off);
     p.status = a.status;
     cudaError_t e = cudaMemsetAsync(ws, 0, g.slots_off, a.stream);
     if (e != cudaSuccess)
