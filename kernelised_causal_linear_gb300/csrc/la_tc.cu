@@ -186,9 +186,9 @@ __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile i
 {
     uint64_t t0 = 0;
     for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity))
+        if (mbar_try_wait_sleep(bar, parity, 20000u))
             return true;
-        if ((n & 31u) == 0u) {
+        if ((n & 3u) == 0u) {
             if (*abort)
                 return false;
             const uint64_t now = globaltimer();
@@ -246,8 +246,8 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
 // Feature map in place on a 128 x 64 bf16 tile (128-byte swizzle) by 128
 // threads; rows >= valid become zero.  With zsum, also the column sums of the
 // result: zsum[warp][64] (rows of this warp's threads only).
-__device__ __forceinline__ void phi_tile(unsigned char* tile, int t, int valid, bool elu,
-                                         float (*zsum)[kD])
+__device__ __noinline__ void phi_tile(unsigned char* tile, int t, int valid, bool elu,
+                                     float (*zsum)[kD])
 {
     const int cc = t & 7, r0 = t >> 3;
     uint4 x[8];
@@ -596,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                         n = -1;
                         break;
                     }
-                    __nanosleep(32);
+                    __nanosleep(200);
                 }
                 if (lane == 0) {
                     
@@ -695,40 +695,41 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     if (lead)
                         TC_TRACE(ci, 3);
                     float rs = 0.f;
-                    const bool upper_zero = ta < 64;  // rows 0..63: keys 64..127 are masked
-                    uint32_t v[2][32];
-                    tmem_ld16(tm + TM_P + lane_off, *reinterpret_cast<uint32_t(*)[16]>(v[0]));
-                    tmem_ld16(tm + TM_P + lane_off + 16,
-                              *reinterpret_cast<uint32_t(*)[16]>(v[0] + 16));
-                    tmem_ld_wait();
-#pragma unroll
+                    // rows 0..63 see only keys 0..63: the upper 64 columns are masked
+                    const int nq = ta < 64 ? 2 : 4;
+#pragma unroll 1
                     for (int q = 0; q < 4; ++q) {
-                        uint32_t* cur = v[q & 1];
-                        if (q < 3 && !(upper_zero && q >= 1)) {
-                            tmem_ld16(tm + TM_P + lane_off + 32 * (q + 1),
-                                      *reinterpret_cast<uint32_t(*)[16]>(v[(q + 1) & 1]));
-                            tmem_ld16(tm + TM_P + lane_off + 32 * (q + 1) + 16,
-                                      *reinterpret_cast<uint32_t(*)[16]>(v[(q + 1) & 1] + 16));
-                        }
                         uint32_t hi[16], lo[16];
-                        if (upper_zero && q >= 2) {
+                        if (q < nq) {
+                            uint32_t v0[16], v1[16];
+                            tmem_ld16(tm + TM_P + lane_off + 32 * q, v0);
+                            tmem_ld16(tm + TM_P + lane_off + 32 * q + 16, v1);
+                            tmem_ld_wait();
+                            const int lim = ta - 32 * q;  // keys jj <= ta stay
 #pragma unroll
-                            for (int mm = 0; mm < 16; ++mm)
-                                hi[mm] = lo[mm] = 0u;
-                        } else {
-#pragma unroll
-                            for (int mm = 0; mm < 16; ++mm) {
-                                const int jj = 32 * q + 2 * mm;
-                                const float a = jj <= ta ? __uint_as_float(cur[2 * mm]) : 0.f;
+                            for (int mm = 0; mm < 8; ++mm) {
+                                const float a = 2 * mm <= lim ? __uint_as_float(v0[2 * mm]) : 0.f;
                                 const float bb =
-                                    jj + 1 <= ta ? __uint_as_float(cur[2 * mm + 1]) : 0.f;
+                                    2 * mm + 1 <= lim ? __uint_as_float(v0[2 * mm + 1]) : 0.f;
                                 rs += a + bb;
                                 split2(a, bb, hi[mm], lo[mm]);
                             }
+#pragma unroll
+                            for (int mm = 0; mm < 8; ++mm) {
+                                const float a =
+                                    16 + 2 * mm <= lim ? __uint_as_float(v1[2 * mm]) : 0.f;
+                                const float bb =
+                                    17 + 2 * mm <= lim ? __uint_as_float(v1[2 * mm + 1]) : 0.f;
+                                rs += a + bb;
+                                split2(a, bb, hi[8 + mm], lo[8 + mm]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int mm = 0; mm < 16; ++mm)
+                                hi[mm] = lo[mm] = 0u;
                         }
                         tmem_st16(tm + TM_PHL + lane_off + 16 * q, hi);
                         tmem_st16(tm + TM_PHL + lane_off + 64 + 16 * q, lo);
-                        tmem_ld_wait();
                     }
                     tmem_st_wait();
                     if (lead)
