@@ -92,7 +92,9 @@ constexpr uint32_t OFF_KV = OFF_Q + NQ * 16384;        // NKV x (V then K)
 constexpr uint32_t OFF_S = OFF_KV + NKV * 32768;       // 2 x (S^T hi, S^T lo)
 constexpr uint32_t OFF_O = OFF_S + 2 * 16384;          // output staging 2 x 16 KiB
 constexpr uint32_t OFF_MISC = OFF_O + 32768;
-constexpr uint32_t kMiscBytes = 8192;
+constexpr uint32_t kMiscBytes = 16384;
+constexpr int kMaxL = 8;       // largest segment (chunks)
+constexpr int NPH = 4;         // phi(K) scratch ring depth, in segments
 constexpr uint32_t SMEM_BYTES = OFF_MISC + kMiscBytes + 1024;  // + alignment slack
 
 // tensor memory columns
@@ -104,6 +106,7 @@ constexpr uint32_t TM_DSEG = 448;  // segment aggregate dS^T (lanes 0..63)
 
 struct TcParams {
     CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mphi;  // phi(K) scratch: per CTA NPH x L tiles of 128 x 64 bf16
     int64_t N;
     int BH;
     int nchunk;   // chunks per sequence
@@ -116,15 +119,16 @@ struct TcParams {
     unsigned* flags;
     float* slots;
     float* sin_scratch;  // per CTA: 2 x S_in
+    void* phi_scratch;   // the tiles mphi describes
     int* status;
 };
 
 struct Misc {
     uint64_t seg_full[NS], seg_empty[NS];
     uint64_t q_full[NQ], q_empty[NQ], q_phi[NQ];
-    uint64_t kv_full[NKV], kv_empty[NKV], kv_phi[NKV];
+    uint64_t kv_full[NKV], kv_empty[NKV], aphi[NKV], phik_stored[NPH];
     uint64_t mma1_done[2], p_ready[2], pv_done[2], srun_read[2], o_done[2], o_free[2];
-    uint64_t epi_done[2], dzc_ready[2];
+    uint64_t epi_done[2];
     uint64_t dseg_done, dseg_free, dzseg_ready[2], agg_pub[2], sin_ready[2], sin_free[2];
     uint64_t drain;
     uint32_t tmem;
@@ -135,9 +139,9 @@ struct Misc {
     float den[2][kC];
     alignas(16) float zprev[2][kD];
     float zrun[kD];
-    float dzc[2][4][kD];     // per C chunk: column sums of phi(K), one row per warp
-    float dza[4][kD];        // per A chunk: the same
+    float dza[4][kD];        // per A chunk: column sums of phi(K), one row per warp
     float dzacc[kD];         // running column sums over the current A segment
+    float dzk[NPH][kMaxL][kD];  // per chunk column sums, kept for phase C
     float dzseg[2][kD];
 };
 static_assert(sizeof(Misc) <= kMiscBytes, "misc");
@@ -228,12 +232,34 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity)
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// elu(x)+1 on two packed bf16, rounded back to bf16: max(x,0) + exp(min(x,0))
+__device__ __forceinline__ uint32_t bf2_min0(uint32_t w)
+{
+    uint32_t r;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(0u));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t bf2_max0(uint32_t w)
+{
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(0u));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t bf2_add(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// elu(x)+1 on two packed bf16: max(x,0) + exp(min(x,0)).  One of the two
+// terms is always exact (0, or exp(0) = 1), so rounding exp(min(x,0)) to bf16
+// first and adding in bf16 gives the correctly rounded result of the fp32 sum.
 __device__ __forceinline__ uint32_t phi2(uint32_t w)
 {
-    const float a = bf_lo(w), b = bf_hi(w);
-    return pack_bf16x2(fmaxf(a, 0.f) + __expf(fminf(a, 0.f)),
-                       fmaxf(b, 0.f) + __expf(fminf(b, 0.f)));
+    const uint32_t mn = bf2_min0(w);
+    return bf2_add(bf2_max0(w), pack_bf16x2(__expf(bf_lo(mn)), __expf(bf_hi(mn))));
 }
 
 // split two fp32 into packed bf16 hi and lo parts
@@ -245,9 +271,10 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
 
 // Feature map in place on a 128 x 64 bf16 tile (128-byte swizzle) by 128
 // threads; rows >= valid become zero.  With zsum, also the column sums of the
-// result: zsum[warp][64] (rows of this warp's threads only).
+// result: zsum[warp][64] (rows of this warp's threads only).  With gdst, the
+// result is also written to global memory as a plain row-major 128 x 64 tile.
 __device__ __noinline__ void phi_tile(unsigned char* tile, int t, int valid, bool elu,
-                                     float (*zsum)[kD])
+                                     float (*zsum)[kD], uint4* gdst)
 {
     const int cc = t & 7, r0 = t >> 3;
     uint4 x[8];
@@ -263,6 +290,8 @@ __device__ __noinline__ void phi_tile(unsigned char* tile, int t, int valid, boo
             x[mm] = make_uint4(phi2(x[mm].x), phi2(x[mm].y), phi2(x[mm].z), phi2(x[mm].w));
         if (r >= valid || elu)
             *reinterpret_cast<uint4*>(tile + sw128_off(r, cc)) = x[mm];
+        if (gdst)
+            gdst[r * 8 + cc] = x[mm];
     }
     if (zsum) {
         float zp[8];
@@ -312,6 +341,33 @@ __device__ __forceinline__ int chunk_valid(const TcParams& p, int c)
     return static_cast<int>(min(static_cast<int64_t>(kC), p.N - static_cast<int64_t>(c) * kC));
 }
 
+// Job order shared by every role.  Round j holds phase A of local segment j
+// and phase C of local segment j-2, interleaved chunk by chunk
+// (A0 C0 A1 C1 ...); the two rounds between a segment's phases hide its
+// look-back.
+struct Round {
+    int j;        // round = local index of the A segment
+    int tA, tC;   // tickets of the A and C segments (-1: none)
+    Seg gA, gC;
+    int nA, nC;
+};
+
+__device__ __forceinline__ void round_setup(const TcParams& p, Round& r, int j, int tA, int tC)
+{
+    r.j = j;
+    r.tA = tA;
+    r.tC = tC;
+    r.nA = r.nC = 0;
+    if (tA >= 0) {
+        r.gA = seg_of(p, tA);
+        r.nA = r.gA.n;
+    }
+    if (tC >= 0) {
+        r.gC = seg_of(p, tC);
+        r.nC = r.gC.n;
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant__ TcParams p)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -334,6 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
         tma_prefetch_desc(&p.mk);
         tma_prefetch_desc(&p.mv);
         tma_prefetch_desc(&p.mo);
+        tma_prefetch_desc(&p.mphi);
     }
     if (tid < kD)
         m->dzacc[tid] = 0.f;
@@ -346,6 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
     tc_fence_after();
     const uint32_t tm = m->tmem;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    // phi(K) scratch tile of local segment jj, chunk k
+    auto phi_index = [&](int jj, int k) {
+        return (static_cast<int>(blockIdx.x) * NPH + jj % NPH) * p.L + k;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------ producer --
@@ -357,52 +418,65 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 q_last[j] = -1;
             for (int j = 0; j < NKV; ++j)
                 kv_last[j] = -1;
-            int kvi = 0, ci = 0, prev = -1;
-            bool ok = true;
-            auto load_kv = [&](const Seg& g, int c, uint64_t pol) -> bool {
+            int kvi = 0, ci = 0, h1 = -1, h2 = -1;
+            bool ok = true, doneA = false;
+            // K (or, in phase C, phi(K) from the scratch tile `phi`) and V
+            auto load_kv = [&](const Seg& g, int c, uint64_t pol, int phi) -> bool {
                 const int ks = kvi % NKV;
                 if (kvi >= NKV && !bwait(&m->kv_empty[ks], ((kvi / NKV) & 1) ^ 1, abort))
                     return false;
                 mbar_arrive_expect_tx(&m->kv_full[ks], 2 * kC * kD * 2);
                 unsigned char* kv = sm + OFF_KV + ks * 32768;
-                tma_load_3d(kv + 16384, &p.mk, 0, c * kC, g.s, &m->kv_full[ks], pol);
+                if (phi >= 0)
+                    tma_load_3d(kv + 16384, &p.mphi, 0, 0, phi, &m->kv_full[ks], pol);
+                else
+                    tma_load_3d(kv + 16384, &p.mk, 0, c * kC, g.s, &m->kv_full[ks], pol);
                 tma_load_3d(kv, &p.mv, 0, c * kC, g.s, &m->kv_full[ks], pol);
                 kv_last[ks] = kvi / NKV;
                 ++kvi;
                 return true;
             };
             for (int j = 0; ok; ++j) {
-                const int t = static_cast<int>(atomicAdd(p.counter, 1u));
-                const int ss = j % NS;
-                if (j >= NS && !bwait(&m->seg_empty[ss], ((j / NS) & 1) ^ 1, abort))
-                    break;
-                m->seg_ticket[ss] = t;
-                mbar_arrive(&m->seg_full[ss]);
-                if (t < p.total) {
-                    const Seg g = seg_of(p, t);
-                    for (int k = 0; k < g.n && ok; ++k)
-                        ok = load_kv(g, g.c0 + k, keep);
+                int tA = -1;
+                if (!doneA) {
+                    const int t = static_cast<int>(atomicAdd(p.counter, 1u));
+                    const int ss = j % NS;
+                    if (j >= NS && !bwait(&m->seg_empty[ss], ((j / NS) & 1) ^ 1, abort))
+                        break;
+                    m->seg_ticket[ss] = t;
+                    mbar_arrive(&m->seg_full[ss]);
+                    if (t < p.total)
+                        tA = t;
+                    else
+                        doneA = true;
                 }
-                if (prev >= 0 && ok) {
-                    const Seg g = seg_of(p, prev);
-                    for (int k = 0; k < g.n && ok; ++k) {
+                Round r;
+                round_setup(p, r, j, tA, h2);
+                if (r.nA == 0 && r.nC == 0 && h1 < 0)
+                    break;
+                const int jc = j - 2;
+                if (r.nC && !bwait(&m->phik_stored[jc % NPH], (jc / NPH) & 1, abort))
+                    break;
+                for (int k = 0; k < max(r.nA, r.nC) && ok; ++k) {
+                    if (k < r.nA)
+                        ok = load_kv(r.gA, r.gA.c0 + k, keep, -1);
+                    if (k < r.nC && ok) {
                         const int qs = ci % NQ;
                         if (ci >= NQ && !bwait(&m->q_empty[qs], ((ci / NQ) & 1) ^ 1, abort)) {
                             ok = false;
                             break;
                         }
                         mbar_arrive_expect_tx(&m->q_full[qs], kC * kD * 2);
-                        tma_load_3d(sm + OFF_Q + qs * 16384, &p.mq, 0, (g.c0 + k) * kC, g.s,
-                                    &m->q_full[qs], stream);
+                        tma_load_3d(sm + OFF_Q + qs * 16384, &p.mq, 0, (r.gC.c0 + k) * kC,
+                                    r.gC.s, &m->q_full[qs], stream);
                         q_last[qs] = ci / NQ;
                         TC_TRACE(ci, 0);
                         ++ci;
-                        ok = load_kv(g, g.c0 + k, stream);
+                        ok = load_kv(r.gC, r.gC.c0 + k, stream, phi_index(jc, k));
                     }
                 }
-                if (t >= p.total)
-                    break;
-                prev = t;
+                h2 = h1;
+                h1 = tA;
             }
             if (*abort) {  // let every load this thread issued land before exit
                 for (int j = 0; j < NQ; ++j)
@@ -420,31 +494,48 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
             const uint32_t id_st = idesc_bf16_f32(128, 64, true, true);
             const uint32_t id_pv = idesc_bf16_f32(128, 64, false, true);
             const uint32_t id_in = idesc_bf16_f32(128, 64, false, false);
-            bool issued = false, ok = true;
-            int kvi = 0, ci = 0, prev = -1, nsegA = 0;
-            // [V | phi(K)]^T phi(K) of the K,V stage `ks` accumulated into d
+            // Operand descriptors of stage 0; a stage or K-step offset of x bytes
+            // adds x >> 4 to the start-address field.
+            const uint64_t dq0 = sdesc_sw128(smem_addr(sm + OFF_Q), 16, 1024);
+            const uint32_t v0 = smem_addr(sm + OFF_KV);
+            const uint64_t dk0 = sdesc_sw128(v0 + 16384, 16, 1024);
+            const uint64_t dvm0 = sdesc_sw128(v0, 16384, 1024);  // [V | phi(K)]: one 128-row A
+            const uint64_t dvb0 = sdesc_sw128(v0, 16, 1024);
+            const uint64_t ds0 = sdesc_sw128(smem_addr(sm + OFF_S), 16, 1024);
+            auto dq = [&](int i) { return dq0 + (uint64_t)(i * (16384 >> 4)); };
+            auto dk = [&](int i) { return dk0 + (uint64_t)(i * (32768 >> 4)); };
+            auto dvm = [&](int i) { return dvm0 + (uint64_t)(i * (32768 >> 4)); };
+            auto dvb = [&](int i) { return dvb0 + (uint64_t)(i * (32768 >> 4)); };
+            auto ds = [&](int i) { return ds0 + (uint64_t)(i * (16384 >> 4)); };
+            bool issued = false, ok = true, doneA = false;
+            int kvi = 0, ci = 0, ai = 0, nsegA = 0, h1 = -1, h2 = -1;
+            // [V | phi(K)]^T phi(K) of stage ks accumulated into d
             auto state_mma = [&](uint32_t d, int ks, bool acc) {
-                const uint32_t v = smem_addr(sm + OFF_KV + ks * 32768);
-                const uint32_t k = v + 16384;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16_ss(d, sdesc_sw128(v + 2048 * kk, 16384, 1024),
-                                sdesc_sw128(k + 2048 * kk, 16, 1024), id_st, acc || kk > 0);
+                    mma_bf16_ss(d, dvm(ks) + 128 * kk, dk(ks) + 128 * kk, id_st, acc || kk > 0);
             };
             for (int j = 0; ok; ++j) {
-                const int ss = j % NS;
-                if (!bwait(&m->seg_full[ss], (j / NS) & 1, abort))
-                    break;
-                const int t = m->seg_ticket[ss];
-                if (t < p.total) {  // phase A: the segment aggregate
-                    const Seg g = seg_of(p, t);
-                    if (nsegA >= 1 && !bwait(&m->dseg_free, (nsegA - 1) & 1, abort)) {
-                        ok = false;
+                int tA = -1;
+                if (!doneA) {
+                    if (!bwait(&m->seg_full[j % NS], (j / NS) & 1, abort))
                         break;
-                    }
-                    for (int k = 0; k < g.n; ++k) {
+                    const int t = m->seg_ticket[j % NS];
+                    if (t < p.total)
+                        tA = t;
+                    else
+                        doneA = true;
+                }
+                Round r;
+                round_setup(p, r, j, tA, h2);
+                if (r.nA == 0 && r.nC == 0 && h1 < 0)
+                    break;
+                for (int k = 0; k < max(r.nA, r.nC) && ok; ++k) {
+                    if (k < r.nA) {  // phase A: segment aggregate into TM_DSEG
                         const int ks = kvi % NKV;
-                        if (!bwait(&m->kv_phi[ks], (kvi / NKV) & 1, abort)) {
+                        if ((k == 0 && nsegA >= 1 &&
+                             !bwait(&m->dseg_free, (nsegA - 1) & 1, abort)) ||
+                            !bwait(&m->aphi[ai % NKV], (ai / NKV) & 1, abort)) {
                             ok = false;
                             break;
                         }
@@ -452,31 +543,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                         state_mma(tm + TM_DSEG, ks, k > 0);
                         mma_commit(&m->kv_empty[ks]);
                         issued = true;
-                        ++kvi;
+                        ++kvi, ++ai;
+                        if (k == r.nA - 1) {
+                            mma_commit(&m->dseg_done);
+                            ++nsegA;
+                        }
                     }
-                    if (!ok)
-                        break;
-                    mma_commit(&m->dseg_done);
-                    
-                    ++nsegA;
-                }
-                if (prev >= 0) {  // phase C of the previous segment
-                    const Seg g = seg_of(p, prev);
-                    for (int k = 0; k < g.n && ok; ++k, ++ci, ++kvi) {
+                    if (k < r.nC) {  // phase C: one chunk of outputs
                         const int b = ci & 1, qs = ci % NQ, ks = kvi % NKV;
                         if (!bwait(&m->q_phi[qs], (ci / NQ) & 1, abort) ||
-                            !bwait(&m->kv_phi[ks], (kvi / NKV) & 1, abort) ||
+                            !bwait(&m->kv_full[ks], (kvi / NKV) & 1, abort) ||
                             !bwait(&m->srun_read[b], (ci >> 1) & 1, abort)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t q = smem_addr(sm + OFF_Q + qs * 16384);
-                        const uint32_t kk0 = smem_addr(sm + OFF_KV + ks * 32768) + 16384;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ss(tm + TM_P, sdesc_sw128(q + 32 * kk, 16, 1024),
-                                        sdesc_sw128(kk0 + 32 * kk, 16, 1024), id_sc, kk > 0);
+                            mma_bf16_ss(tm + TM_P, dq(qs) + 2 * kk, dk(ks) + 2 * kk, id_sc, kk > 0);
                         state_mma(tm + TM_SRUN, ks, true);
                         mma_commit(&m->mma1_done[b]);
                         TC_TRACE(ci, 7);
@@ -488,35 +572,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                         }
                         tc_fence_after();
                         TC_TRACE(ci, 14);
-                        const uint32_t v = smem_addr(sm + OFF_KV + ks * 32768);
                         const uint32_t o = tm + TM_O + 64 * b;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            mma_bf16_ts(o, tm + TM_PHL + 8 * kk,
-                                        sdesc_sw128(v + 2048 * kk, 16, 1024), id_pv, kk > 0);
+                            mma_bf16_ts(o, tm + TM_PHL + 8 * kk, dvb(ks) + 128 * kk, id_pv, kk > 0);
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            mma_bf16_ts(o, tm + TM_PHL + 64 + 8 * kk,
-                                        sdesc_sw128(v + 2048 * kk, 16, 1024), id_pv, 1);
+                            mma_bf16_ts(o, tm + TM_PHL + 64 + 8 * kk, dvb(ks) + 128 * kk, id_pv, 1);
                         mma_commit(&m->pv_done[b]);
                         mma_commit(&m->kv_empty[ks]);
                         TC_TRACE(ci, 8);
-                        const uint32_t sh = smem_addr(sm + OFF_S + b * 16384);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ss(o, sdesc_sw128(q + 32 * kk, 16, 1024),
-                                        sdesc_sw128(sh + 32 * kk, 16, 1024), id_in, 1);
+                            mma_bf16_ss(o, dq(qs) + 2 * kk, ds(b) + 2 * kk, id_in, 1);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ss(o, sdesc_sw128(q + 32 * kk, 16, 1024),
-                                        sdesc_sw128(sh + 8192 + 32 * kk, 16, 1024), id_in, 1);
+                            mma_bf16_ss(o, dq(qs) + 2 * kk, ds(b) + 512 + 2 * kk, id_in, 1);
                         mma_commit(&m->o_done[b]);
                         TC_TRACE(ci, 9);
+                        ++ci, ++kvi;
                     }
                 }
-                if (t >= p.total)
-                    break;
-                prev = t;
+                h2 = h1;
+                h1 = tA;
             }
             if (issued && *abort) {  // every MMA issued here retires before tensor memory is freed
                 mma_commit(&m->drain);
@@ -599,7 +677,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     __nanosleep(200);
                 }
                 if (lane == 0) {
-                    
                     m->nlist = n;
                     if (n < 0) {
                         set_status(p.status, n == -1 ? LA_ERR_TIMEOUT : LA_ERR_DEVICE_CHECK);
@@ -662,179 +739,282 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 st_release(const_cast<unsigned*>(flag_base) + my,
                            (static_cast<unsigned>(gi + 1) << 2) | 2u);
                 mbar_arrive(&m->sin_ready[j & 1]);
-                
             }
         }
     } else if (warp >= 4 && warp < 8) {
-        // ------------------------------------------------ P (warps 4-7) ----
+        // ---------------------------------- P, epilogue (warps 4-7) --------
         const int ta = tid - 128;
         const bool lead = ta == 0;
-        int ci = 0, prev = -1;
-        for (int j = 0;; ++j) {
-            const int ss = j % NS;
-            if (!group_ok(!lead || bwait(&m->seg_full[ss], (j / NS) & 1, abort), 1, 128))
-                break;
-            const int t = m->seg_ticket[ss];
-            bool ok = true;
-            if (prev >= 0) {  // phase C of the previous segment
-                const Seg g = seg_of(p, prev);
-                for (int k = 0; k < g.n; ++k, ++ci) {
-                    const int b = ci & 1;
-                    // P: causal mask, row sums, bf16 hi/lo into TM_PHL
-                    if (!group_ok(!lead ||
-                                      (bwait(&m->mma1_done[b], (ci >> 1) & 1, abort) &&
-                                       (ci < 1 || bwait(&m->pv_done[(ci - 1) & 1],
-                                                        ((ci - 1) >> 1) & 1, abort)) &&
-                                       (ci < 2 ||
-                                        bwait(&m->epi_done[b], ((ci >> 1) & 1) ^ 1, abort))),
-                                  1, 128)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (lead)
-                        TC_TRACE(ci, 3);
-                    float rs = 0.f;
-                    // rows 0..63 see only keys 0..63: the upper 64 columns are masked
-                    const int nq = ta < 64 ? 2 : 4;
-#pragma unroll 1
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t hi[16], lo[16];
-                        if (q < nq) {
-                            uint32_t v0[16], v1[16];
-                            tmem_ld16(tm + TM_P + lane_off + 32 * q, v0);
-                            tmem_ld16(tm + TM_P + lane_off + 32 * q + 16, v1);
-                            tmem_ld_wait();
-                            const int lim = ta - 32 * q;  // keys jj <= ta stay
+        const uint64_t pol = policy_evict_first();
+        unsigned char* sO = sm + OFF_O;
+        int ci = 0, h1 = -1, h2 = -1;
+        bool doneA = false;
+        // the epilogue of a chunk runs after P of the next one; its row sum of P
+        // (the intra-chunk denominator) waits in a register
+        int pend_ci = -1, pend_c = 0, pend_s = 0, pend_last = 0, pend_ss = 0;
+        float pend_rs = 0.f;
+        auto epilogue = [&]() -> bool {
+            const int cj = pend_ci, b = cj & 1, qs = cj % NQ;
+            if (!group_ok(!lead || (bwait(&m->q_phi[qs], (cj / NQ) & 1, abort) &&
+                                    bwait(&m->srun_read[b], (cj >> 1) & 1, abort) &&
+                                    bwait(&m->o_done[b], (cj >> 1) & 1, abort)),
+                          1, 128))
+                return false;
+            tc_fence_after();
+            if (lead)
+                TC_TRACE(cj, 5);
+            float den = pend_rs;
+            if (norm) {
+                const unsigned char* sQ = sm + OFF_Q + qs * 16384;
+                const float* z = m->zprev[b];
 #pragma unroll
-                            for (int mm = 0; mm < 8; ++mm) {
-                                const float a = 2 * mm <= lim ? __uint_as_float(v0[2 * mm]) : 0.f;
-                                const float bb =
-                                    2 * mm + 1 <= lim ? __uint_as_float(v0[2 * mm + 1]) : 0.f;
-                                rs += a + bb;
-                                split2(a, bb, hi[mm], lo[mm]);
-                            }
-#pragma unroll
-                            for (int mm = 0; mm < 8; ++mm) {
-                                const float a =
-                                    16 + 2 * mm <= lim ? __uint_as_float(v1[2 * mm]) : 0.f;
-                                const float bb =
-                                    17 + 2 * mm <= lim ? __uint_as_float(v1[2 * mm + 1]) : 0.f;
-                                rs += a + bb;
-                                split2(a, bb, hi[8 + mm], lo[8 + mm]);
-                            }
-                        } else {
-#pragma unroll
-                            for (int mm = 0; mm < 16; ++mm)
-                                hi[mm] = lo[mm] = 0u;
-                        }
-                        tmem_st16(tm + TM_PHL + lane_off + 16 * q, hi);
-                        tmem_st16(tm + TM_PHL + lane_off + 64 + 16 * q, lo);
-                    }
-                    tmem_st_wait();
-                    if (lead)
-                        TC_TRACE(ci, 10);
-                    m->den[b][ta] = rs;
-                    tc_fence_before();
-                    named_bar(1, 128);
-                    if (lead) {
-                        mbar_arrive(&m->p_ready[b]);
-                        TC_TRACE(ci, 6);
-                    }
+                for (int cc = 0; cc < 8; ++cc) {
+                    const uint4 x = *reinterpret_cast<const uint4*>(sQ + sw128_off(ta, cc));
+                    const float4 z0 = *reinterpret_cast<const float4*>(z + 8 * cc);
+                    const float4 z1 = *reinterpret_cast<const float4*>(z + 8 * cc + 4);
+                    den = fmaf(bf_lo(x.x), z0.x, den);
+                    den = fmaf(bf_hi(x.x), z0.y, den);
+                    den = fmaf(bf_lo(x.y), z0.z, den);
+                    den = fmaf(bf_hi(x.y), z0.w, den);
+                    den = fmaf(bf_lo(x.z), z1.x, den);
+                    den = fmaf(bf_hi(x.z), z1.y, den);
+                    den = fmaf(bf_lo(x.w), z1.z, den);
+                    den = fmaf(bf_hi(x.w), z1.w, den);
                 }
             }
-            if (!ok || t >= p.total)
+            const float inv = norm ? 1.0f / fmaxf(den, FLT_MIN) : 1.0f;
+            if (lead)
+                bulk_wait_read<0>();  // the previous tile has left the staging buffer
+            named_bar(1, 128);
+            uint32_t rr[4][16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                tmem_ld16(tm + TM_O + 64 * b + lane_off + 16 * q, rr[q]);
+            tmem_ld_wait();
+            if (lead)
+                TC_TRACE(cj, 13);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int col4 = 4 * q + u;
+                    const float4 o = make_float4(__uint_as_float(rr[q][4 * u]) * inv,
+                                                 __uint_as_float(rr[q][4 * u + 1]) * inv,
+                                                 __uint_as_float(rr[q][4 * u + 2]) * inv,
+                                                 __uint_as_float(rr[q][4 * u + 3]) * inv);
+                    *reinterpret_cast<float4*>(sO + (col4 >> 3) * 16384 +
+                                               sw128_off(ta, col4 & 7)) = o;
+                }
+            }
+            tc_fence_before();
+            fence_proxy_async_smem();
+            named_bar(1, 128);
+            if (lead) {
+                mbar_arrive(&m->o_free[b]);
+                mbar_arrive(&m->q_empty[qs]);
+                mbar_arrive(&m->epi_done[b]);
+                if (pend_last)
+                    mbar_arrive(&m->seg_empty[pend_ss]);
+                tma_store_3d(&p.mo, sO, 0, pend_c * kC, pend_s, pol);
+                tma_store_3d(&p.mo, sO + 16384, 32, pend_c * kC, pend_s, pol);
+                bulk_commit();
+                TC_TRACE(cj, 15);
+            }
+            pend_ci = -1;
+            return true;
+        };
+        bool ok = true;
+        for (int j = 0; ok; ++j) {
+            int tA = -1;
+            if (!doneA) {
+                if (!group_ok(!lead || bwait(&m->seg_full[j % NS], (j / NS) & 1, abort), 1, 128))
+                    break;
+                const int t = m->seg_ticket[j % NS];
+                if (t < p.total)
+                    tA = t;
+                else
+                    doneA = true;
+            }
+            Round r;
+            round_setup(p, r, j, tA, h2);
+            if (r.nA == 0 && r.nC == 0 && h1 < 0)
                 break;
-            prev = t;
+            for (int k = 0; k < r.nC; ++k, ++ci) {
+                const int b = ci & 1;
+                // P: causal mask, row sums, bf16 hi/lo into TM_PHL
+                if (!group_ok(!lead || (bwait(&m->mma1_done[b], (ci >> 1) & 1, abort) &&
+                                        (ci < 1 || bwait(&m->pv_done[(ci - 1) & 1],
+                                                         ((ci - 1) >> 1) & 1, abort))),
+                              1, 128)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lead)
+                    TC_TRACE(ci, 3);
+                float rs = 0.f;
+                // rows 0..63 see only keys 0..63: the upper 64 columns are masked
+                const int nq = ta < 64 ? 2 : 4;
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t hi[16], lo[16];
+                    if (q < nq) {
+                        uint32_t v0[16], v1[16];
+                        tmem_ld16(tm + TM_P + lane_off + 32 * q, v0);
+                        tmem_ld16(tm + TM_P + lane_off + 32 * q + 16, v1);
+                        tmem_ld_wait();
+                        const int lim = ta - 32 * q;  // keys jj <= ta stay
+#pragma unroll
+                        for (int mm = 0; mm < 8; ++mm) {
+                            const float a = 2 * mm <= lim ? __uint_as_float(v0[2 * mm]) : 0.f;
+                            const float bb =
+                                2 * mm + 1 <= lim ? __uint_as_float(v0[2 * mm + 1]) : 0.f;
+                            rs += a + bb;
+                            split2(a, bb, hi[mm], lo[mm]);
+                        }
+#pragma unroll
+                        for (int mm = 0; mm < 8; ++mm) {
+                            const float a =
+                                16 + 2 * mm <= lim ? __uint_as_float(v1[2 * mm]) : 0.f;
+                            const float bb =
+                                17 + 2 * mm <= lim ? __uint_as_float(v1[2 * mm + 1]) : 0.f;
+                            rs += a + bb;
+                            split2(a, bb, hi[8 + mm], lo[8 + mm]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int mm = 0; mm < 16; ++mm)
+                            hi[mm] = lo[mm] = 0u;
+                    }
+                    tmem_st16(tm + TM_PHL + lane_off + 16 * q, hi);
+                    tmem_st16(tm + TM_PHL + lane_off + 64 + 16 * q, lo);
+                }
+                tmem_st_wait();
+                if (lead)
+                    TC_TRACE(ci, 10);
+                tc_fence_before();
+                named_bar(1, 128);
+                if (lead) {
+                    mbar_arrive(&m->p_ready[b]);
+                    TC_TRACE(ci, 6);
+                }
+                if (pend_ci >= 0 && !epilogue()) {
+                    ok = false;
+                    break;
+                }
+                pend_ci = ci, pend_c = r.gC.c0 + k, pend_s = r.gC.s, pend_rs = rs;
+                pend_last = k == r.nC - 1, pend_ss = (j - 2) % NS;
+            }
+            h2 = h1;
+            h1 = tA;
         }
+        if (ok && pend_ci >= 0)
+            epilogue();
+        if (lead)
+            bulk_wait<0>();
     } else if (warp >= 8 && warp < 12) {
         // ------------- phi(K), segment aggregate, S_prev (warps 8-11) ------
         const int tb = tid - 256, wb = warp - 8;
         const bool lead = tb == 0;
-        int kvi = 0, ci = 0, prev = -1, nsegA = 0;
-        for (int j = 0;; ++j) {
-            const int ss = j % NS;
-            if (!group_ok(!lead || bwait(&m->seg_full[ss], (j / NS) & 1, abort), 2, 128))
+        int kvi = 0, ci = 0, ai = 0, nsegA = 0, h1 = -1, h2 = -1;
+        bool ok = true, doneA = false;
+        for (int j = 0; ok; ++j) {
+            int tA = -1;
+            if (!doneA) {
+                if (!group_ok(!lead || bwait(&m->seg_full[j % NS], (j / NS) & 1, abort), 2, 128))
+                    break;
+                const int t = m->seg_ticket[j % NS];
+                if (t < p.total)
+                    tA = t;
+                else
+                    doneA = true;
+            }
+            Round r;
+            round_setup(p, r, j, tA, h2);
+            if (r.nA == 0 && r.nC == 0 && h1 < 0)
                 break;
-            const int t = m->seg_ticket[ss];
-            bool ok = true;
-            if (t < p.total) {  // phase A of segment j: phi(K), dz, then the aggregate
-                const Seg g = seg_of(p, t);
-                const int gi = t / p.BH;
-                for (int k = 0; k < g.n; ++k, ++kvi) {
+            const int jc = j - 2;
+            for (int k = 0; k < max(r.nA, r.nC) && ok; ++k) {
+                if (k < r.nA) {  // phase A: phi(K) kept for phase C, column sums
                     const int ks = kvi % NKV;
                     if (!group_ok(!lead || bwait(&m->kv_full[ks], (kvi / NKV) & 1, abort), 2,
                                   128)) {
                         ok = false;
                         break;
                     }
-                    phi_tile(sm + OFF_KV + ks * 32768 + 16384, tb, chunk_valid(p, g.c0 + k), elu,
-                             m->dza);
+                    unsigned char* ktile = sm + OFF_KV + ks * 32768 + 16384;
+                    if (lead)
+                        TC_TRACE(ai, 2);
+                    // phi(K) is kept for phase C in the scratch (plain stores,
+                    // fenced before the TMA loads of phase C read it)
+                    phi_tile(ktile, tb, chunk_valid(p, r.gA.c0 + k), elu, m->dza,
+                             reinterpret_cast<uint4*>(p.phi_scratch) +
+                                 static_cast<size_t>(phi_index(j, k)) * (kC * kD * 2 / 16));
                     fence_proxy_async_smem();
                     named_bar(2, 128);
-                    if (tb < kD)
-                        m->dzacc[tb] += m->dza[0][tb] + m->dza[1][tb] + m->dza[2][tb] +
-                                        m->dza[3][tb];
-                    if (lead)
-                        mbar_arrive(&m->kv_phi[ks]);
-                    named_bar(2, 128);
-                }
-                if (!ok ||
-                    !group_ok(!lead || bwait(&m->dseg_done, nsegA & 1, abort), 2, 128))
-                    break;
-                tc_fence_after();
-                float* agg = p.slots + (static_cast<size_t>(g.s) * p.R + gi % p.R) * kSlotFloats;
-                if (wb < 2) {  // dS^T rows = tensor-memory lanes 0..63
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t r[16];
-                        tmem_ld16(tm + TM_DSEG + lane_off + 16 * q, r);
-                        tmem_ld_wait();
-                        float4* d4 = reinterpret_cast<float4*>(agg + tb * kD + 16 * q);
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            __stcg(d4 + u, make_float4(__uint_as_float(r[4 * u]),
-                                                       __uint_as_float(r[4 * u + 1]),
-                                                       __uint_as_float(r[4 * u + 2]),
-                                                       __uint_as_float(r[4 * u + 3])));
+                    if (tb < kD) {
+                        const float dz =
+                            m->dza[0][tb] + m->dza[1][tb] + m->dza[2][tb] + m->dza[3][tb];
+                        m->dzacc[tb] += dz;
+                        m->dzk[j % NPH][k][tb] = dz;
                     }
-                } else {
-                    __stcg(agg + kD * kD + (tb - 64), m->dzacc[tb - 64]);
-                    m->dzacc[tb - 64] = 0.f;
-                }
-                tc_fence_before();
-                named_bar(2, 128);
-                if (lead) {
-                    mbar_arrive(&m->dseg_free);
-                    __threadfence();
-                    st_release(p.flags + static_cast<size_t>(g.s) * p.R + gi % p.R,
-                               (static_cast<unsigned>(gi + 1) << 2) | 1u);
-                    mbar_arrive(&m->agg_pub[j & 1]);
-                    
-                }
-                ++nsegA;
-            }
-            if (prev >= 0 && ok) {  // phase C of segment j-1: phi(K), running state
-                const Seg g = seg_of(p, prev);
-                const int jp = j - 1;
-                for (int k = 0; k < g.n; ++k, ++ci, ++kvi) {
-                    const int b = ci & 1, ks = kvi % NKV;
-                    if (!group_ok(!lead || bwait(&m->kv_full[ks], (kvi / NKV) & 1, abort), 2,
-                                  128)) {
-                        ok = false;
-                        break;
-                    }
-                    if (lead)
-                        TC_TRACE(ci, 11);
-                    phi_tile(sm + OFF_KV + ks * 32768 + 16384, tb, chunk_valid(p, g.c0 + k), elu,
-                             m->dzc[b]);
-                    fence_proxy_async_smem();
-                    named_bar(2, 128);
                     if (lead) {
-                        mbar_arrive(&m->kv_phi[ks]);
-                        TC_TRACE(ci, 2);
+                        mbar_arrive(&m->aphi[ai % NKV]);
+                        TC_TRACE(ai, 11);
                     }
-                    // S_prev, z_prev of chunk ci
+                    named_bar(2, 128);
+                    ++kvi, ++ai;
+                    if (k == r.nA - 1) {  // segment aggregate complete: publish it
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        __threadfence();
+                        named_bar(2, 128);
+                        if (lead)
+                            mbar_arrive(&m->phik_stored[j % NPH]);
+                        const int gi = r.tA / p.BH;
+                        // agg_pub[j & 1] is re-armed only after the look-back warps
+                        // consumed it for segment j-2 (their sin_ready follows that)
+                        if (!group_ok(!lead || (bwait(&m->dseg_done, nsegA & 1, abort) &&
+                                                (j < 2 || bwait(&m->sin_ready[(j - 2) & 1],
+                                                                ((j - 2) >> 1) & 1, abort))),
+                                      2, 128)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        float* agg =
+                            p.slots + (static_cast<size_t>(r.gA.s) * p.R + gi % p.R) * kSlotFloats;
+                        if (wb < 2) {  // dS^T rows = tensor-memory lanes 0..63
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                uint32_t rr[16];
+                                tmem_ld16(tm + TM_DSEG + lane_off + 16 * q, rr);
+                                tmem_ld_wait();
+                                float4* d4 = reinterpret_cast<float4*>(agg + tb * kD + 16 * q);
+#pragma unroll
+                                for (int u = 0; u < 4; ++u)
+                                    __stcg(d4 + u, make_float4(__uint_as_float(rr[4 * u]),
+                                                               __uint_as_float(rr[4 * u + 1]),
+                                                               __uint_as_float(rr[4 * u + 2]),
+                                                               __uint_as_float(rr[4 * u + 3])));
+                            }
+                        } else {
+                            __stcg(agg + kD * kD + (tb - 64), m->dzacc[tb - 64]);
+                            m->dzacc[tb - 64] = 0.f;
+                        }
+                        tc_fence_before();
+                        named_bar(2, 128);
+                        if (lead) {
+                            mbar_arrive(&m->dseg_free);
+                            __threadfence();
+                            st_release(p.flags + static_cast<size_t>(r.gA.s) * p.R + gi % p.R,
+                                       (static_cast<unsigned>(gi + 1) << 2) | 1u);
+                            mbar_arrive(&m->agg_pub[j & 1]);
+                        }
+                        ++nsegA;
+                    }
+                }
+                if (k < r.nC) {  // phase C: S_prev, z_prev of chunk ci
+                    const int b = ci & 1;
                     if (!group_ok(!lead || ci < 2 ||
                                       (bwait(&m->o_done[b], ((ci >> 1) & 1) ^ 1, abort) &&
                                        bwait(&m->epi_done[b], ((ci >> 1) & 1) ^ 1, abort)),
@@ -844,7 +1024,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                                             abort),
                                   2, 128) ||
                         !group_ok(!lead || k > 0 ||
-                                      bwait(&m->sin_ready[jp & 1], (jp >> 1) & 1, abort),
+                                      bwait(&m->sin_ready[jc & 1], (jc >> 1) & 1, abort),
                                   2, 128)) {
                         ok = false;
                         break;
@@ -857,7 +1037,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                         if (k == 0) {  // segment start: S_in from the look-back
                             const float4* src = reinterpret_cast<const float4*>(
                                 p.sin_scratch +
-                                (static_cast<size_t>(blockIdx.x) * 2 + (jp & 1)) * kStateFloats +
+                                (static_cast<size_t>(blockIdx.x) * 2 + (jc & 1)) * kStateFloats +
                                 tb * kD);
 #pragma unroll
                             for (int u = 0; u < 16; ++u) {
@@ -867,22 +1047,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                             }
 #pragma unroll
                             for (int q = 0; q < 4; ++q) {
-                                uint32_t r[16];
+                                uint32_t rr[16];
 #pragma unroll
                                 for (int u = 0; u < 16; ++u)
-                                    r[u] = __float_as_uint(sp[16 * q + u]);
-                                tmem_st16(tm + TM_SRUN + lane_off + 16 * q, r);
+                                    rr[u] = __float_as_uint(sp[16 * q + u]);
+                                tmem_st16(tm + TM_SRUN + lane_off + 16 * q, rr);
                             }
                             tmem_st_wait();
                         } else {
 #pragma unroll
                             for (int q = 0; q < 4; ++q) {
-                                uint32_t r[16];
-                                tmem_ld16(tm + TM_SRUN + lane_off + 16 * q, r);
+                                uint32_t rr[16];
+                                tmem_ld16(tm + TM_SRUN + lane_off + 16 * q, rr);
                                 tmem_ld_wait();
 #pragma unroll
                                 for (int u = 0; u < 16; ++u)
-                                    sp[16 * q + u] = __uint_as_float(r[u]);
+                                    sp[16 * q + u] = __uint_as_float(rr[u]);
                             }
                         }
 #pragma unroll
@@ -900,13 +1080,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                         float z;
                         if (k == 0)
                             z = __ldcg(p.sin_scratch +
-                                       (static_cast<size_t>(blockIdx.x) * 2 + (jp & 1)) *
+                                       (static_cast<size_t>(blockIdx.x) * 2 + (jc & 1)) *
                                            kStateFloats +
                                        kD * kD + i);
                         else
-                            z = m->zrun[i] + m->dzc[(ci - 1) & 1][0][i] +
-                                m->dzc[(ci - 1) & 1][1][i] + m->dzc[(ci - 1) & 1][2][i] +
-                                m->dzc[(ci - 1) & 1][3][i];
+                            z = m->zrun[i] + m->dzk[jc % NPH][k - 1][i];
                         m->zrun[i] = z;
                         m->zprev[b][i] = z;
                     }
@@ -915,134 +1093,57 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     named_bar(2, 128);
                     if (lead) {
                         if (k == 0)
-                            mbar_arrive(&m->sin_free[jp & 1]);
+                            mbar_arrive(&m->sin_free[jc & 1]);
                         mbar_arrive(&m->srun_read[b]);
                         TC_TRACE(ci, 4);
                     }
+                    ++ci, ++kvi;
                 }
             }
-            if (!ok || t >= p.total)
-                break;
-            prev = t;
+            h2 = h1;
+            h1 = tA;
         }
     } else if (warp >= 12) {
-        // ------------------------------ phi(Q), epilogue (warps 12-15) -----
+        // ----------------------------------------- phi(Q) (warps 12-15) ----
         const int tcx = tid - 384;
         const bool lead = tcx == 0;
-        const uint64_t pol = policy_evict_first();
-        unsigned char* sO = sm + OFF_O;
-        int ci = 0, prev = -1;
-        // the epilogue of a chunk runs after phi(Q) of the next one
-        int pend_ci = -1, pend_c = 0, pend_s = 0, pend_last = 0, pend_ss = 0;
-        auto epilogue = [&]() -> bool {
-            const int cj = pend_ci, b = cj & 1, qs = cj % NQ;
-            if (!group_ok(!lead || (bwait(&m->p_ready[b], (cj >> 1) & 1, abort) &&
-                                    bwait(&m->srun_read[b], (cj >> 1) & 1, abort) &&
-                                    bwait(&m->o_done[b], (cj >> 1) & 1, abort)),
-                          3, 128))
-                return false;
-            tc_fence_after();
-            if (lead)
-                TC_TRACE(cj, 5);
-            float den = 0.f;
-            if (norm) {
-                den = m->den[b][tcx];
-                const unsigned char* sQ = sm + OFF_Q + qs * 16384;
-                const float* z = m->zprev[b];
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(sQ + sw128_off(tcx, cc));
-                    const float* zz = z + 8 * cc;
-                    den = fmaf(bf_lo(x.x), zz[0], den);
-                    den = fmaf(bf_hi(x.x), zz[1], den);
-                    den = fmaf(bf_lo(x.y), zz[2], den);
-                    den = fmaf(bf_hi(x.y), zz[3], den);
-                    den = fmaf(bf_lo(x.z), zz[4], den);
-                    den = fmaf(bf_hi(x.z), zz[5], den);
-                    den = fmaf(bf_lo(x.w), zz[6], den);
-                    den = fmaf(bf_hi(x.w), zz[7], den);
-                }
-            }
-            const float inv = norm ? 1.0f / fmaxf(den, FLT_MIN) : 1.0f;
-            if (lead)
-                bulk_wait_read<0>();  // the previous tile has left the staging buffer
-            named_bar(3, 128);
-            uint32_t r[4][16];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                tmem_ld16(tm + TM_O + 64 * b + lane_off + 16 * q, r[q]);
-            tmem_ld_wait();
-            if (lead)
-                TC_TRACE(cj, 13);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int col4 = 4 * q + u;
-                    const float4 o = make_float4(__uint_as_float(r[q][4 * u]) * inv,
-                                                 __uint_as_float(r[q][4 * u + 1]) * inv,
-                                                 __uint_as_float(r[q][4 * u + 2]) * inv,
-                                                 __uint_as_float(r[q][4 * u + 3]) * inv);
-                    *reinterpret_cast<float4*>(sO + (col4 >> 3) * 16384 +
-                                               sw128_off(tcx, col4 & 7)) = o;
-                }
-            }
-            tc_fence_before();
-            fence_proxy_async_smem();
-            named_bar(3, 128);
-            if (lead) {
-                mbar_arrive(&m->o_free[b]);
-                mbar_arrive(&m->q_empty[qs]);
-                mbar_arrive(&m->epi_done[b]);
-                if (pend_last)
-                    mbar_arrive(&m->seg_empty[pend_ss]);
-                tma_store_3d(&p.mo, sO, 0, pend_c * kC, pend_s, pol);
-                tma_store_3d(&p.mo, sO + 16384, 32, pend_c * kC, pend_s, pol);
-                bulk_commit();
-                TC_TRACE(cj, 15);
-            }
-            pend_ci = -1;
-            return true;
-        };
-        bool ok = true;
+        int ci = 0, h1 = -1, h2 = -1;
+        bool ok = true, doneA = false;
         for (int j = 0; ok; ++j) {
-            const int ss = j % NS;
-            if (!group_ok(!lead || bwait(&m->seg_full[ss], (j / NS) & 1, abort), 3, 128))
+            int tA = -1;
+            if (!doneA) {
+                if (!group_ok(!lead || bwait(&m->seg_full[j % NS], (j / NS) & 1, abort), 3, 128))
+                    break;
+                const int t = m->seg_ticket[j % NS];
+                if (t < p.total)
+                    tA = t;
+                else
+                    doneA = true;
+            }
+            Round r;
+            round_setup(p, r, j, tA, h2);
+            if (r.nA == 0 && r.nC == 0 && h1 < 0)
                 break;
-            const int t = m->seg_ticket[ss];
-            if (prev >= 0) {
-                const Seg g = seg_of(p, prev);
-                for (int k = 0; k < g.n; ++k, ++ci) {
-                    const int qs = ci % NQ;
-                    if (!group_ok(!lead || bwait(&m->q_full[qs], (ci / NQ) & 1, abort), 3, 128)) {
-                        ok = false;
-                        break;
-                    }
-                    if (lead)
-                        TC_TRACE(ci, 12);
-                    phi_tile(sm + OFF_Q + qs * 16384, tcx, chunk_valid(p, g.c0 + k), elu, nullptr);
-                    fence_proxy_async_smem();
-                    named_bar(3, 128);
-                    if (lead) {
-                        mbar_arrive(&m->q_phi[qs]);
-                        TC_TRACE(ci, 1);
-                    }
-                    if (pend_ci >= 0 && !epilogue()) {
-                        ok = false;
-                        break;
-                    }
-                    pend_ci = ci, pend_c = g.c0 + k, pend_s = g.s;
-                    pend_last = k == g.n - 1, pend_ss = (j - 1) % NS;
+            for (int k = 0; k < r.nC; ++k, ++ci) {
+                const int qs = ci % NQ;
+                if (!group_ok(!lead || bwait(&m->q_full[qs], (ci / NQ) & 1, abort), 3, 128)) {
+                    ok = false;
+                    break;
+                }
+                if (lead)
+                    TC_TRACE(ci, 12);
+                phi_tile(sm + OFF_Q + qs * 16384, tcx, chunk_valid(p, r.gC.c0 + k), elu, nullptr,
+                         nullptr);
+                fence_proxy_async_smem();
+                named_bar(3, 128);
+                if (lead) {
+                    mbar_arrive(&m->q_phi[qs]);
+                    TC_TRACE(ci, 1);
                 }
             }
-            if (t >= p.total)
-                break;
-            prev = t;
+            h2 = h1;
+            h1 = tA;
         }
-        if (ok && pend_ci >= 0)
-            epilogue();
-        if (lead)
-            bulk_wait<0>();
     }
 
     // ---- teardown
@@ -1095,7 +1196,7 @@ struct TcGeom {
     int nseg;
     int R;       // ring slots per sequence
     int total;   // segment tickets
-    size_t flags_off, slots_off, sin_off, bytes;
+    size_t flags_off, slots_off, sin_off, phi_off, bytes;
 };
 
 int sm_count()
@@ -1116,7 +1217,7 @@ TcGeom tc_geom(int64_t BH, int64_t N, int sms)
     const int64_t chunks = BH * g.nchunk;
     // about a dozen segments per CTA keeps the tail short; long segments make
     // the look-back rare
-    g.L = (int)std::max<int64_t>(1, std::min<int64_t>(8, chunks / ((int64_t)sms * 12)));
+    g.L = (int)std::max<int64_t>(1, std::min<int64_t>(kMaxL, chunks / ((int64_t)sms * 12)));
     g.nseg = (g.nchunk + g.L - 1) / g.L;
     g.total = (int)(BH * g.nseg);
     int G = sms;
@@ -1131,7 +1232,8 @@ TcGeom tc_geom(int64_t BH, int64_t N, int sms)
     g.flags_off = 256;
     g.slots_off = (g.flags_off + sizeof(unsigned) * (size_t)BH * g.R + 255) & ~(size_t)255;
     g.sin_off = g.slots_off + sizeof(float) * (size_t)BH * g.R * kSlotFloats;
-    g.bytes = g.sin_off + sizeof(float) * (size_t)G * 2 * kStateFloats;
+    g.phi_off = (g.sin_off + sizeof(float) * (size_t)G * 2 * kStateFloats + 1023) & ~(size_t)1023;
+    g.bytes = g.phi_off + (size_t)G * NPH * g.L * kC * kD * 2;
     return g;
 }
 
@@ -1162,6 +1264,9 @@ cudaError_t tc_forward(const FwdArgs& a)
         !make_map(&p.mo, a.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 64, a.N, BH, 32))
         return cudaErrorInvalidValue;
     unsigned char* ws = static_cast<unsigned char*>(a.ws);
+    if (!make_map(&p.mphi, ws + g.phi_off, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, kC,
+                  (int64_t)g.G * NPH * g.L, 64))
+        return cudaErrorInvalidValue;
     p.N = a.N;
     p.BH = (int)BH;
     p.nchunk = g.nchunk;
@@ -1174,6 +1279,7 @@ cudaError_t tc_forward(const FwdArgs& a)
     p.flags = reinterpret_cast<unsigned*>(ws + g.flags_off);
     p.slots = reinterpret_cast<float*>(ws + g.slots_off);
     p.sin_scratch = reinterpret_cast<float*>(ws + g.sin_off);
+    p.phi_scratch = ws + g.phi_off;
     p.status = a.status;
     cudaError_t e = cudaMemsetAsync(ws, 0, g.slots_off, a.stream);
     if (e != cudaSuccess)
