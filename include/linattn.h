@@ -184,7 +184,7 @@ LA_API la_status la_decode_step(float* S, float* z, const void* q, const void* k
  * results: serialise them.  All other arguments and results are exactly
  * those of la_forward.
  */
-#define LA_NOALLOC_SCRATCH_BYTES (32u << 20)
+#define LA_NOALLOC_SCRATCH_BYTES (64u << 20)
 LA_API la_status la_forward_noalloc(const void* q, const void* k, const void* v, float* out,
                                     int64_t B, int64_t H, int64_t N, int d, int dv, int causal,
                                     int feature_map, const float* gamma, int dtype,

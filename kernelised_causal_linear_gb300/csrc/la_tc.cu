@@ -9,54 +9,61 @@
 // every earlier token:
 //
 //   P     = tril(phi(Q_c) phi(K_c)^T)                      (fp32, tensor memory)
-//   num   = P V_c + phi(Q_c) S_prev                        (tensor cores)
-//   den   = rowsum(P) + phi(Q_c) z_prev                    (CUDA cores, fp32)
+//   [num | den] = P [V_c | 1] + phi(Q_c) [S_prev | z_prev] (tensor cores)
 //   o     = num / max(den, FLT_MIN)
 //   dS_c  = phi(K_c)^T V_c,  dz_c = column sums of phi(K_c)
 //
 // ("Linear Attention Kernel", section "Rewrite: associativity": phi(K)^T V
 // is the only intermediate; "Efficient Attention Variants", section 5: the
-// prefix state S_t, z_t and the normalised read).
+// prefix state S_t, z_t and the normalised read).  The ones column of
+// [V_c | 1] makes the row sums of P, and the extra column z_prev of the state
+// operand makes phi(q).z_prev, in the same accumulator as the numerator.
 //
 // Chunks are grouped into segments of L consecutive chunks of one sequence.
 // One persistent CTA per SM takes segments in ticket order (segment-major over
 // the B*H sequences) and runs each in two phases:
-//   A  the segment's aggregate: K, V of every chunk (kept in L2 with an
-//      evict-last hint), phi(K), dS accumulated on the tensor cores, dz;
-//      published at once to a ring of per-segment slots in global memory;
-//   C  the outputs: Q, K, V again (K, V from L2), with the running state
-//      S_prev = S_in + the segment's earlier chunks carried in tensor memory.
+//   A  K, V of every chunk (V kept in L2 with an evict-last hint); phi(K),
+//      also kept in a scratch ring for phase C; the segment's running sum of
+//      [dS^T; dz] accumulated on the tensor cores and, after every chunk but
+//      the last, copied out as a prefix snapshot; the total (the aggregate) is
+//      published to a ring of per-segment slots in global memory;
+//   C  the outputs: Q, phi(K) (scratch) and V (L2); S_prev of chunk k is
+//      S_in + the snapshot after chunk k-1, so the chunks of a segment do not
+//      wait on each other.
 // Between them a decoupled look-back over the predecessors' slots gives S_in,
 // the state before the segment, and publishes the segment's inclusive prefix.
-// Phase A of segment j+1 runs before phase C of segment j, so the look-back
-// of segment j is hidden behind it.  The look-back starts from the nearest
-// inclusive prefix and adds later aggregates in segment order, so every
-// prefix is the same left-to-right fp32 sum whatever the timing: results are
-// bitwise reproducible.
+// Round j interleaves phase A of local segment j with phase C of segment j-1,
+// chunk by chunk, so the look-back of a segment is hidden behind a round.
+// The look-back starts from the nearest inclusive prefix and adds later
+// aggregates in segment order, so every prefix is the same left-to-right fp32
+// sum whatever the timing: results are bitwise reproducible.
 //
-// The CTA is warp-specialised; work flows through rings of shared-memory
-// stages and tensor-memory buffers, synchronised by mbarriers:
-//   warp 0      producer: segment tickets, TMA loads
-//   warp 1      MMA issuer: segment aggregate, scores, chunk state, P V,
-//               phi(Q) S_prev
-//   warps 2-3   look-back over the predecessors' slots, S_in, inclusive prefix
-//   warps 4-7   phi(K) in place and its column sums (phases A and C); P:
-//               causal mask, row sums, bf16 hi/lo re-pack in tensor memory
-//   warps 8-11  segment aggregate out of tensor memory and published; running
-//               state S_prev as bf16 hi/lo for the tensor cores, z_prev
-//   warps 12-15 phi(Q) in place (one chunk ahead), epilogue: denominator,
-//               output tile by TMA store
+// [V | e] (V and a constant 2 KiB block e whose first column is all ones)
+// is read in two places: as the A operand of the state MMAs, where D =
+// [V | e]^T phi(K) holds dS^T in lanes 0..63 and dz in lane 64, and as the B
+// operand of P [V | e], whose column 64 is rowsum(P).
+//
+// The CTA is warp-specialised; work flows through shared-memory stages and
+// tensor-memory buffers, synchronised by mbarriers:
+//   warp 0      producer: segment tickets, phase-A loads (K, V)
+//   warps 2, 3  producers: phase-C loads (Q, phi(K), V) of output warpgroup
+//               0 and 1
+//   warps 4-7   phase A: phi(K) in place and to the scratch ring; the
+//               segment's running [dS^T; dz] on the tensor cores and its
+//               snapshots; the aggregate; then, one segment behind, the
+//               look-back that yields S_in and the inclusive prefix (the
+//               predecessors' prefixes are mostly published by then)
+//   warps 8-11, 12-15
+//               output warpgroups 0 and 1, taking alternate chunks: S_prev
+//               from S_in and the snapshot, phi(Q), scores, P (causal mask,
+//               bf16 hi/lo in place), [num | den], epilogue and TMA store,
+//               each issuing its own MMAs.  Two chunks are in flight at once,
+//               so one group's MMAs and loads overlap the other's arithmetic.
+//   warp 1      idle
 //
 // Precision: phi(Q), phi(K) and V enter the MMAs as bf16 (phi rounded once);
 // P and S_prev are fp32 and enter as a bf16 hi/lo pair (two MMAs each), so
 // their rounding is ~2^-17 relative; states and denominators stay fp32.
-//
-// Operands: Q, K, V chunks arrive by TMA in the 128-byte swizzled layout.
-// The scores MMA reads Q and K K-major; the state MMAs read [V | phi(K)] as an
-// MN-major A of 128 rows (the second 64 rows are discarded) against phi(K)
-// MN-major, giving dS^T in lanes 0..63; P's hi/lo parts sit in tensor memory
-// as the A operand of P V; S_prev^T hi/lo sit in shared memory K-major for
-// phi(Q) S_prev.
 //
 // Every wait is bounded (%globaltimer); on expiry the CTA records
 // LA_ERR_TIMEOUT, every role leaves its loop, the CTA drains its own TMA loads,
@@ -78,31 +85,37 @@ using namespace sm100;
 constexpr int kC = 128;        // tokens per chunk
 constexpr int kD = 64;         // d = dv
 constexpr int kThreads = 512;  // 16 warps
-constexpr int NQ = 3;          // Q stages
-constexpr int NKV = 3;         // K,V stages
 constexpr int NS = 4;          // segment-ticket ring
+constexpr int NSIN = 4;        // S_in ring (a segment's S_in lives through its phase C)
 constexpr int kStateFloats = kD * kD + kD;         // S^T (dv x d) then z (d)
 constexpr int kSlotFloats = 2 * kStateFloats;      // aggregate, inclusive
 constexpr int kMaxList = 128;                      // look-back entries
 constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s for any single wait
 
 // shared memory (offsets from a 1024-byte aligned base)
-constexpr uint32_t OFF_Q = 0;                          // NQ x (128 x 64 bf16)
-constexpr uint32_t OFF_KV = OFF_Q + NQ * 16384;        // NKV x (V then K)
-constexpr uint32_t OFF_S = OFF_KV + NKV * 32768;       // 2 x (S^T hi, S^T lo)
-constexpr uint32_t OFF_O = OFF_S + 2 * 16384;          // output staging 2 x 16 KiB
-constexpr uint32_t OFF_MISC = OFF_O + 32768;
-constexpr uint32_t kMiscBytes = 16384;
+constexpr int kON = 80;                                // output accumulator: num (64), den, pad
+constexpr uint32_t kSBytes = kON * 128;                // [S_prev^T; z_prev] bf16, 80 x 64
+constexpr int NA = 2;                                  // phase-A K,V stages
+// per output warpgroup: Q, V (later the fp32 output staging), phi(K), S hi/lo
+constexpr uint32_t CW_Q = 0, CW_V = 16384, CW_K = 32768, CW_S = 49152;
+constexpr uint32_t kCWBytes = CW_S + 2 * kSBytes;
+constexpr uint32_t OFF_CW = 0;                         // 2 x kCWBytes
+constexpr uint32_t OFF_A = OFF_CW + 2 * kCWBytes;      // NA x (V then K)
+constexpr uint32_t OFF_MISC = OFF_A + NA * 32768;
+constexpr uint32_t kMiscBytes = 2048;
+constexpr uint32_t OFF_ONES = OFF_MISC + kMiscBytes;   // 2 KiB: the e rows of [V | e]
 constexpr int kMaxL = 8;       // largest segment (chunks)
-constexpr int NPH = 4;         // phi(K) scratch ring depth, in segments
-constexpr uint32_t SMEM_BYTES = OFF_MISC + kMiscBytes + 1024;  // + alignment slack
+constexpr int NPH = 4;         // phi(K) scratch and snapshot ring depth, in segments
+constexpr uint32_t SMEM_BYTES = OFF_ONES + 2048 + 1024;  // + alignment slack
+static_assert(OFF_ONES % 1024 == 0 && kCWBytes % 1024 == 0 && kSBytes % 1024 == 0 &&
+                  CW_V == CW_Q + 16384,
+              "layout");
+static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 // tensor memory columns
-constexpr uint32_t TM_P = 0;       // scores fp32, 128 columns
-constexpr uint32_t TM_PHL = 128;   // P hi (128..191), P lo (192..255), bf16 pairs
-constexpr uint32_t TM_O = 256;     // 2 x 64: output accumulators
-constexpr uint32_t TM_SRUN = 384;  // running S_prev^T (lanes 0..63)
-constexpr uint32_t TM_DSEG = 448;  // segment aggregate dS^T (lanes 0..63)
+constexpr uint32_t TM_P = 0;       // 2 x 128: scores fp32, then P hi/lo in place
+constexpr uint32_t TM_O = 256;     // 2 x 80: [num | den] accumulators
+constexpr uint32_t TM_DSEG = 448;  // segment aggregate so far [dS^T; dz] (lanes 0..64)
 
 struct TcParams {
     CUtensorMap mq, mk, mv, mo;
@@ -118,31 +131,24 @@ struct TcParams {
     unsigned* counter;
     unsigned* flags;
     float* slots;
-    float* sin_scratch;  // per CTA: 2 x S_in
+    float* sin_scratch;  // per CTA: NSIN x S_in
     void* phi_scratch;   // the tiles mphi describes
+    float* snap;         // per CTA: NPH x (L-1) prefix snapshots [S^T; z]
+    float* out;          // [BH][N][64] fp32
     int* status;
 };
 
 struct Misc {
     uint64_t seg_full[NS], seg_empty[NS];
-    uint64_t q_full[NQ], q_empty[NQ], q_phi[NQ];
-    uint64_t kv_full[NKV], kv_empty[NKV], aphi[NKV], phik_stored[NPH];
-    uint64_t mma1_done[2], p_ready[2], pv_done[2], srun_read[2], o_done[2], o_free[2];
-    uint64_t epi_done[2];
-    uint64_t dseg_done, dseg_free, dzseg_ready[2], agg_pub[2], sin_ready[2], sin_free[2];
-    uint64_t drain;
+    uint64_t a_full[NA], a_empty[NA];
+    uint64_t c_full[2], k_free[2], qv_free[2], s_done[2], o_done[2];
+    uint64_t phik_stored[NPH], dseg_done, sin_ready[NSIN], sin_free[NSIN];
+    uint64_t drain[3];
     uint32_t tmem;
     int abort;
     int seg_ticket[NS];
     int nlist;
     int list[kMaxList];
-    float den[2][kC];
-    alignas(16) float zprev[2][kD];
-    float zrun[kD];
-    float dza[4][kD];        // per A chunk: column sums of phi(K), one row per warp
-    float dzacc[kD];         // running column sums over the current A segment
-    float dzk[NPH][kMaxL][kD];  // per chunk column sums, kept for phase C
-    float dzseg[2][kD];
 };
 static_assert(sizeof(Misc) <= kMiscBytes, "misc");
 
@@ -180,13 +186,21 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p)
     return v;
 }
 
+// Drop a 128-byte L2 line without writing it back (scratch read for the last
+// time).
+__device__ __forceinline__ void l2_discard(const void* ptr)
+{
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(ptr) : "memory");
+}
+
 __device__ __forceinline__ void named_bar(int id, int count)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile int* abort)
+// Bounded wait that also gives up as soon as another role has aborted.  The
+// first test is inline; the sleeping loop is one shared out-of-line copy.
+__device__ __noinline__ bool bwait_slow(uint64_t* bar, uint32_t parity, volatile int* abort)
 {
     uint64_t t0 = 0;
     for (uint32_t n = 1;; ++n) {
@@ -204,6 +218,11 @@ __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile i
             }
         }
     }
+}
+
+__device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile int* abort)
+{
+    return mbar_test_wait(bar, parity) || bwait_slow(bar, parity, abort);
 }
 
 // A thread group waits through one leader; bar.red hands every thread the
@@ -232,88 +251,106 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity)
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __forceinline__ uint32_t bf2_min0(uint32_t w)
+// Packed fp32 pair arithmetic (two lanes of work per instruction).
+__device__ __forceinline__ float2 sub2(float2 a, float2 b)
 {
-    uint32_t r;
-    asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(0u));
+    float2 r;
+    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+        "sub.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return r;
 }
 
-__device__ __forceinline__ uint32_t bf2_max0(uint32_t w)
+__device__ __forceinline__ float2 add2(float2 a, float2 b)
 {
-    uint32_t r;
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(0u));
+    float2 r;
+    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+        "add.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return r;
 }
 
-__device__ __forceinline__ uint32_t bf2_add(uint32_t a, uint32_t b)
-{
-    uint32_t r;
-    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
-// elu(x)+1 on two packed bf16: max(x,0) + exp(min(x,0)).  One of the two
-// terms is always exact (0, or exp(0) = 1), so rounding exp(min(x,0)) to bf16
-// first and adding in bf16 gives the correctly rounded result of the fp32 sum.
-__device__ __forceinline__ uint32_t phi2(uint32_t w)
-{
-    const uint32_t mn = bf2_min0(w);
-    return bf2_add(bf2_max0(w), pack_bf16x2(__expf(bf_lo(mn)), __expf(bf_hi(mn))));
-}
-
-// split two fp32 into packed bf16 hi and lo parts
+// split two fp32 into packed bf16 hi and lo parts (hi + lo = x to ~2^-17)
 __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo)
 {
     hi = pack_bf16x2(a, b);
-    lo = pack_bf16x2(a - bf_lo(hi), b - bf_hi(hi));
+    const float2 r = sub2(make_float2(a, b), make_float2(bf_lo(hi), bf_hi(hi)));
+    lo = pack_bf16x2(r.x, r.y);
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+        "mul.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+__device__ __forceinline__ float ex2(float t)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+    return r;
+}
+
+// elu(x)+1 on two packed bf16: max(x,0) + exp(min(x,0)), with
+// exp(u) = 2^(u log2 e) on the hardware base-2 exponential; the fp32 result is
+// rounded once to bf16.
+__device__ __forceinline__ uint32_t phi2(uint32_t w)
+{
+    const float a = bf_lo(w), b = bf_hi(w);
+    const float2 t = mul2(make_float2(fminf(a, 0.f), fminf(b, 0.f)),
+                          make_float2(1.4426950408889634f, 1.4426950408889634f));
+    const float2 r = add2(make_float2(fmaxf(a, 0.f), fmaxf(b, 0.f)), make_float2(ex2(t.x), ex2(t.y)));
+    return pack_bf16x2(r.x, r.y);
 }
 
 // Feature map in place on a 128 x 64 bf16 tile (128-byte swizzle) by 128
-// threads; rows >= valid become zero.  With zsum, also the column sums of the
-// result: zsum[warp][64] (rows of this warp's threads only).  With gdst, the
-// result is also written to global memory as a plain row-major 128 x 64 tile.
-__device__ __noinline__ void phi_tile(unsigned char* tile, int t, int valid, bool elu,
-                                     float (*zsum)[kD], uint4* gdst)
+// threads; rows >= valid become zero.  With gdst, the result is also written
+// to global memory as a plain row-major 128 x 64 tile.
+__device__ __forceinline__ void phi_tile(unsigned char* tile, int t, int valid, bool elu, uint4* gdst)
 {
     const int cc = t & 7, r0 = t >> 3;
-    uint4 x[8];
+#pragma unroll 2
+    for (int mm = 0; mm < 8; mm += 2) {
+        uint4 x[2];
 #pragma unroll
-    for (int mm = 0; mm < 8; ++mm)
-        x[mm] = *reinterpret_cast<const uint4*>(tile + sw128_off(r0 + 16 * mm, cc));
+        for (int u = 0; u < 2; ++u)
+            x[u] = *reinterpret_cast<const uint4*>(tile + sw128_off(r0 + 16 * (mm + u), cc));
 #pragma unroll
-    for (int mm = 0; mm < 8; ++mm) {
-        const int r = r0 + 16 * mm;
-        if (r >= valid)
-            x[mm] = make_uint4(0, 0, 0, 0);
-        else if (elu)
-            x[mm] = make_uint4(phi2(x[mm].x), phi2(x[mm].y), phi2(x[mm].z), phi2(x[mm].w));
-        if (r >= valid || elu)
-            *reinterpret_cast<uint4*>(tile + sw128_off(r, cc)) = x[mm];
-        if (gdst)
-            gdst[r * 8 + cc] = x[mm];
+        for (int u = 0; u < 2; ++u) {
+            const int r = r0 + 16 * (mm + u);
+            if (r >= valid)
+                x[u] = make_uint4(0, 0, 0, 0);
+            else if (elu)
+                x[u] = make_uint4(phi2(x[u].x), phi2(x[u].y), phi2(x[u].z), phi2(x[u].w));
+            if (r >= valid || elu)
+                *reinterpret_cast<uint4*>(tile + sw128_off(r, cc)) = x[u];
+            if (gdst)
+                gdst[r * 8 + cc] = x[u];
+        }
     }
-    if (zsum) {
-        float zp[8];
+}
+
+// D (+)= [V | e]^T phi(K) over one 128-token stage: V at vaddr and phi(K) at
+// kaddr (MN-major, 128-byte swizzle), e the constant block at `ones`.  The
+// second 64 rows of A are read at start + LBO; every K step advances the start
+// by 2 KiB, so LBO shrinks by the same amount to keep hitting the one block.
+// Executed by a whole warp; the lane with `issue` set issues.
+__device__ __forceinline__ void state_mma(uint32_t d, uint32_t vaddr, uint32_t kaddr,
+                                          uint32_t ones, bool acc, uint32_t issue)
+{
+    const uint32_t id = idesc_bf16_f32(128, 64, true, true);
+    const uint64_t a0 = sdesc_sw128(vaddr, ones - vaddr, 1024);
+    const uint64_t b0 = sdesc_sw128(kaddr, 16, 1024);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            zp[e] = 0.f;
-#pragma unroll
-        for (int mm = 0; mm < 8; ++mm) {
-            zp[0] += bf_lo(x[mm].x), zp[1] += bf_hi(x[mm].x);
-            zp[2] += bf_lo(x[mm].y), zp[3] += bf_hi(x[mm].y);
-            zp[4] += bf_lo(x[mm].z), zp[5] += bf_hi(x[mm].z);
-            zp[6] += bf_lo(x[mm].w), zp[7] += bf_hi(x[mm].w);
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            zp[e] += __shfl_xor_sync(0xffffffffu, zp[e], 8);
-            zp[e] += __shfl_xor_sync(0xffffffffu, zp[e], 16);
-        }
-        if ((t & 31) < 8)
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                zsum[(t >> 5) & 3][8 * cc + e] = zp[e];
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t step = static_cast<uint64_t>(kk * 128);
+        mma_bf16_ss_w(d, a0 + step - (step << 16), b0 + step, id, acc || kk > 0, issue);
     }
 }
 
@@ -342,9 +379,9 @@ __device__ __forceinline__ int chunk_valid(const TcParams& p, int c)
 }
 
 // Job order shared by every role.  Round j holds phase A of local segment j
-// and phase C of local segment j-2, interleaved chunk by chunk
-// (A0 C0 A1 C1 ...); the two rounds between a segment's phases hide its
-// look-back.
+// and phase C of local segment j-kLag, interleaved chunk by chunk
+// (A0 C0 A1 C1 ...); the rounds between a segment's phases hide its look-back.
+constexpr int kLag = 2;
 struct Round {
     int j;        // round = local index of the A segment
     int tA, tC;   // tickets of the A and C segments (-1: none)
@@ -368,6 +405,37 @@ __device__ __forceinline__ void round_setup(const TcParams& p, Round& r, int j, 
     }
 }
 
+// Every role but the producer walks the same rounds: it learns the A ticket
+// of round j from the producer's ring (seg_full) and carries the C ticket kLag
+// rounds behind.  A thread group waits through its leader on named barrier
+// `barid` (a single thread passes barid < 0).  Returns false when the CTA has
+// no more work (or aborted).
+struct RoundWalker {
+    int h1 = -1, h2 = -1;
+    bool doneA = false;
+    __device__ __forceinline__ bool next(const TcParams& p, Misc* m, Round& r, int j, bool lead,
+                                         int barid, int count, volatile int* abort)
+    {
+        int tA = -1;
+        if (!doneA) {
+            int okw = !lead || bwait(&m->seg_full[j % NS], (j / NS) & 1, abort);
+            if (barid >= 0)
+                okw = group_ok(okw, barid, count);
+            if (!okw)
+                return false;
+            const int t = m->seg_ticket[j % NS];
+            if (t < p.total)
+                tA = t;
+            else
+                doneA = true;
+        }
+        round_setup(p, r, j, tA, kLag == 1 ? h1 : h2);
+        h2 = h1;
+        h1 = tA;
+        return !(r.nA == 0 && r.nC == 0 && (kLag == 1 || h2 < 0));
+    }
+};
+
 __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant__ TcParams p)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -378,12 +446,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool norm = p.fm != LA_FM_NONE;
     const bool elu = p.fm == LA_FM_ELU1;
+    const int Ls = max(p.L - 1, 1);  // prefix snapshots per segment
+    const unsigned full = 0xffffffffu;
 
     if (tid == 0) {
         uint64_t* bars = reinterpret_cast<uint64_t*>(m);
-        const int nbars = static_cast<int>((reinterpret_cast<uint64_t*>(&m->drain) - bars) + 1);
+        const int nbars = static_cast<int>((reinterpret_cast<uint64_t*>(&m->drain[2]) - bars) + 1);
         for (int i = 0; i < nbars; ++i)
             mbar_init(&bars[i], 1);
+        // both output warpgroups release a ticket slot and an S_in buffer
+        for (int i = 0; i < NS; ++i)
+            mbar_init(&m->seg_empty[i], 2);
+        for (int i = 0; i < NSIN; ++i)
+            mbar_init(&m->sin_free[i], 2);
         m->abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&p.mq);
@@ -392,8 +467,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
         tma_prefetch_desc(&p.mo);
         tma_prefetch_desc(&p.mphi);
     }
-    if (tid < kD)
-        m->dzacc[tid] = 0.f;
+    // the e block of [V | e]: element 0 of each of its 16 rows is 1, the rest 0
+    // (128-byte swizzle: 16-byte chunk 0 of row r sits at chunk r & 7)
+    if (tid < 128) {
+        const int r = tid >> 3, c = tid & 7;
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (c == (r & 7))
+            w.x = 0x3F80u;  // bf16 1.0 in the low half
+        *reinterpret_cast<uint4*>(sm + OFF_ONES + r * 128 + c * 16) = w;
+    }
+    // rows 65..79 of the [S_prev^T; z_prev] operands (hi and lo, both
+    // warpgroups) stay zero
+    for (int i = tid; i < 4 * 15 * 8; i += kThreads) {
+        const int t = i / 120, rr = 65 + (i % 120) / 8, c = i % 8;
+        *reinterpret_cast<uint4*>(sm + OFF_CW + (t >> 1) * kCWBytes + CW_S + (t & 1) * kSBytes +
+                                  rr * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
     if (warp == 0) {
         tmem_alloc(&m->tmem, 512);
         tmem_relinquish();
@@ -403,227 +493,160 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
     tc_fence_after();
     const uint32_t tm = m->tmem;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t ones = smem_addr(sm + OFF_ONES);
     // phi(K) scratch tile of local segment jj, chunk k
     auto phi_index = [&](int jj, int k) {
         return (static_cast<int>(blockIdx.x) * NPH + jj % NPH) * p.L + k;
     };
+    // prefix snapshot [S^T; z] after chunk k of local segment jj
+    auto snap_ptr = [&](int jj, int k) {
+        return p.snap +
+               (static_cast<size_t>((static_cast<int>(blockIdx.x) * NPH + jj % NPH) * Ls + k)) *
+                   kStateFloats;
+    };
 
     if (warp == 0) {
-        // ------------------------------------------------------ producer --
+        // --------------------------------- producer: tickets, phase-A loads --
         if (lane == 0) {
             const uint64_t keep = policy_evict_last();
             const uint64_t stream = policy_evict_first();
-            int q_last[NQ], kv_last[NKV];
-            for (int j = 0; j < NQ; ++j)
-                q_last[j] = -1;
-            for (int j = 0; j < NKV; ++j)
-                kv_last[j] = -1;
-            int kvi = 0, ci = 0, h1 = -1, h2 = -1;
-            bool ok = true, doneA = false;
-            // K (or, in phase C, phi(K) from the scratch tile `phi`) and V
-            auto load_kv = [&](const Seg& g, int c, uint64_t pol, int phi) -> bool {
-                const int ks = kvi % NKV;
-                if (kvi >= NKV && !bwait(&m->kv_empty[ks], ((kvi / NKV) & 1) ^ 1, abort))
-                    return false;
-                mbar_arrive_expect_tx(&m->kv_full[ks], 2 * kC * kD * 2);
-                unsigned char* kv = sm + OFF_KV + ks * 32768;
-                if (phi >= 0)
-                    tma_load_3d(kv + 16384, &p.mphi, 0, 0, phi, &m->kv_full[ks], pol);
-                else
-                    tma_load_3d(kv + 16384, &p.mk, 0, c * kC, g.s, &m->kv_full[ks], pol);
-                tma_load_3d(kv, &p.mv, 0, c * kC, g.s, &m->kv_full[ks], pol);
-                kv_last[ks] = kvi / NKV;
-                ++kvi;
-                return true;
-            };
-            for (int j = 0; ok; ++j) {
-                int tA = -1;
-                if (!doneA) {
-                    const int t = static_cast<int>(atomicAdd(p.counter, 1u));
-                    const int ss = j % NS;
-                    if (j >= NS && !bwait(&m->seg_empty[ss], ((j / NS) & 1) ^ 1, abort))
+            int a_last[NA];
+            for (int i = 0; i < NA; ++i)
+                a_last[i] = -1;
+            int ai = 0;
+            for (int j = 0;; ++j) {
+                const int ss = j % NS;
+                if (j >= NS && !bwait(&m->seg_empty[ss], ((j / NS) & 1) ^ 1, abort))
+                    break;
+                const int t = static_cast<int>(atomicAdd(p.counter, 1u));
+                m->seg_ticket[ss] = t;
+                mbar_arrive(&m->seg_full[ss]);
+                if (t >= p.total)
+                    break;
+                const Seg g = seg_of(p, t);
+                bool ok = true;
+                for (int k = 0; k < g.n; ++k, ++ai) {
+                    const int s = ai % NA;
+                    if (ai >= NA && !bwait(&m->a_empty[s], ((ai / NA) & 1) ^ 1, abort)) {
+                        ok = false;
                         break;
-                    m->seg_ticket[ss] = t;
-                    mbar_arrive(&m->seg_full[ss]);
-                    if (t < p.total)
-                        tA = t;
-                    else
-                        doneA = true;
-                }
-                Round r;
-                round_setup(p, r, j, tA, h2);
-                if (r.nA == 0 && r.nC == 0 && h1 < 0)
-                    break;
-                const int jc = j - 2;
-                if (r.nC && !bwait(&m->phik_stored[jc % NPH], (jc / NPH) & 1, abort))
-                    break;
-                for (int k = 0; k < max(r.nA, r.nC) && ok; ++k) {
-                    if (k < r.nA)
-                        ok = load_kv(r.gA, r.gA.c0 + k, keep, -1);
-                    if (k < r.nC && ok) {
-                        const int qs = ci % NQ;
-                        if (ci >= NQ && !bwait(&m->q_empty[qs], ((ci / NQ) & 1) ^ 1, abort)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&m->q_full[qs], kC * kD * 2);
-                        tma_load_3d(sm + OFF_Q + qs * 16384, &p.mq, 0, (r.gC.c0 + k) * kC,
-                                    r.gC.s, &m->q_full[qs], stream);
-                        q_last[qs] = ci / NQ;
-                        TC_TRACE(ci, 0);
-                        ++ci;
-                        ok = load_kv(r.gC, r.gC.c0 + k, stream, phi_index(jc, k));
                     }
+                    mbar_arrive_expect_tx(&m->a_full[s], 2 * kC * kD * 2);
+                    unsigned char* st = sm + OFF_A + s * 32768;
+                    tma_load_3d(st + 16384, &p.mk, 0, (g.c0 + k) * kC, g.s, &m->a_full[s], stream);
+                    tma_load_3d(st, &p.mv, 0, (g.c0 + k) * kC, g.s, &m->a_full[s], keep);
+                    a_last[s] = ai / NA;
                 }
-                h2 = h1;
-                h1 = tA;
-            }
-            if (*abort) {  // let every load this thread issued land before exit
-                for (int j = 0; j < NQ; ++j)
-                    if (q_last[j] >= 0)
-                        drain_wait(&m->q_full[j], q_last[j] & 1);
-                for (int j = 0; j < NKV; ++j)
-                    if (kv_last[j] >= 0)
-                        drain_wait(&m->kv_full[j], kv_last[j] & 1);
-            }
-        }
-    } else if (warp == 1) {
-        // ---------------------------------------------------- MMA issuer --
-        if (lane == 0) {
-            const uint32_t id_sc = idesc_bf16_f32(128, 128, false, false);
-            const uint32_t id_st = idesc_bf16_f32(128, 64, true, true);
-            const uint32_t id_pv = idesc_bf16_f32(128, 64, false, true);
-            const uint32_t id_in = idesc_bf16_f32(128, 64, false, false);
-            // Operand descriptors of stage 0; a stage or K-step offset of x bytes
-            // adds x >> 4 to the start-address field.
-            const uint64_t dq0 = sdesc_sw128(smem_addr(sm + OFF_Q), 16, 1024);
-            const uint32_t v0 = smem_addr(sm + OFF_KV);
-            const uint64_t dk0 = sdesc_sw128(v0 + 16384, 16, 1024);
-            const uint64_t dvm0 = sdesc_sw128(v0, 16384, 1024);  // [V | phi(K)]: one 128-row A
-            const uint64_t dvb0 = sdesc_sw128(v0, 16, 1024);
-            const uint64_t ds0 = sdesc_sw128(smem_addr(sm + OFF_S), 16, 1024);
-            auto dq = [&](int i) { return dq0 + (uint64_t)(i * (16384 >> 4)); };
-            auto dk = [&](int i) { return dk0 + (uint64_t)(i * (32768 >> 4)); };
-            auto dvm = [&](int i) { return dvm0 + (uint64_t)(i * (32768 >> 4)); };
-            auto dvb = [&](int i) { return dvb0 + (uint64_t)(i * (32768 >> 4)); };
-            auto ds = [&](int i) { return ds0 + (uint64_t)(i * (16384 >> 4)); };
-            bool issued = false, ok = true, doneA = false;
-            int kvi = 0, ci = 0, ai = 0, nsegA = 0, h1 = -1, h2 = -1;
-            // [V | phi(K)]^T phi(K) of stage ks accumulated into d
-            auto state_mma = [&](uint32_t d, int ks, bool acc) {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16_ss(d, dvm(ks) + 128 * kk, dk(ks) + 128 * kk, id_st, acc || kk > 0);
-            };
-            for (int j = 0; ok; ++j) {
-                int tA = -1;
-                if (!doneA) {
-                    if (!bwait(&m->seg_full[j % NS], (j / NS) & 1, abort))
-                        break;
-                    const int t = m->seg_ticket[j % NS];
-                    if (t < p.total)
-                        tA = t;
-                    else
-                        doneA = true;
-                }
-                Round r;
-                round_setup(p, r, j, tA, h2);
-                if (r.nA == 0 && r.nC == 0 && h1 < 0)
+                if (!ok)
                     break;
-                for (int k = 0; k < max(r.nA, r.nC) && ok; ++k) {
-                    if (k < r.nA) {  // phase A: segment aggregate into TM_DSEG
-                        const int ks = kvi % NKV;
-                        if ((k == 0 && nsegA >= 1 &&
-                             !bwait(&m->dseg_free, (nsegA - 1) & 1, abort)) ||
-                            !bwait(&m->aphi[ai % NKV], (ai / NKV) & 1, abort)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        state_mma(tm + TM_DSEG, ks, k > 0);
-                        mma_commit(&m->kv_empty[ks]);
-                        issued = true;
-                        ++kvi, ++ai;
-                        if (k == r.nA - 1) {
-                            mma_commit(&m->dseg_done);
-                            ++nsegA;
-                        }
-                    }
-                    if (k < r.nC) {  // phase C: one chunk of outputs
-                        const int b = ci & 1, qs = ci % NQ, ks = kvi % NKV;
-                        if (!bwait(&m->q_phi[qs], (ci / NQ) & 1, abort) ||
-                            !bwait(&m->kv_full[ks], (kvi / NKV) & 1, abort) ||
-                            !bwait(&m->srun_read[b], (ci >> 1) & 1, abort)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ss(tm + TM_P, dq(qs) + 2 * kk, dk(ks) + 2 * kk, id_sc, kk > 0);
-                        state_mma(tm + TM_SRUN, ks, true);
-                        mma_commit(&m->mma1_done[b]);
-                        TC_TRACE(ci, 7);
-                        issued = true;
-                        if (!bwait(&m->p_ready[b], (ci >> 1) & 1, abort) ||
-                            (ci >= 2 && !bwait(&m->o_free[b], ((ci >> 1) & 1) ^ 1, abort))) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        TC_TRACE(ci, 14);
-                        const uint32_t o = tm + TM_O + 64 * b;
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            mma_bf16_ts(o, tm + TM_PHL + 8 * kk, dvb(ks) + 128 * kk, id_pv, kk > 0);
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            mma_bf16_ts(o, tm + TM_PHL + 64 + 8 * kk, dvb(ks) + 128 * kk, id_pv, 1);
-                        mma_commit(&m->pv_done[b]);
-                        mma_commit(&m->kv_empty[ks]);
-                        TC_TRACE(ci, 8);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ss(o, dq(qs) + 2 * kk, ds(b) + 2 * kk, id_in, 1);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ss(o, dq(qs) + 2 * kk, ds(b) + 512 + 2 * kk, id_in, 1);
-                        mma_commit(&m->o_done[b]);
-                        TC_TRACE(ci, 9);
-                        ++ci, ++kvi;
-                    }
-                }
-                h2 = h1;
-                h1 = tA;
             }
-            if (issued && *abort) {  // every MMA issued here retires before tensor memory is freed
-                mma_commit(&m->drain);
-                drain_wait(&m->drain, 0);
-            }
+            if (*abort)  // let every load this thread issued land before exit
+                for (int i = 0; i < NA; ++i)
+                    if (a_last[i] >= 0)
+                        drain_wait(&m->a_full[i], a_last[i] & 1);
         }
     } else if (warp == 2 || warp == 3) {
-        // ------------------------------------ look-back, S_in (warps 2-3) --
-        const int tl = tid - 64;  // 0..63
-        const bool lead = tl == 0;
-        const unsigned full = 0xffffffffu;
-        for (int j = 0;; ++j) {
-            const int ss = j % NS;
-            if (!group_ok(!lead || bwait(&m->seg_full[ss], (j / NS) & 1, abort), 4, 64))
-                break;
-            const int t = m->seg_ticket[ss];
-            if (t >= p.total)
-                break;
+        // ----------------------------- producers: phase-C loads (warps 2, 3) --
+        // Chunk ci of phase C goes to output warpgroup ci & 1, whose loads
+        // warp 2 + (ci & 1) issues: phi(K) as soon as that group's previous
+        // scores are done, Q and V once its previous output tile has left the
+        // staging area (the Q and V slots).
+        if (lane == 0) {
+            const int wg = warp - 2;
+            const uint64_t stream = policy_evict_first();
+            unsigned char* cw = sm + OFF_CW + wg * kCWBytes;
+            int c_last = -1, ci = 0, u = 0;
+            bool ok = true;
+            RoundWalker w;
+            Round r;
+            for (int j = 0; ok && w.next(p, m, r, j, true, -1, 1, abort); ++j) {
+                if (!r.nC)
+                    continue;
+                const int jc = j - kLag;
+                const int ci0 = ci + ((ci & 1) != wg ? 1 : 0);
+                const int mine = ci0 < ci + r.nC ? (ci + r.nC - ci0 + 1) / 2 : 0;
+                if (mine && !bwait(&m->phik_stored[jc % NPH], (jc / NPH) & 1, abort))
+                    break;
+                for (int e = 0; e < mine; ++e, ++u) {
+                    const int c = ci0 + 2 * e, k = c - ci;
+                    if (u >= 1 && !bwait(&m->k_free[wg], (u - 1) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&m->c_full[wg], 3 * kC * kD * 2);
+                    tma_load_3d(cw + CW_K, &p.mphi, 0, 0, phi_index(jc, k), &m->c_full[wg], stream);
+                    if (u >= 1 && !bwait(&m->qv_free[wg], (u - 1) & 1, abort)) {
+                        ok = false;  // this phase cannot complete: not drained below
+                        break;
+                    }
+                    const int row = (r.gC.c0 + k) * kC;
+                    tma_load_3d(cw + CW_Q, &p.mq, 0, row, r.gC.s, &m->c_full[wg], stream);
+                    tma_load_3d(cw + CW_V, &p.mv, 0, row, r.gC.s, &m->c_full[wg], stream);
+                    c_last = u;
+                    TC_TRACE(c, 0);
+                }
+                ci += r.nC;
+            }
+            if (*abort && c_last >= 0)  // let every complete load set land before exit
+                drain_wait(&m->c_full[wg], c_last & 1);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // -------------------------- phase A (warpgroup of warps 4-7) --------
+        // phi(K) in place and to the scratch ring; the segment's running
+        // [dS^T; dz] on the tensor cores (warp 4 issues), read out after every
+        // chunk as a prefix snapshot, the last as the segment aggregate.  After
+        // each segment's aggregate, the look-back of the segment before it.
+        const int tb = tid - 128, wb = warp - 4;
+        const bool lead = tb == 0;
+        const uint32_t issue = wb == 0 ? elect_one() : 0u;
+        const uint32_t a0 = smem_addr(sm + OFF_A);
+        int ai = 0, prev_t = -1;
+        bool ok = true, issued = false;
+        // [dS^T; dz] so far (tensor-memory lanes 0..64) copied to dst
+        auto readout = [&](int x, float* dst) -> bool {
+            if (!group_ok(!lead || bwait(&m->dseg_done, x & 1, abort), 1, 128))
+                return false;
+            tc_fence_after();
+            if (wb < 3) {
+                uint32_t rr[4][16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    tmem_ld16(tm + TM_DSEG + lane_off + 16 * q, rr[q]);
+                tmem_ld_wait();
+                if (tb <= kD) {
+                    float4* d4 = reinterpret_cast<float4*>(dst + tb * kD);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            __stcg(d4 + 4 * q + u, make_float4(__uint_as_float(rr[q][4 * u]),
+                                                               __uint_as_float(rr[q][4 * u + 1]),
+                                                               __uint_as_float(rr[q][4 * u + 2]),
+                                                               __uint_as_float(rr[q][4 * u + 3])));
+                }
+            }
+            tc_fence_before();
+            named_bar(1, 128);
+            return true;
+        };
+        // Decoupled look-back of local segment jl (ticket t): S_in, the state
+        // before it, from the nearest inclusive prefix plus the later
+        // aggregates in segment order; then its own inclusive prefix.
+        auto lookback = [&](int jl, int t) -> bool {
+            if (!group_ok(!lead || jl < NSIN ||
+                              bwait(&m->sin_free[jl % NSIN], ((jl / NSIN) & 1) ^ 1, abort),
+                          1, 128))
+                return false;
             const Seg g = seg_of(p, t);
             const int gi = t / p.BH;
-            if (!group_ok(!lead || j < 2 || bwait(&m->sin_free[j & 1], ((j >> 1) & 1) ^ 1, abort),
-                          4, 64))
-                break;
             const unsigned* flag_base = p.flags + static_cast<size_t>(g.s) * p.R;
             float* slot_base = p.slots + static_cast<size_t>(g.s) * p.R * kSlotFloats;
-            if (warp == 2) {
-                // Lane l watches segment base - l.  With a wrapping ring only R-1
-                // slots behind this segment are distinct from its own; a slot
-                // holding another epoch reads as not ready.
+            if (lead)
+                TC_TRACE(jl, 5);
+            if (wb == 0) {
+                // Lane l watches segment base - l.  With a wrapping ring only
+                // R-1 slots behind this segment are distinct from its own; a
+                // slot holding another epoch reads as not ready.
                 const int W = p.R >= p.nseg ? 32 : min(32, p.R - 1);
                 const unsigned active = W >= 32 ? 0xffffffffu : ((1u << W) - 1u);
                 int n = 0, base = gi - 1;
@@ -684,465 +707,396 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     }
                 }
             }
-            named_bar(4, 64);
-            const int nlist = m->nlist;
-            if (nlist < 0)
-                break;
-            // S_in: the nearest inclusive prefix plus the later aggregates in
-            // segment order; thread tl owns float4 words tl + 64 u, u = 0..16.
-            float4 acc[17];
+            named_bar(1, 128);
+            const int n = m->nlist;
+            if (n < 0)
+                return false;
+            if (lead)
+                TC_TRACE(jl, 11);
+            // thread tb owns float4 words tb + 128 v of the state
+            constexpr int NV = (kStateFloats / 4 + 127) / 128;  // 9
+            float4 acc[NV];
 #pragma unroll
-            for (int u = 0; u < 17; ++u)
-                acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int e = nlist - 1; e >= 0; --e) {
+            for (int v = 0; v < NV; ++v)
+                acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int e = n - 1; e >= 0; --e) {
                 const int ent = m->list[e];
                 const float4* src = reinterpret_cast<const float4*>(
                     slot_base + static_cast<size_t>(ent >> 1) * kSlotFloats +
                     ((ent & 1) ? kStateFloats : 0));
 #pragma unroll
-                for (int u = 0; u < 17; ++u) {
-                    const int f = tl + 64 * u;
+                for (int v = 0; v < NV; ++v) {
+                    const int f = tb + 128 * v;
                     if (f < kStateFloats / 4) {
                         const float4 x = __ldcg(src + f);
-                        acc[u].x += x.x, acc[u].y += x.y, acc[u].z += x.z, acc[u].w += x.w;
+                        acc[v].x += x.x, acc[v].y += x.y, acc[v].z += x.z, acc[v].w += x.w;
                     }
                 }
             }
             float4* sin = reinterpret_cast<float4*>(
-                p.sin_scratch + (static_cast<size_t>(blockIdx.x) * 2 + (j & 1)) * kStateFloats);
-#pragma unroll
-            for (int u = 0; u < 17; ++u) {
-                const int f = tl + 64 * u;
-                if (f < kStateFloats / 4)
-                    __stcg(sin + f, acc[u]);
-            }
-            // the inclusive prefix needs this segment's own aggregate
-            if (!group_ok(!lead || bwait(&m->agg_pub[j & 1], (j >> 1) & 1, abort), 4, 64))
-                break;
+                p.sin_scratch + (static_cast<size_t>(blockIdx.x) * NSIN + jl % NSIN) * kStateFloats);
             const int my = gi % p.R;
             const float4* agg =
                 reinterpret_cast<const float4*>(slot_base + static_cast<size_t>(my) * kSlotFloats);
             float4* inc = reinterpret_cast<float4*>(slot_base + static_cast<size_t>(my) * kSlotFloats +
                                                     kStateFloats);
 #pragma unroll
-            for (int u = 0; u < 17; ++u) {
-                const int f = tl + 64 * u;
+            for (int v = 0; v < NV; ++v) {
+                const int f = tb + 128 * v;
                 if (f < kStateFloats / 4) {
                     const float4 a = __ldcg(agg + f);
-                    __stcg(inc + f, make_float4(acc[u].x + a.x, acc[u].y + a.y, acc[u].z + a.z,
-                                                acc[u].w + a.w));
+                    __stcg(sin + f, acc[v]);
+                    __stcg(inc + f, make_float4(acc[v].x + a.x, acc[v].y + a.y, acc[v].z + a.z,
+                                                acc[v].w + a.w));
                 }
             }
-            named_bar(4, 64);
+            __threadfence();
+            named_bar(1, 128);
             if (lead) {
-                __threadfence();
                 st_release(const_cast<unsigned*>(flag_base) + my,
                            (static_cast<unsigned>(gi + 1) << 2) | 2u);
-                mbar_arrive(&m->sin_ready[j & 1]);
+                mbar_arrive(&m->sin_ready[jl % NSIN]);
+                TC_TRACE(jl, 12);
             }
-        }
-    } else if (warp >= 4 && warp < 8) {
-        // ---------------------------------- P, epilogue (warps 4-7) --------
-        const int ta = tid - 128;
-        const bool lead = ta == 0;
-        const uint64_t pol = policy_evict_first();
-        unsigned char* sO = sm + OFF_O;
-        int ci = 0, h1 = -1, h2 = -1;
-        bool doneA = false;
-        // the epilogue of a chunk runs after P of the next one; its row sum of P
-        // (the intra-chunk denominator) waits in a register
-        int pend_ci = -1, pend_c = 0, pend_s = 0, pend_last = 0, pend_ss = 0;
-        float pend_rs = 0.f;
-        auto epilogue = [&]() -> bool {
-            const int cj = pend_ci, b = cj & 1, qs = cj % NQ;
-            if (!group_ok(!lead || (bwait(&m->q_phi[qs], (cj / NQ) & 1, abort) &&
-                                    bwait(&m->srun_read[b], (cj >> 1) & 1, abort) &&
-                                    bwait(&m->o_done[b], (cj >> 1) & 1, abort)),
-                          1, 128))
-                return false;
-            tc_fence_after();
-            if (lead)
-                TC_TRACE(cj, 5);
-            float den = pend_rs;
-            if (norm) {
-                const unsigned char* sQ = sm + OFF_Q + qs * 16384;
-                const float* z = m->zprev[b];
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(sQ + sw128_off(ta, cc));
-                    const float4 z0 = *reinterpret_cast<const float4*>(z + 8 * cc);
-                    const float4 z1 = *reinterpret_cast<const float4*>(z + 8 * cc + 4);
-                    den = fmaf(bf_lo(x.x), z0.x, den);
-                    den = fmaf(bf_hi(x.x), z0.y, den);
-                    den = fmaf(bf_lo(x.y), z0.z, den);
-                    den = fmaf(bf_hi(x.y), z0.w, den);
-                    den = fmaf(bf_lo(x.z), z1.x, den);
-                    den = fmaf(bf_hi(x.z), z1.y, den);
-                    den = fmaf(bf_lo(x.w), z1.z, den);
-                    den = fmaf(bf_hi(x.w), z1.w, den);
-                }
-            }
-            const float inv = norm ? 1.0f / fmaxf(den, FLT_MIN) : 1.0f;
-            if (lead)
-                bulk_wait_read<0>();  // the previous tile has left the staging buffer
-            named_bar(1, 128);
-            uint32_t rr[4][16];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                tmem_ld16(tm + TM_O + 64 * b + lane_off + 16 * q, rr[q]);
-            tmem_ld_wait();
-            if (lead)
-                TC_TRACE(cj, 13);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int col4 = 4 * q + u;
-                    const float4 o = make_float4(__uint_as_float(rr[q][4 * u]) * inv,
-                                                 __uint_as_float(rr[q][4 * u + 1]) * inv,
-                                                 __uint_as_float(rr[q][4 * u + 2]) * inv,
-                                                 __uint_as_float(rr[q][4 * u + 3]) * inv);
-                    *reinterpret_cast<float4*>(sO + (col4 >> 3) * 16384 +
-                                               sw128_off(ta, col4 & 7)) = o;
-                }
-            }
-            tc_fence_before();
-            fence_proxy_async_smem();
-            named_bar(1, 128);
-            if (lead) {
-                mbar_arrive(&m->o_free[b]);
-                mbar_arrive(&m->q_empty[qs]);
-                mbar_arrive(&m->epi_done[b]);
-                if (pend_last)
-                    mbar_arrive(&m->seg_empty[pend_ss]);
-                tma_store_3d(&p.mo, sO, 0, pend_c * kC, pend_s, pol);
-                tma_store_3d(&p.mo, sO + 16384, 32, pend_c * kC, pend_s, pol);
-                bulk_commit();
-                TC_TRACE(cj, 15);
-            }
-            pend_ci = -1;
             return true;
         };
-        bool ok = true;
-        for (int j = 0; ok; ++j) {
-            int tA = -1;
-            if (!doneA) {
-                if (!group_ok(!lead || bwait(&m->seg_full[j % NS], (j / NS) & 1, abort), 1, 128))
+        RoundWalker w;
+        Round r;
+        for (int j = 0; ok && w.next(p, m, r, j, lead, 1, 128, abort); ++j) {
+            for (int k = 0; k < r.nA; ++k, ++ai) {
+                const int s = ai % NA;
+                if (!group_ok(!lead || bwait(&m->a_full[s], (ai / NA) & 1, abort), 1, 128)) {
+                    ok = false;
                     break;
-                const int t = m->seg_ticket[j % NS];
-                if (t < p.total)
-                    tA = t;
-                else
-                    doneA = true;
+                }
+                unsigned char* ktile = sm + OFF_A + s * 32768 + 16384;
+                if (lead)
+                    TC_TRACE(ai, 9);
+                // phi(K) is kept for phase C in the scratch (plain stores, fenced
+                // before the TMA loads of phase C read it)
+                phi_tile(ktile, tb, chunk_valid(p, r.gA.c0 + k), elu,
+                         reinterpret_cast<uint4*>(p.phi_scratch) +
+                             static_cast<size_t>(phi_index(j, k)) * (kC * kD * 2 / 16));
+                fence_proxy_async_smem();
+                named_bar(1, 128);
+                // the state before chunk k of the segment, for phase C
+                if (k >= 1 && !(ok = readout(ai - 1, snap_ptr(j, k - 1))))
+                    break;
+                if (wb == 0) {
+                    tc_fence_after();
+                    state_mma(tm + TM_DSEG, a0 + s * 32768, a0 + s * 32768 + 16384, ones, k > 0,
+                              issue);
+                    mma_commit_w(&m->dseg_done, issue);
+                    mma_commit_w(&m->a_empty[s], issue);
+                    issued = true;
+                    if (lead)
+                        TC_TRACE(ai, 10);
+                }
+                if (k == r.nA - 1) {  // segment aggregate complete: publish it
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    __threadfence();
+                    named_bar(1, 128);
+                    if (lead) {
+                        mbar_arrive(&m->phik_stored[j % NPH]);
+                        TC_TRACE(j, 15);
+                    }
+                    const int gi = r.tA / p.BH;
+                    float* agg =
+                        p.slots + (static_cast<size_t>(r.gA.s) * p.R + gi % p.R) * kSlotFloats;
+                    if (!(ok = readout(ai, agg)))
+                        break;
+                    if (lead) {
+                        __threadfence();
+                        st_release(p.flags + static_cast<size_t>(r.gA.s) * p.R + gi % p.R,
+                                   (static_cast<unsigned>(gi + 1) << 2) | 1u);
+                    }
+                }
             }
-            Round r;
-            round_setup(p, r, j, tA, h2);
-            if (r.nA == 0 && r.nC == 0 && h1 < 0)
+            // the previous segment's look-back, one segment behind, so its
+            // predecessors have usually published their inclusive prefixes
+            if (ok && prev_t >= 0 && !(ok = lookback(j - 1, prev_t)))
                 break;
-            for (int k = 0; k < r.nC; ++k, ++ci) {
-                const int b = ci & 1;
-                // P: causal mask, row sums, bf16 hi/lo into TM_PHL
-                if (!group_ok(!lead || (bwait(&m->mma1_done[b], (ci >> 1) & 1, abort) &&
-                                        (ci < 1 || bwait(&m->pv_done[(ci - 1) & 1],
-                                                         ((ci - 1) >> 1) & 1, abort))),
-                              1, 128)) {
+            prev_t = r.nA ? r.tA : -1;
+        }
+        if (issued && *abort) {
+            mma_commit_w(&m->drain[0], issue);
+            drain_wait(&m->drain[0], 0);
+        }
+    } else if (warp >= 8) {
+        // ------------------- phase C (warpgroups of warps 8-11 and 12-15) ---
+        // Warpgroup wg takes every other chunk ci (ci & 1 == wg) and runs it
+        // through: S_prev, phi(Q), scores, P, [num | den], epilogue.  Its
+        // first warp issues the MMAs.
+        const int wg = (warp - 8) >> 2;
+        const int tc = tid - 256 - 128 * wg;   // row of the chunk = tensor-memory lane
+        const int wq = tc >> 5;                // 32-row block
+        const bool lead = tc == 0;
+        const int barid = 2 + wg;
+        const uint32_t issue = wq == 0 ? elect_one() : 0u;
+        unsigned char* cw = sm + OFF_CW + wg * kCWBytes;
+        const uint32_t cwa = smem_addr(cw);
+        const uint64_t pol = policy_evict_first();
+        const uint32_t id_sc = idesc_bf16_f32(128, 128, false, false);
+        const uint32_t id_pv = idesc_bf16_f32(128, kON, false, true);
+        const uint32_t id_in = idesc_bf16_f32(128, kON, false, false);
+        const uint32_t tp = tm + TM_P + 128 * wg, to = tm + TM_O + kON * wg;
+        int ci = 0, u = 0;
+        bool ok = true, issued = false;
+        RoundWalker w;
+        Round r;
+        for (int j = 0; ok && w.next(p, m, r, j, lead, barid, 128, abort); ++j) {
+            if (!r.nC)
+                continue;
+            const int jc = j - kLag;
+            // this group's chunks of the segment: ci0, ci0 + 2, ...
+            const int ci0 = ci + ((ci & 1) != wg ? 1 : 0);
+            const int mine = ci0 < ci + r.nC ? (ci + r.nC - ci0 + 1) / 2 : 0;
+            for (int e = 0; e < mine && ok; ++e, ++u) {
+                const int c = ci0 + 2 * e, k = c - ci;
+                // S_prev = S_in + the segment's prefix before chunk k, as
+                // [S_prev^T; z_prev] hi/lo (free: this group's previous chunk
+                // is done with it)
+                if (!group_ok(!lead || e > 0 ||
+                                  (bwait(&m->sin_ready[jc % NSIN], (jc / NSIN) & 1, abort) &&
+                                   bwait(&m->phik_stored[jc % NPH], (jc / NPH) & 1, abort)),
+                              barid, 128)) {
+                    ok = false;
+                    break;
+                }
+                if (lead)
+                    TC_TRACE(c, 13);
+                {
+                    // 65 rows x 8 chunks of 8 floats: item tc + 128 v is row
+                    // (item >> 3), chunk (item & 7); every load issued first
+                    const float* s_in =
+                        p.sin_scratch +
+                        (static_cast<size_t>(blockIdx.x) * NSIN + jc % NSIN) * kStateFloats;
+                    const float* s_pf = snap_ptr(jc, max(k - 1, 0));
+                    unsigned char* sShi = cw + CW_S;
+                    unsigned char* sSlo = sShi + kSBytes;
+                    constexpr int NU = 4;
+                    const int nu = NU + (tc < 8 ? 1 : 0);  // 520 items = 4 x 128 + 8
+                    float4 x[NU + 1][2], y[NU + 1][2];
+#pragma unroll
+                    for (int v = 0; v <= NU; ++v) {
+                        if (v < nu) {
+                            const float4* a4 =
+                                reinterpret_cast<const float4*>(s_in + 8 * (tc + 128 * v));
+                            x[v][0] = __ldcg(a4), x[v][1] = __ldcg(a4 + 1);
+                            if (k >= 1) {
+                                const float4* b4 =
+                                    reinterpret_cast<const float4*>(s_pf + 8 * (tc + 128 * v));
+                                y[v][0] = __ldcg(b4), y[v][1] = __ldcg(b4 + 1);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int v = 0; v <= NU; ++v) {
+                        if (v < nu) {
+                            const int item = tc + 128 * v, row = item >> 3, cc = item & 7;
+                            float4 x0 = x[v][0], x1 = x[v][1];
+                            if (k >= 1) {
+                                x0.x += y[v][0].x, x0.y += y[v][0].y, x0.z += y[v][0].z,
+                                    x0.w += y[v][0].w;
+                                x1.x += y[v][1].x, x1.y += y[v][1].y, x1.z += y[v][1].z,
+                                    x1.w += y[v][1].w;
+                            }
+                            uint4 h, l;
+                            split2(x0.x, x0.y, h.x, l.x);
+                            split2(x0.z, x0.w, h.y, l.y);
+                            split2(x1.x, x1.y, h.z, l.z);
+                            split2(x1.z, x1.w, h.w, l.w);
+                            *reinterpret_cast<uint4*>(sShi + sw128_off(row, cc)) = h;
+                            *reinterpret_cast<uint4*>(sSlo + sw128_off(row, cc)) = l;
+                        }
+                    }
+                }
+                // Q, phi(K), V of chunk c
+                if (!group_ok(!lead || bwait(&m->c_full[wg], u & 1, abort), barid, 128)) {
+                    ok = false;
+                    break;
+                }
+                if (k >= 1) {  // every thread has read the snapshot before chunk k
+                    const unsigned char* sp =
+                        reinterpret_cast<const unsigned char*>(snap_ptr(jc, k - 1));
+                    l2_discard(sp + 128 * tc);
+                    if (tc < (kStateFloats * 4) / 128 - 128)
+                        l2_discard(sp + 128 * (128 + tc));
+                }
+                if (lead)
+                    TC_TRACE(c, 14);
+                phi_tile(cw + CW_Q, tc, chunk_valid(p, r.gC.c0 + k), elu, nullptr);
+                fence_proxy_async_smem();
+                named_bar(barid, 128);
+                if (lead)
+                    TC_TRACE(c, 1);
+                // scores into this group's score buffer
+                if (wq == 0) {
+                    tc_fence_after();
+                    const uint64_t dq = sdesc_sw128(cwa + CW_Q, 16, 1024);
+                    const uint64_t dk = sdesc_sw128(cwa + CW_K, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ss_w(tp, dq + 2 * kk, dk + 2 * kk, id_sc, kk > 0, issue);
+                    mma_commit_w(&m->s_done[wg], issue);
+                    // phi(Q) [S_prev^T; z_prev] (hi, lo) starts the output
+                    // accumulator while P is prepared
+                    const uint64_t ds = sdesc_sw128(cwa + CW_S, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ss_w(to, dq + 2 * kk, ds + 2 * kk, id_in, kk > 0, issue);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ss_w(to, dq + 2 * kk, ds + (kSBytes >> 4) + 2 * kk, id_in, 1,
+                                      issue);
+                    issued = true;
+                    if (lead)
+                        TC_TRACE(c, 2);
+                }
+                if (!group_ok(!lead || bwait(&m->s_done[wg], u & 1, abort), barid, 128)) {
+                    ok = false;
+                    break;
+                }
+                if (lead) {
+                    mbar_arrive(&m->k_free[wg]);  // phi(K) slot free for the next chunk
+                    TC_TRACE(c, 3);
+                }
+                // the scores were the last reader of the chunk's phi(K) tile
+                l2_discard(static_cast<unsigned char*>(p.phi_scratch) +
+                           static_cast<size_t>(phi_index(jc, k)) * (kC * kD * 2) + 128 * tc);
+                tc_fence_after();
+                // P = tril(scores) as bf16 hi/lo, in place: keys 32q..32q+31 of
+                // row tc move to columns 32q..32q+15 (hi) and 32q+16..32q+31 (lo).
+                // Blocks left of the diagonal are kept whole, the diagonal block
+                // is masked, blocks right of it become zero.
+                {
+                    const uint32_t pb = tp + lane_off;
+#pragma unroll 1
+                    for (int q = 0; q <= wq; ++q) {
+                        uint32_t v0[16], v1[16], hi[16], lo[16];
+                        tmem_ld16(pb + 32 * q, v0);
+                        tmem_ld16(pb + 32 * q + 16, v1);
+                        tmem_ld_wait();
+                        if (q < wq) {
+#pragma unroll
+                            for (int mm = 0; mm < 8; ++mm) {
+                                split2(__uint_as_float(v0[2 * mm]), __uint_as_float(v0[2 * mm + 1]),
+                                       hi[mm], lo[mm]);
+                                split2(__uint_as_float(v1[2 * mm]), __uint_as_float(v1[2 * mm + 1]),
+                                       hi[8 + mm], lo[8 + mm]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int mm = 0; mm < 8; ++mm) {
+                                split2(2 * mm <= lane ? __uint_as_float(v0[2 * mm]) : 0.f,
+                                       2 * mm + 1 <= lane ? __uint_as_float(v0[2 * mm + 1]) : 0.f,
+                                       hi[mm], lo[mm]);
+                                split2(16 + 2 * mm <= lane ? __uint_as_float(v1[2 * mm]) : 0.f,
+                                       17 + 2 * mm <= lane ? __uint_as_float(v1[2 * mm + 1]) : 0.f,
+                                       hi[8 + mm], lo[8 + mm]);
+                            }
+                        }
+                        tmem_st16(pb + 32 * q, hi);
+                        tmem_st16(pb + 32 * q + 16, lo);
+                    }
+                    uint32_t zz[16];
+#pragma unroll
+                    for (int mm = 0; mm < 16; ++mm)
+                        zz[mm] = 0u;
+#pragma unroll 1
+                    for (int q = wq + 1; q < 4; ++q) {
+                        tmem_st16(pb + 32 * q, zz);
+                        tmem_st16(pb + 32 * q + 16, zz);
+                    }
+                    tmem_st_wait();
+                }
+                tc_fence_before();
+                named_bar(barid, 128);
+                if (lead)
+                    TC_TRACE(c, 4);
+                // [num | den] += P [V | e] (P hi/lo pairs)
+                if (wq == 0) {
+                    tc_fence_after();
+                    const uint32_t vs = cwa + CW_V;
+                    const uint64_t bv = sdesc_sw128(vs, ones - vs, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t step = static_cast<uint64_t>(kk * 128);
+                        mma_bf16_ts_w(to, tp + 32 * (kk >> 1) + 8 * (kk & 1),
+                                      bv + step - (step << 16), id_pv, 1, issue);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t step = static_cast<uint64_t>(kk * 128);
+                        mma_bf16_ts_w(to, tp + 32 * (kk >> 1) + 16 + 8 * (kk & 1),
+                                      bv + step - (step << 16), id_pv, 1, issue);
+                    }
+                    mma_commit_w(&m->o_done[wg], issue);
+                    if (lead)
+                        TC_TRACE(c, 6);
+                }
+                if (!group_ok(!lead || bwait(&m->o_done[wg], u & 1, abort), barid, 128)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 if (lead)
-                    TC_TRACE(ci, 3);
-                float rs = 0.f;
-                // rows 0..63 see only keys 0..63: the upper 64 columns are masked
-                const int nq = ta < 64 ? 2 : 4;
-#pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t hi[16], lo[16];
-                    if (q < nq) {
-                        uint32_t v0[16], v1[16];
-                        tmem_ld16(tm + TM_P + lane_off + 32 * q, v0);
-                        tmem_ld16(tm + TM_P + lane_off + 32 * q + 16, v1);
-                        tmem_ld_wait();
-                        const int lim = ta - 32 * q;  // keys jj <= ta stay
+                    TC_TRACE(c, 7);
+                // epilogue: o = num / den into the staging area (the Q and V
+                // slots, free now), then two TMA stores of 32 columns
+                {
+                    const uint32_t o = to + lane_off;
+                    uint32_t rr[4][16];
 #pragma unroll
-                        for (int mm = 0; mm < 8; ++mm) {
-                            const float a = 2 * mm <= lim ? __uint_as_float(v0[2 * mm]) : 0.f;
-                            const float bb =
-                                2 * mm + 1 <= lim ? __uint_as_float(v0[2 * mm + 1]) : 0.f;
-                            rs += a + bb;
-                            split2(a, bb, hi[mm], lo[mm]);
+                    for (int q = 0; q < 4; ++q)
+                        tmem_ld16(o + 16 * q, rr[q]);
+                    const uint32_t dn = tmem_ld1(o + kD);
+                    tmem_ld_wait();
+                    const float inv = norm ? 1.0f / fmaxf(__uint_as_float(dn), FLT_MIN) : 1.0f;
+                    unsigned char* sO = cw + CW_Q;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int col4 = 4 * q + v;
+                            const float2 a = mul2(make_float2(__uint_as_float(rr[q][4 * v]),
+                                                              __uint_as_float(rr[q][4 * v + 1])),
+                                                  make_float2(inv, inv));
+                            const float2 bq = mul2(make_float2(__uint_as_float(rr[q][4 * v + 2]),
+                                                               __uint_as_float(rr[q][4 * v + 3])),
+                                                   make_float2(inv, inv));
+                            *reinterpret_cast<float4*>(sO + (col4 >> 3) * 16384 +
+                                                       sw128_off(tc, col4 & 7)) =
+                                make_float4(a.x, a.y, bq.x, bq.y);
                         }
-#pragma unroll
-                        for (int mm = 0; mm < 8; ++mm) {
-                            const float a =
-                                16 + 2 * mm <= lim ? __uint_as_float(v1[2 * mm]) : 0.f;
-                            const float bb =
-                                17 + 2 * mm <= lim ? __uint_as_float(v1[2 * mm + 1]) : 0.f;
-                            rs += a + bb;
-                            split2(a, bb, hi[8 + mm], lo[8 + mm]);
-                        }
-                    } else {
-#pragma unroll
-                        for (int mm = 0; mm < 16; ++mm)
-                            hi[mm] = lo[mm] = 0u;
                     }
-                    tmem_st16(tm + TM_PHL + lane_off + 16 * q, hi);
-                    tmem_st16(tm + TM_PHL + lane_off + 64 + 16 * q, lo);
                 }
-                tmem_st_wait();
-                if (lead)
-                    TC_TRACE(ci, 10);
                 tc_fence_before();
-                named_bar(1, 128);
+                fence_proxy_async_smem();
+                named_bar(barid, 128);
                 if (lead) {
-                    mbar_arrive(&m->p_ready[b]);
-                    TC_TRACE(ci, 6);
+                    const int row = (r.gC.c0 + k) * kC;
+                    tma_store_3d(&p.mo, cw + CW_Q, 0, row, r.gC.s, pol);
+                    tma_store_3d(&p.mo, cw + CW_V, 32, row, r.gC.s, pol);
+                    bulk_commit();
+                    TC_TRACE(c, 8);
+                    // the tile has left the Q and V slots: let the next loads in
+                    bulk_wait_read<0>();
+                    mbar_arrive(&m->qv_free[wg]);
                 }
-                if (pend_ci >= 0 && !epilogue()) {
-                    ok = false;
-                    break;
-                }
-                pend_ci = ci, pend_c = r.gC.c0 + k, pend_s = r.gC.s, pend_rs = rs;
-                pend_last = k == r.nC - 1, pend_ss = (j - 2) % NS;
             }
-            h2 = h1;
-            h1 = tA;
+            // this group is done with the segment's S_in and ticket slot
+            if (ok && lead) {
+                mbar_arrive(&m->sin_free[jc % NSIN]);
+                mbar_arrive(&m->seg_empty[jc % NS]);
+            }
+            ci += r.nC;
         }
-        if (ok && pend_ci >= 0)
-            epilogue();
         if (lead)
             bulk_wait<0>();
-    } else if (warp >= 8 && warp < 12) {
-        // ------------- phi(K), segment aggregate, S_prev (warps 8-11) ------
-        const int tb = tid - 256, wb = warp - 8;
-        const bool lead = tb == 0;
-        int kvi = 0, ci = 0, ai = 0, nsegA = 0, h1 = -1, h2 = -1;
-        bool ok = true, doneA = false;
-        for (int j = 0; ok; ++j) {
-            int tA = -1;
-            if (!doneA) {
-                if (!group_ok(!lead || bwait(&m->seg_full[j % NS], (j / NS) & 1, abort), 2, 128))
-                    break;
-                const int t = m->seg_ticket[j % NS];
-                if (t < p.total)
-                    tA = t;
-                else
-                    doneA = true;
-            }
-            Round r;
-            round_setup(p, r, j, tA, h2);
-            if (r.nA == 0 && r.nC == 0 && h1 < 0)
-                break;
-            const int jc = j - 2;
-            for (int k = 0; k < max(r.nA, r.nC) && ok; ++k) {
-                if (k < r.nA) {  // phase A: phi(K) kept for phase C, column sums
-                    const int ks = kvi % NKV;
-                    if (!group_ok(!lead || bwait(&m->kv_full[ks], (kvi / NKV) & 1, abort), 2,
-                                  128)) {
-                        ok = false;
-                        break;
-                    }
-                    unsigned char* ktile = sm + OFF_KV + ks * 32768 + 16384;
-                    if (lead)
-                        TC_TRACE(ai, 2);
-                    // phi(K) is kept for phase C in the scratch (plain stores,
-                    // fenced before the TMA loads of phase C read it)
-                    phi_tile(ktile, tb, chunk_valid(p, r.gA.c0 + k), elu, m->dza,
-                             reinterpret_cast<uint4*>(p.phi_scratch) +
-                                 static_cast<size_t>(phi_index(j, k)) * (kC * kD * 2 / 16));
-                    fence_proxy_async_smem();
-                    named_bar(2, 128);
-                    if (tb < kD) {
-                        const float dz =
-                            m->dza[0][tb] + m->dza[1][tb] + m->dza[2][tb] + m->dza[3][tb];
-                        m->dzacc[tb] += dz;
-                        m->dzk[j % NPH][k][tb] = dz;
-                    }
-                    if (lead) {
-                        mbar_arrive(&m->aphi[ai % NKV]);
-                        TC_TRACE(ai, 11);
-                    }
-                    named_bar(2, 128);
-                    ++kvi, ++ai;
-                    if (k == r.nA - 1) {  // segment aggregate complete: publish it
-                        asm volatile("fence.proxy.async.global;" ::: "memory");
-                        __threadfence();
-                        named_bar(2, 128);
-                        if (lead)
-                            mbar_arrive(&m->phik_stored[j % NPH]);
-                        const int gi = r.tA / p.BH;
-                        // agg_pub[j & 1] is re-armed only after the look-back warps
-                        // consumed it for segment j-2 (their sin_ready follows that)
-                        if (!group_ok(!lead || (bwait(&m->dseg_done, nsegA & 1, abort) &&
-                                                (j < 2 || bwait(&m->sin_ready[(j - 2) & 1],
-                                                                ((j - 2) >> 1) & 1, abort))),
-                                      2, 128)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        float* agg =
-                            p.slots + (static_cast<size_t>(r.gA.s) * p.R + gi % p.R) * kSlotFloats;
-                        if (wb < 2) {  // dS^T rows = tensor-memory lanes 0..63
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                uint32_t rr[16];
-                                tmem_ld16(tm + TM_DSEG + lane_off + 16 * q, rr);
-                                tmem_ld_wait();
-                                float4* d4 = reinterpret_cast<float4*>(agg + tb * kD + 16 * q);
-#pragma unroll
-                                for (int u = 0; u < 4; ++u)
-                                    __stcg(d4 + u, make_float4(__uint_as_float(rr[4 * u]),
-                                                               __uint_as_float(rr[4 * u + 1]),
-                                                               __uint_as_float(rr[4 * u + 2]),
-                                                               __uint_as_float(rr[4 * u + 3])));
-                            }
-                        } else {
-                            __stcg(agg + kD * kD + (tb - 64), m->dzacc[tb - 64]);
-                            m->dzacc[tb - 64] = 0.f;
-                        }
-                        tc_fence_before();
-                        named_bar(2, 128);
-                        if (lead) {
-                            mbar_arrive(&m->dseg_free);
-                            __threadfence();
-                            st_release(p.flags + static_cast<size_t>(r.gA.s) * p.R + gi % p.R,
-                                       (static_cast<unsigned>(gi + 1) << 2) | 1u);
-                            mbar_arrive(&m->agg_pub[j & 1]);
-                        }
-                        ++nsegA;
-                    }
-                }
-                if (k < r.nC) {  // phase C: S_prev, z_prev of chunk ci
-                    const int b = ci & 1;
-                    if (!group_ok(!lead || ci < 2 ||
-                                      (bwait(&m->o_done[b], ((ci >> 1) & 1) ^ 1, abort) &&
-                                       bwait(&m->epi_done[b], ((ci >> 1) & 1) ^ 1, abort)),
-                                  2, 128) ||
-                        !group_ok(!lead || ci < 1 ||
-                                      bwait(&m->mma1_done[(ci - 1) & 1], ((ci - 1) >> 1) & 1,
-                                            abort),
-                                  2, 128) ||
-                        !group_ok(!lead || k > 0 ||
-                                      bwait(&m->sin_ready[jc & 1], (jc >> 1) & 1, abort),
-                                  2, 128)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    unsigned char* sShi = sm + OFF_S + b * 16384;
-                    unsigned char* sSlo = sShi + 8192;
-                    if (wb < 2) {  // S_prev^T row tb: tensor-memory lane tb
-                        float sp[kD];
-                        if (k == 0) {  // segment start: S_in from the look-back
-                            const float4* src = reinterpret_cast<const float4*>(
-                                p.sin_scratch +
-                                (static_cast<size_t>(blockIdx.x) * 2 + (jc & 1)) * kStateFloats +
-                                tb * kD);
-#pragma unroll
-                            for (int u = 0; u < 16; ++u) {
-                                const float4 x = __ldcg(src + u);
-                                sp[4 * u] = x.x, sp[4 * u + 1] = x.y, sp[4 * u + 2] = x.z,
-                                       sp[4 * u + 3] = x.w;
-                            }
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                uint32_t rr[16];
-#pragma unroll
-                                for (int u = 0; u < 16; ++u)
-                                    rr[u] = __float_as_uint(sp[16 * q + u]);
-                                tmem_st16(tm + TM_SRUN + lane_off + 16 * q, rr);
-                            }
-                            tmem_st_wait();
-                        } else {
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                uint32_t rr[16];
-                                tmem_ld16(tm + TM_SRUN + lane_off + 16 * q, rr);
-                                tmem_ld_wait();
-#pragma unroll
-                                for (int u = 0; u < 16; ++u)
-                                    sp[16 * q + u] = __uint_as_float(rr[u]);
-                            }
-                        }
-#pragma unroll
-                        for (int cc = 0; cc < 8; ++cc) {
-                            uint4 h, l;
-                            split2(sp[8 * cc + 0], sp[8 * cc + 1], h.x, l.x);
-                            split2(sp[8 * cc + 2], sp[8 * cc + 3], h.y, l.y);
-                            split2(sp[8 * cc + 4], sp[8 * cc + 5], h.z, l.z);
-                            split2(sp[8 * cc + 6], sp[8 * cc + 7], h.w, l.w);
-                            *reinterpret_cast<uint4*>(sShi + sw128_off(tb, cc)) = h;
-                            *reinterpret_cast<uint4*>(sSlo + sw128_off(tb, cc)) = l;
-                        }
-                    } else {  // z_prev
-                        const int i = tb - 64;
-                        float z;
-                        if (k == 0)
-                            z = __ldcg(p.sin_scratch +
-                                       (static_cast<size_t>(blockIdx.x) * 2 + (jc & 1)) *
-                                           kStateFloats +
-                                       kD * kD + i);
-                        else
-                            z = m->zrun[i] + m->dzk[jc % NPH][k - 1][i];
-                        m->zrun[i] = z;
-                        m->zprev[b][i] = z;
-                    }
-                    fence_proxy_async_smem();
-                    tc_fence_before();
-                    named_bar(2, 128);
-                    if (lead) {
-                        if (k == 0)
-                            mbar_arrive(&m->sin_free[jc & 1]);
-                        mbar_arrive(&m->srun_read[b]);
-                        TC_TRACE(ci, 4);
-                    }
-                    ++ci, ++kvi;
-                }
-            }
-            h2 = h1;
-            h1 = tA;
-        }
-    } else if (warp >= 12) {
-        // ----------------------------------------- phi(Q) (warps 12-15) ----
-        const int tcx = tid - 384;
-        const bool lead = tcx == 0;
-        int ci = 0, h1 = -1, h2 = -1;
-        bool ok = true, doneA = false;
-        for (int j = 0; ok; ++j) {
-            int tA = -1;
-            if (!doneA) {
-                if (!group_ok(!lead || bwait(&m->seg_full[j % NS], (j / NS) & 1, abort), 3, 128))
-                    break;
-                const int t = m->seg_ticket[j % NS];
-                if (t < p.total)
-                    tA = t;
-                else
-                    doneA = true;
-            }
-            Round r;
-            round_setup(p, r, j, tA, h2);
-            if (r.nA == 0 && r.nC == 0 && h1 < 0)
-                break;
-            for (int k = 0; k < r.nC; ++k, ++ci) {
-                const int qs = ci % NQ;
-                if (!group_ok(!lead || bwait(&m->q_full[qs], (ci / NQ) & 1, abort), 3, 128)) {
-                    ok = false;
-                    break;
-                }
-                if (lead)
-                    TC_TRACE(ci, 12);
-                phi_tile(sm + OFF_Q + qs * 16384, tcx, chunk_valid(p, r.gC.c0 + k), elu, nullptr,
-                         nullptr);
-                fence_proxy_async_smem();
-                named_bar(3, 128);
-                if (lead) {
-                    mbar_arrive(&m->q_phi[qs]);
-                    TC_TRACE(ci, 1);
-                }
-            }
-            h2 = h1;
-            h1 = tA;
+        if (issued && *abort) {
+            mma_commit_w(&m->drain[1 + wg], issue);
+            drain_wait(&m->drain[1 + wg], 0);
         }
     }
 
@@ -1196,7 +1150,7 @@ struct TcGeom {
     int nseg;
     int R;       // ring slots per sequence
     int total;   // segment tickets
-    size_t flags_off, slots_off, sin_off, phi_off, bytes;
+    size_t flags_off, slots_off, sin_off, phi_off, snap_off, bytes;
 };
 
 int sm_count()
@@ -1232,8 +1186,9 @@ TcGeom tc_geom(int64_t BH, int64_t N, int sms)
     g.flags_off = 256;
     g.slots_off = (g.flags_off + sizeof(unsigned) * (size_t)BH * g.R + 255) & ~(size_t)255;
     g.sin_off = g.slots_off + sizeof(float) * (size_t)BH * g.R * kSlotFloats;
-    g.phi_off = (g.sin_off + sizeof(float) * (size_t)G * 2 * kStateFloats + 1023) & ~(size_t)1023;
-    g.bytes = g.phi_off + (size_t)G * NPH * g.L * kC * kD * 2;
+    g.phi_off = (g.sin_off + sizeof(float) * (size_t)G * NSIN * kStateFloats + 1023) & ~(size_t)1023;
+    g.snap_off = g.phi_off + (size_t)G * NPH * g.L * kC * kD * 2;
+    g.bytes = g.snap_off + sizeof(float) * (size_t)G * NPH * (g.L - 1) * kStateFloats;
     return g;
 }
 
@@ -1280,6 +1235,8 @@ cudaError_t tc_forward(const FwdArgs& a)
     p.slots = reinterpret_cast<float*>(ws + g.slots_off);
     p.sin_scratch = reinterpret_cast<float*>(ws + g.sin_off);
     p.phi_scratch = ws + g.phi_off;
+    p.snap = reinterpret_cast<float*>(ws + g.snap_off);
+    p.out = static_cast<float*>(a.out);
     p.status = a.status;
     cudaError_t e = cudaMemsetAsync(ws, 0, g.slots_off, a.stream);
     if (e != cudaSuccess)
