@@ -50,9 +50,8 @@
 //               0 and 1
 //   warps 4-7   phase A: phi(K) in place and to the scratch ring; the
 //               segment's running [dS^T; dz] on the tensor cores and its
-//               snapshots; the aggregate; then, one segment behind, the
-//               look-back that yields S_in and the inclusive prefix (the
-//               predecessors' prefixes are mostly published by then)
+//               snapshots; the aggregate; then the look-back that yields
+//               S_in and the inclusive prefix
 //   warps 8-11, 12-15
 //               output warpgroups 0 and 1, taking alternate chunks: S_prev
 //               from S_in and the snapshot, phi(Q), scores, P (causal mask,
@@ -381,7 +380,7 @@ __device__ __forceinline__ int chunk_valid(const TcParams& p, int c)
 // Job order shared by every role.  Round j holds phase A of local segment j
 // and phase C of local segment j-kLag, interleaved chunk by chunk
 // (A0 C0 A1 C1 ...); the rounds between a segment's phases hide its look-back.
-constexpr int kLag = 2;
+constexpr int kLag = 1;
 struct Round {
     int j;        // round = local index of the A segment
     int tA, tC;   // tickets of the A and C segments (-1: none)
@@ -810,11 +809,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                         st_release(p.flags + static_cast<size_t>(r.gA.s) * p.R + gi % p.R,
                                    (static_cast<unsigned>(gi + 1) << 2) | 1u);
                     }
+                    if (kLag == 1) {  // S_in is needed in the next round
+                        if (!(ok = lookback(j, r.tA)))
+                            break;
+                    }
                 }
             }
-            // the previous segment's look-back, one segment behind, so its
-            // predecessors have usually published their inclusive prefixes
-            if (ok && prev_t >= 0 && !(ok = lookback(j - 1, prev_t)))
+            // with a longer lag, the look-back runs one segment behind, when
+            // the predecessors have mostly published their inclusive prefixes
+            if (kLag > 1 && ok && prev_t >= 0 && !(ok = lookback(j - 1, prev_t)))
                 break;
             prev_t = r.nA ? r.tA : -1;
         }
