@@ -62,6 +62,28 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (read + write) of `kernel` on `workload`, from the
+    ncu summary under profiles/, or None when there is none or the kernel's
+    source has changed since it was taken (the summary records the SHA-256 of
+    the source file it measured)."""
+    import hashlib
+    import re
+
+    path = ROOT / "profiles" / f"{kernel}_{workload}_counters.md"
+    if not path.exists():
+        return None
+    text = path.read_text()
+    m_src = re.search(r"^source: (\S+) sha256 ([0-9a-f]{64})$", text, re.M)
+    m_tr = re.search(r"^traffic_bytes_per_launch: (\d+)$", text, re.M)
+    if not m_src or not m_tr:
+        return None
+    src = ROOT / m_src.group(1)
+    if not src.exists() or hashlib.sha256(src.read_bytes()).hexdigest() != m_src.group(2):
+        return None
+    return int(m_tr.group(1))
+
+
 # ------------------------------------------------------------ clocks -----
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during a region."""
@@ -277,6 +299,8 @@ def main():
                    "sample": f"{desc}; {dt:.1f} s wall"}
 
     achieved = bytes_per_launch / (ms_step / 1e3) / 1e9
+    kernel = ("k_fwd_tc64" if la_path_dtype(w) == "bf16" else "la_forward") if not decode \
+        else "k_decode_step"
     line = {
         "metric": METRIC if not decode else "batched decode step token*heads/s, d=dv=128",
         "value": value,
@@ -304,9 +328,8 @@ def main():
             "peak": peaks["hbm_gbs"],
             "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"],
-            "traffic": None,
-            "kernel": ("k_fwd_tc64" if la_path_dtype(w) == "bf16" else "la_forward (all launches)")
-                      if not decode else "k_decode_step",
+            "traffic": profiled_traffic(kernel, w.name),
+            "kernel": kernel,
             "peak_source": f"{peak_src} HBM copy bandwidth",
             "algorithmic_bytes_per_launch": bytes_per_launch,
         },

@@ -95,7 +95,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s for any single wait
 constexpr int kON = 80;                                // output accumulator: num (64), den, pad
 constexpr uint32_t kSBytes = kON * 128;                // [S_prev^T; z_prev] bf16, 80 x 64
 constexpr int NA = 2;                                  // phase-A K,V stages
-// per output warpgroup: Q, V (later the fp32 output staging), phi(K), S hi/lo
+// per output warpgroup: Q, V, phi(K), S hi/lo (phi(K) and S later the fp32 output staging)
 constexpr uint32_t CW_Q = 0, CW_V = 16384, CW_K = 32768, CW_S = 49152;
 constexpr uint32_t kCWBytes = CW_S + 2 * kSBytes;
 constexpr uint32_t OFF_CW = 0;                         // 2 x kCWBytes
@@ -107,7 +107,7 @@ constexpr int kMaxL = 8;       // largest segment (chunks)
 constexpr int NPH = 4;         // phi(K) scratch and snapshot ring depth, in segments
 constexpr uint32_t SMEM_BYTES = OFF_ONES + 2048 + 1024;  // + alignment slack
 static_assert(OFF_ONES % 1024 == 0 && kCWBytes % 1024 == 0 && kSBytes % 1024 == 0 &&
-                  CW_V == CW_Q + 16384,
+                  CW_S == CW_K + 16384 && CW_S + 16384 <= kCWBytes,
               "layout");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
@@ -140,7 +140,7 @@ struct TcParams {
 struct Misc {
     uint64_t seg_full[NS], seg_empty[NS];
     uint64_t a_full[NA], a_empty[NA];
-    uint64_t c_full[2], k_free[2], qv_free[2], s_done[2], o_done[2];
+    uint64_t qv_full[2], k_full[2], k_free[2], qv_free[2], s_done[2], o_done[2];
     uint64_t phik_stored[NPH], dseg_done, sin_ready[NSIN], sin_free[NSIN];
     uint64_t drain[3];
     uint32_t tmem;
@@ -148,6 +148,7 @@ struct Misc {
     int seg_ticket[NS];
     int nlist;
     int list[kMaxList];
+    volatile int trace_done;
 };
 static_assert(sizeof(Misc) <= kMiscBytes, "misc");
 
@@ -158,7 +159,7 @@ __device__ unsigned long long* g_tc_trace;
 #define TC_TRACE(i, ev)                                                                       \
     do {                                                                                      \
         if (g_tc_trace && (i) < 64)                                                           \
-            g_tc_trace[(static_cast<size_t>(blockIdx.x) * 64 + (i)) * 16 + (ev)] = clock64(); \
+            g_tc_trace[(static_cast<size_t>(blockIdx.x) * 64 + (i)) * 32 + (ev)] = clock64(); \
     } while (0)
 #else
 #define TC_TRACE(i, ev) \
@@ -459,6 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
         for (int i = 0; i < NSIN; ++i)
             mbar_init(&m->sin_free[i], 2);
         m->abort = 0;
+        m->trace_done = 0;
         fence_mbar_init();
         tma_prefetch_desc(&p.mq);
         tma_prefetch_desc(&p.mk);
@@ -568,27 +570,48 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     break;
                 for (int e = 0; e < mine; ++e, ++u) {
                     const int c = ci0 + 2 * e, k = c - ci;
+                    // Q and V once the previous chunk's MMAs are done; phi(K) once
+                    // its output tile (staged in the phi(K) and S slots) has left
+                    if (u >= 1 && !bwait(&m->qv_free[wg], (u - 1) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const int row = (r.gC.c0 + k) * kC;
+                    mbar_arrive_expect_tx(&m->qv_full[wg], 2 * kC * kD * 2);
+                    tma_load_3d(cw + CW_Q, &p.mq, 0, row, r.gC.s, &m->qv_full[wg], stream);
+                    tma_load_3d(cw + CW_V, &p.mv, 0, row, r.gC.s, &m->qv_full[wg], stream);
+                    TC_TRACE(c, 0);
                     if (u >= 1 && !bwait(&m->k_free[wg], (u - 1) & 1, abort)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&m->c_full[wg], 3 * kC * kD * 2);
-                    tma_load_3d(cw + CW_K, &p.mphi, 0, 0, phi_index(jc, k), &m->c_full[wg], stream);
-                    if (u >= 1 && !bwait(&m->qv_free[wg], (u - 1) & 1, abort)) {
-                        ok = false;  // this phase cannot complete: not drained below
-                        break;
-                    }
-                    const int row = (r.gC.c0 + k) * kC;
-                    tma_load_3d(cw + CW_Q, &p.mq, 0, row, r.gC.s, &m->c_full[wg], stream);
-                    tma_load_3d(cw + CW_V, &p.mv, 0, row, r.gC.s, &m->c_full[wg], stream);
+                    mbar_arrive_expect_tx(&m->k_full[wg], kC * kD * 2);
+                    tma_load_3d(cw + CW_K, &p.mphi, 0, 0, phi_index(jc, k), &m->k_full[wg], stream);
                     c_last = u;
-                    TC_TRACE(c, 0);
                 }
                 ci += r.nC;
             }
-            if (*abort && c_last >= 0)  // let every complete load set land before exit
-                drain_wait(&m->c_full[wg], c_last & 1);
+            if (*abort && c_last >= 0) {  // let every complete load set land before exit
+                drain_wait(&m->qv_full[wg], c_last & 1);
+                drain_wait(&m->k_full[wg], c_last & 1);
+            }
         }
+#ifdef LA_TC_TRACE
+    } else if (warp == 1) {
+        // trace builds: record when each load set lands (phase completions)
+        if (lane == 0 && g_tc_trace) {
+            int uq0 = 0, uq1 = 0, uk0 = 0, uk1 = 0, ua = 0;
+            const uint64_t t0 = globaltimer();
+            while (m->trace_done < 2 && globaltimer() - t0 < 500000000ull && !*abort) {
+                __nanosleep(20);
+                if (mbar_test_wait(&m->qv_full[0], uq0 & 1)) { TC_TRACE(uq0, 16); ++uq0; }
+                if (mbar_test_wait(&m->qv_full[1], uq1 & 1)) { TC_TRACE(uq1, 17); ++uq1; }
+                if (mbar_test_wait(&m->k_full[0], uk0 & 1)) { TC_TRACE(uk0, 18); ++uk0; }
+                if (mbar_test_wait(&m->k_full[1], uk1 & 1)) { TC_TRACE(uk1, 19); ++uk1; }
+                if (mbar_test_wait(&m->a_full[ua % NA], (ua / NA) & 1)) { TC_TRACE(ua, 20); ++ua; }
+            }
+        }
+#endif
     } else if (warp >= 4 && warp < 8) {
         // -------------------------- phase A (warpgroup of warps 4-7) --------
         // phi(K) in place and to the scratch ring; the segment's running
@@ -710,8 +733,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
             const int n = m->nlist;
             if (n < 0)
                 return false;
-            if (lead)
+            if (lead) {
                 TC_TRACE(jl, 11);
+#ifdef LA_TC_TRACE
+                if (g_tc_trace && jl < 64)
+                    g_tc_trace[(static_cast<size_t>(blockIdx.x) * 64 + jl) * 32 + 21] = n;
+#endif
+            }
             // thread tb owns float4 words tb + 128 v of the state
             constexpr int NV = (kStateFloats / 4 + 127) / 128;  // 9
             float4 acc[NV];
@@ -749,9 +777,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                                                 acc[v].w + a.w));
                 }
             }
+            if (lead)
+                TC_TRACE(jl, 22);
             __threadfence();
             named_bar(1, 128);
             if (lead) {
+                TC_TRACE(jl, 23);
                 st_release(const_cast<unsigned*>(flag_base) + my,
                            (static_cast<unsigned>(gi + 1) << 2) | 2u);
                 mbar_arrive(&m->sin_ready[jl % NSIN]);
@@ -877,6 +908,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     const float* s_pf = snap_ptr(jc, max(k - 1, 0));
                     unsigned char* sShi = cw + CW_S;
                     unsigned char* sSlo = sShi + kSBytes;
+                    // rows 65..79 of the hi part were output staging: zero again
+                    if (tc < 15 * 8)
+                        *reinterpret_cast<uint4*>(sShi + (65 + (tc >> 3)) * 128 + (tc & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
                     constexpr int NU = 4;
                     const int nu = NU + (tc < 8 ? 1 : 0);  // 520 items = 4 x 128 + 8
                     float4 x[NU + 1][2], y[NU + 1][2];
@@ -914,8 +949,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                         }
                     }
                 }
-                // Q, phi(K), V of chunk c
-                if (!group_ok(!lead || bwait(&m->c_full[wg], u & 1, abort), barid, 128)) {
+                // Q and V of chunk c
+                if (!group_ok(!lead || bwait(&m->qv_full[wg], u & 1, abort), barid, 128)) {
                     ok = false;
                     break;
                 }
@@ -933,8 +968,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 named_bar(barid, 128);
                 if (lead)
                     TC_TRACE(c, 1);
-                // scores into this group's score buffer
-                if (wq == 0) {
+                // scores into this group's score buffer, once phi(K) is in
+                if (wq == 0 && __all_sync(full, bwait(&m->k_full[wg], u & 1, abort))) {
                     tc_fence_after();
                     const uint64_t dq = sdesc_sw128(cwa + CW_Q, 16, 1024);
                     const uint64_t dk = sdesc_sw128(cwa + CW_K, 16, 1024);
@@ -960,10 +995,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     ok = false;
                     break;
                 }
-                if (lead) {
-                    mbar_arrive(&m->k_free[wg]);  // phi(K) slot free for the next chunk
+                if (lead)
                     TC_TRACE(c, 3);
-                }
                 // the scores were the last reader of the chunk's phi(K) tile
                 l2_discard(static_cast<unsigned char*>(p.phi_scratch) +
                            static_cast<size_t>(phi_index(jc, k)) * (kC * kD * 2) + 128 * tc);
@@ -1043,9 +1076,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     break;
                 }
                 tc_fence_after();
-                if (lead)
+                if (lead) {
+                    mbar_arrive(&m->qv_free[wg]);  // Q and V slots free for the next chunk
                     TC_TRACE(c, 7);
-                // epilogue: o = num / den into the staging area (the Q and V
+                }
+                // epilogue: o = num / den into the staging area (the phi(K) and S
                 // slots, free now), then two TMA stores of 32 columns
                 {
                     const uint32_t o = to + lane_off;
@@ -1056,7 +1091,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     const uint32_t dn = tmem_ld1(o + kD);
                     tmem_ld_wait();
                     const float inv = norm ? 1.0f / fmaxf(__uint_as_float(dn), FLT_MIN) : 1.0f;
-                    unsigned char* sO = cw + CW_Q;
+                    unsigned char* sO = cw + CW_K;  // columns 32..63 land in the S slot
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
 #pragma unroll
@@ -1079,14 +1114,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 named_bar(barid, 128);
                 if (lead) {
                     const int row = (r.gC.c0 + k) * kC;
-                    tma_store_3d(&p.mo, cw + CW_Q, 0, row, r.gC.s, pol);
-                    tma_store_3d(&p.mo, cw + CW_V, 32, row, r.gC.s, pol);
+                    tma_store_3d(&p.mo, cw + CW_K, 0, row, r.gC.s, pol);
+                    tma_store_3d(&p.mo, cw + CW_S, 32, row, r.gC.s, pol);
                     bulk_commit();
                     TC_TRACE(c, 8);
-                    // the tile has left the Q and V slots: let the next loads in
+                    // the tile has left the phi(K) and S slots: the next phi(K)
+                    // may land and S_prev may be rebuilt
                     bulk_wait_read<0>();
-                    mbar_arrive(&m->qv_free[wg]);
+                    mbar_arrive(&m->k_free[wg]);
                 }
+                named_bar(barid, 128);
             }
             // this group is done with the segment's S_in and ticket slot
             if (ok && lead) {
@@ -1095,8 +1132,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
             }
             ci += r.nC;
         }
-        if (lead)
+        if (lead) {
             bulk_wait<0>();
+#ifdef LA_TC_TRACE
+            atomicAdd(const_cast<int*>(&m->trace_done), 1);
+#endif
+        }
         if (issued && *abort) {
             mma_commit_w(&m->drain[1 + wg], issue);
             drain_wait(&m->drain[1 + wg], 0);
