@@ -62,6 +62,21 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's value (every rank gets it); x itself on one rank."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_step: int, world: int, steps: int, ms_total: float) -> float:
+    """Whole-job units per second: every rank processes units_per_step per
+    step (weak scaling), the job takes the slowest rank's time."""
+    return units_per_step * world * steps / (ms_total / 1e3)
+
+
 def profiled_traffic(kernel: str, workload: str):
     """DRAM bytes per launch (read + write) of `kernel` on `workload`, from the
     ncu summary under profiles/, or None when there is none or the kernel's
@@ -273,13 +288,9 @@ def main():
         torch.cuda.synchronize()
         n1 = la.la_launch_count()
         barrier()
-    ms_total = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms_total], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world, "cuda")
     ms_step = ms_total / steps
-    value = units_per_step * world * steps / (ms_total / 1e3)
+    value = job_throughput(units_per_step, world, steps, ms_total)
     assert la.la_get_device_status() == 0
 
     # --- end to end through the C ABI with pinned host buffers ------------
