@@ -89,6 +89,8 @@ constexpr int NSIN = 4;        // S_in ring (a segment's S_in lives through its 
 constexpr int kStateFloats = kD * kD + kD;         // S^T (dv x d) then z (d)
 constexpr int kSlotFloats = 2 * kStateFloats;      // aggregate, inclusive
 constexpr int kMaxList = 128;                      // look-back entries
+constexpr uint32_t kImgPart = 65 * 128;            // rows 0..64 of one bf16 part (hi or lo)
+constexpr uint32_t kImgBytes = 2 * kImgPart;       // one S_prev operand image: hi, then lo
 constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s for any single wait
 
 // shared memory (offsets from a 1024-byte aligned base)
@@ -130,7 +132,7 @@ struct TcParams {
     unsigned* counter;
     unsigned* flags;
     float* slots;
-    float* sin_scratch;  // per CTA: NSIN x S_in
+    unsigned char* sprime;  // per CTA: NSIN x L images of [S_prev^T; z_prev] hi, lo (kImgBytes)
     void* phi_scratch;   // the tiles mphi describes
     float* snap;         // per CTA: NPH x (L-1) prefix snapshots [S^T; z]
     float* out;          // [BH][N][64] fp32
@@ -141,7 +143,8 @@ struct Misc {
     uint64_t seg_full[NS], seg_empty[NS];
     uint64_t a_full[NA], a_empty[NA];
     uint64_t qv_full[2], k_full[2], k_free[2], qv_free[2], s_done[2], o_done[2];
-    uint64_t phik_stored[NPH], dseg_done, sin_ready[NSIN], sin_free[NSIN];
+    uint64_t phik_stored[NPH], dseg_done, sin_ready[NSIN], sin_free[NSIN], agg_ready[NSIN],
+        sp_ready[NSIN];
     uint64_t drain[3];
     uint32_t tmem;
     int abort;
@@ -507,122 +510,370 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
     };
 
     if (warp == 0) {
-        // --------------------------------- producer: tickets, phase-A loads --
+        // ------------------------------------------ producer (one thread) --
+        // Three load streams, each advanced as soon as its next step is free:
+        // the tickets with the phase-A K,V stages, and the phase-C loads of
+        // each output warpgroup.  Chunk ci of phase C goes to warpgroup
+        // ci & 1: Q and V once that group's previous chunk is done with them,
+        // phi(K) once its previous output tile has left the staging area and,
+        // for a segment's first chunk, once phase A has released the tiles.
         if (lane == 0) {
             const uint64_t keep = policy_evict_last();
             const uint64_t stream = policy_evict_first();
             int a_last[NA];
             for (int i = 0; i < NA; ++i)
                 a_last[i] = -1;
-            int ai = 0;
-            for (int j = 0;; ++j) {
-                const int ss = j % NS;
-                if (j >= NS && !bwait(&m->seg_empty[ss], ((j / NS) & 1) ^ 1, abort))
-                    break;
-                const int t = static_cast<int>(atomicAdd(p.counter, 1u));
-                m->seg_ticket[ss] = t;
-                mbar_arrive(&m->seg_full[ss]);
-                if (t >= p.total)
-                    break;
-                const Seg g = seg_of(p, t);
-                bool ok = true;
-                for (int k = 0; k < g.n; ++k, ++ai) {
-                    const int s = ai % NA;
-                    if (ai >= NA && !bwait(&m->a_empty[s], ((ai / NA) & 1) ^ 1, abort)) {
-                        ok = false;
+            int ja = 0, ka = 0, ai = 0, nt = 0;  // nt: tickets published
+            bool a_seg = false, a_done = false;
+            Seg ga{};
+            struct CStream {
+                int jc = 0, cbase = 0, e = 0, mine = 0, k0 = 0, u = 0;
+                int qv_last = -1, k_last = -1;
+                bool seg = false, kphase = false, done = false;
+                Seg g{};
+            } cs[2];
+            uint64_t idle_since = 0;
+            while (!(a_done && cs[0].done && cs[1].done)) {
+                bool prog = false;
+                if (!a_done) {
+                    if (!a_seg) {
+                        const int ss = ja % NS;
+                        if (ja < NS || mbar_test_wait(&m->seg_empty[ss], ((ja / NS) & 1) ^ 1)) {
+                            const int t = static_cast<int>(atomicAdd(p.counter, 1u));
+                            m->seg_ticket[ss] = t;
+                            mbar_arrive(&m->seg_full[ss]);
+                            ++nt;
+                            prog = true;
+                            if (t >= p.total) {
+                                a_done = true;
+                            } else {
+                                ga = seg_of(p, t);
+                                ka = 0;
+                                a_seg = true;
+                            }
+                        }
+                    } else {
+                        const int s = ai % NA;
+                        if (ai < NA || mbar_test_wait(&m->a_empty[s], ((ai / NA) & 1) ^ 1)) {
+                            mbar_arrive_expect_tx(&m->a_full[s], 2 * kC * kD * 2);
+                            unsigned char* st = sm + OFF_A + s * 32768;
+                            tma_load_3d(st + 16384, &p.mk, 0, (ga.c0 + ka) * kC, ga.s, &m->a_full[s],
+                                        stream);
+                            tma_load_3d(st, &p.mv, 0, (ga.c0 + ka) * kC, ga.s, &m->a_full[s], keep);
+                            a_last[s] = ai / NA;
+                            ++ai;
+                            prog = true;
+                            if (++ka == ga.n) {
+                                a_seg = false;
+                                ++ja;
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int wg = 0; wg < 2; ++wg) {
+                    CStream& c = cs[wg];
+                    if (c.done)
+                        continue;
+                    if (!c.seg) {  // the next segment, once its ticket is out
+                        if (c.jc >= nt)
+                            continue;
+                        const int t = m->seg_ticket[c.jc % NS];
+                        prog = true;
+                        if (t >= p.total) {
+                            c.done = true;
+                            continue;
+                        }
+                        c.g = seg_of(p, t);
+                        const int ci0 = c.cbase + ((c.cbase & 1) != wg ? 1 : 0);
+                        c.k0 = ci0 - c.cbase;
+                        c.mine = ci0 < c.cbase + c.g.n ? (c.cbase + c.g.n - ci0 + 1) / 2 : 0;
+                        c.e = 0;
+                        c.seg = c.mine > 0;
+                        if (!c.seg) {
+                            c.cbase += c.g.n;
+                            ++c.jc;
+                            continue;
+                        }
+                    }
+                    unsigned char* cw = sm + OFF_CW + wg * kCWBytes;
+                    const int row = (c.g.c0 + c.k0 + 2 * c.e) * kC;
+                    if (!c.kphase &&
+                        (c.u == 0 || mbar_test_wait(&m->qv_free[wg], (c.u - 1) & 1))) {
+                        mbar_arrive_expect_tx(&m->qv_full[wg], 2 * kC * kD * 2);
+                        tma_load_3d(cw + CW_Q, &p.mq, 0, row, c.g.s, &m->qv_full[wg], stream);
+                        tma_load_3d(cw + CW_V, &p.mv, 0, row, c.g.s, &m->qv_full[wg], stream);
+                        c.qv_last = c.u;
+                        c.kphase = true;
+                        prog = true;
+                        TC_TRACE(c.cbase + c.k0 + 2 * c.e, 0);
+                    }
+                    const int kk = c.k0 + 2 * c.e;
+                    if (c.kphase &&
+                        (c.e > 0 ||
+                         mbar_test_wait(&m->phik_stored[c.jc % NPH], (c.jc / NPH) & 1)) &&
+                        mbar_test_wait(kk == 0 ? &m->sin_ready[c.jc % NSIN] : &m->sp_ready[c.jc % NSIN],
+                                       (c.jc / NSIN) & 1) &&
+                        (c.u == 0 || mbar_test_wait(&m->k_free[wg], (c.u - 1) & 1))) {
+                        mbar_arrive_expect_tx(&m->k_full[wg], kC * kD * 2 + kImgBytes);
+                        tma_load_3d(cw + CW_K, &p.mphi, 0, 0, phi_index(c.jc, kk), &m->k_full[wg],
+                                    stream);
+                        const unsigned char* img =
+                            p.sprime +
+                            ((static_cast<size_t>(blockIdx.x) * NSIN + c.jc % NSIN) * p.L + kk) *
+                                kImgBytes;
+                        bulk_load(cw + CW_S, img, kImgPart, &m->k_full[wg], stream);
+                        bulk_load(cw + CW_S + kSBytes, img + kImgPart, kImgPart, &m->k_full[wg],
+                                  stream);
+                        c.k_last = c.u;
+                        c.kphase = false;
+                        ++c.u;
+                        prog = true;
+                        if (++c.e == c.mine) {
+                            c.seg = false;
+                            c.cbase += c.g.n;
+                            ++c.jc;
+                        }
+                    }
+                }
+                if (prog) {
+                    idle_since = 0;
+                } else {
+                    if (*abort)
+                        break;
+                    const uint64_t now = globaltimer();
+                    if (!idle_since) {
+                        idle_since = now;
+                    } else if (now - idle_since > kWaitNs) {
+                        set_status(p.status, LA_ERR_TIMEOUT);
+                        *abort = 1;
                         break;
                     }
-                    mbar_arrive_expect_tx(&m->a_full[s], 2 * kC * kD * 2);
-                    unsigned char* st = sm + OFF_A + s * 32768;
-                    tma_load_3d(st + 16384, &p.mk, 0, (g.c0 + k) * kC, g.s, &m->a_full[s], stream);
-                    tma_load_3d(st, &p.mv, 0, (g.c0 + k) * kC, g.s, &m->a_full[s], keep);
-                    a_last[s] = ai / NA;
+                    __nanosleep(32);
                 }
-                if (!ok)
-                    break;
             }
-            if (*abort)  // let every load this thread issued land before exit
+            if (*abort) {  // let every load this thread issued land before exit
                 for (int i = 0; i < NA; ++i)
                     if (a_last[i] >= 0)
                         drain_wait(&m->a_full[i], a_last[i] & 1);
-        }
-    } else if (warp == 2 || warp == 3) {
-        // ----------------------------- producers: phase-C loads (warps 2, 3) --
-        // Chunk ci of phase C goes to output warpgroup ci & 1, whose loads
-        // warp 2 + (ci & 1) issues: phi(K) as soon as that group's previous
-        // scores are done, Q and V once its previous output tile has left the
-        // staging area (the Q and V slots).
-        if (lane == 0) {
-            const int wg = warp - 2;
-            const uint64_t stream = policy_evict_first();
-            unsigned char* cw = sm + OFF_CW + wg * kCWBytes;
-            int c_last = -1, ci = 0, u = 0;
-            bool ok = true;
-            RoundWalker w;
-            Round r;
-            for (int j = 0; ok && w.next(p, m, r, j, true, -1, 1, abort); ++j) {
-                if (!r.nC)
-                    continue;
-                const int jc = j - kLag;
-                const int ci0 = ci + ((ci & 1) != wg ? 1 : 0);
-                const int mine = ci0 < ci + r.nC ? (ci + r.nC - ci0 + 1) / 2 : 0;
-                if (mine && !bwait(&m->phik_stored[jc % NPH], (jc / NPH) & 1, abort))
-                    break;
-                for (int e = 0; e < mine; ++e, ++u) {
-                    const int c = ci0 + 2 * e, k = c - ci;
-                    // Q and V once the previous chunk's MMAs are done; phi(K) once
-                    // its output tile (staged in the phi(K) and S slots) has left
-                    if (u >= 1 && !bwait(&m->qv_free[wg], (u - 1) & 1, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    const int row = (r.gC.c0 + k) * kC;
-                    mbar_arrive_expect_tx(&m->qv_full[wg], 2 * kC * kD * 2);
-                    tma_load_3d(cw + CW_Q, &p.mq, 0, row, r.gC.s, &m->qv_full[wg], stream);
-                    tma_load_3d(cw + CW_V, &p.mv, 0, row, r.gC.s, &m->qv_full[wg], stream);
-                    TC_TRACE(c, 0);
-                    if (u >= 1 && !bwait(&m->k_free[wg], (u - 1) & 1, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&m->k_full[wg], kC * kD * 2);
-                    tma_load_3d(cw + CW_K, &p.mphi, 0, 0, phi_index(jc, k), &m->k_full[wg], stream);
-                    c_last = u;
+                for (int wg = 0; wg < 2; ++wg) {
+                    if (cs[wg].qv_last >= 0)
+                        drain_wait(&m->qv_full[wg], cs[wg].qv_last & 1);
+                    if (cs[wg].k_last >= 0)
+                        drain_wait(&m->k_full[wg], cs[wg].k_last & 1);
                 }
-                ci += r.nC;
-            }
-            if (*abort && c_last >= 0) {  // let every complete load set land before exit
-                drain_wait(&m->qv_full[wg], c_last & 1);
-                drain_wait(&m->k_full[wg], c_last & 1);
             }
         }
+    } else if (warp < 4) {
+        // ------------------------------------ look-back (warps 1-3) --------
+        // For each segment whose aggregate phase A has published: what the
+        // predecessors have published, the nearest exclusive prefix with that
+        // segment's aggregate and every aggregate after it, summed farthest
+        // first, gives S_in of this segment bitwise equal to adding the
+        // aggregates one by one from the start of the sequence.  S_in goes to
+        // the output warpgroups and is published as this segment's exclusive
+        // prefix.
+        constexpr int kLB = 96, barLB = 4;
+        const int tl = tid - 32;
+        const bool lead = tl == 0;
+        bool ok = true;
+        RoundWalker w;
+        Round r;
+        for (int j = 0; ok && w.next(p, m, r, j, lead, barLB, kLB, abort); ++j) {
+            if (!r.nA)
+                continue;
+            if (!group_ok(!lead || (bwait(&m->agg_ready[j % NSIN], (j / NSIN) & 1, abort) &&
+                                    (j < NSIN || bwait(&m->sin_free[j % NSIN],
+                                                       ((j / NSIN) & 1) ^ 1, abort))),
+                          barLB, kLB)) {
+                ok = false;
+                break;
+            }
+            const int t = r.tA, gi = t / p.BH, my = gi % p.R;
+            unsigned* flag_base = p.flags + static_cast<size_t>(r.gA.s) * p.R;
+            float* slot_base = p.slots + static_cast<size_t>(r.gA.s) * p.R * kSlotFloats;
+            if (lead)
+                TC_TRACE(j, 5);
+            if (warp == 1) {
+                // Lane l watches segment base - l.  With a wrapping ring only
+                // R-1 slots behind this segment are distinct from its own; a
+                // slot holding another epoch reads as not ready.  List entries
+                // are slot << 1 | part (0: aggregate, 1: exclusive prefix),
+                // nearest first.
+                const int W = p.R >= p.nseg ? 32 : min(32, p.R - 1);
+                const unsigned active = W >= 32 ? 0xffffffffu : ((1u << W) - 1u);
+                int n = 0, base = gi - 1;
+                uint64_t start = 0;
+                while (base >= 0) {
+                    const int pg = base - lane;
+                    bool ready = true, excl = true;
+                    if (lane >= W) {
+                        ready = excl = false;
+                    } else if (pg >= 0) {
+                        const unsigned f = ld_acquire(flag_base + pg % p.R);
+                        ready = (f >> 2) == static_cast<unsigned>(pg + 1) && (f & 3u) != 0u;
+                        excl = ready && (f & 3u) == 2u;
+                    }
+                    const unsigned mi = __ballot_sync(full, excl) & active;
+                    const unsigned mr = __ballot_sync(full, ready) & active;
+                    if (mi) {
+                        const int ls = __ffs(mi) - 1;
+                        const unsigned need = ls == 0 ? 0u : ((1u << ls) - 1u);
+                        if ((mr & need) == need) {
+                            const int tail = base - ls >= 0 ? 2 : 0;
+                            if (n + ls + tail > kMaxList) {
+                                n = -2;
+                                break;
+                            }
+                            if (lane < ls)
+                                m->list[n + lane] = (pg % p.R) << 1;
+                            if (lane == ls && tail) {
+                                m->list[n + ls] = (pg % p.R) << 1;
+                                m->list[n + ls + 1] = ((pg % p.R) << 1) | 1;
+                            }
+                            n += ls + tail;
+                            break;
+                        }
+                    } else if (mr == active) {
+                        if (n + W > kMaxList) {
+                            n = -2;
+                            break;
+                        }
+                        if (lane < W)
+                            m->list[n + lane] = (pg % p.R) << 1;
+                        n += W;
+                        base -= W;
+                        start = 0;
+                        continue;
+                    }
+                    const uint64_t now = globaltimer();
+                    if (!start)
+                        start = now;
+                    if (__any_sync(full, now - start > kWaitNs || *abort)) {
+                        n = -1;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+                if (lane == 0) {
+                    m->nlist = n;
+                    if (n < 0) {
+                        set_status(p.status, n == -1 ? LA_ERR_TIMEOUT : LA_ERR_DEVICE_CHECK);
+                        *abort = 1;
+                    }
+                }
+            }
+            named_bar(barLB, kLB);
+            const int n = m->nlist;
+            if (n < 0) {
+                ok = false;
+                break;
+            }
+            if (lead) {
+                TC_TRACE(j, 11);
 #ifdef LA_TC_TRACE
-    } else if (warp == 1) {
-        // trace builds: record when each load set lands (phase completions)
-        if (lane == 0 && g_tc_trace) {
-            int uq0 = 0, uq1 = 0, uk0 = 0, uk1 = 0, ua = 0;
-            const uint64_t t0 = globaltimer();
-            while (m->trace_done < 2 && globaltimer() - t0 < 500000000ull && !*abort) {
-                __nanosleep(20);
-                if (mbar_test_wait(&m->qv_full[0], uq0 & 1)) { TC_TRACE(uq0, 16); ++uq0; }
-                if (mbar_test_wait(&m->qv_full[1], uq1 & 1)) { TC_TRACE(uq1, 17); ++uq1; }
-                if (mbar_test_wait(&m->k_full[0], uk0 & 1)) { TC_TRACE(uk0, 18); ++uk0; }
-                if (mbar_test_wait(&m->k_full[1], uk1 & 1)) { TC_TRACE(uk1, 19); ++uk1; }
-                if (mbar_test_wait(&m->a_full[ua % NA], (ua / NA) & 1)) { TC_TRACE(ua, 20); ++ua; }
+                if (g_tc_trace && j < 64)
+                    g_tc_trace[(static_cast<size_t>(blockIdx.x) * 64 + j) * 32 + 21] = n;
+#endif
+            }
+            // thread tl owns float4 words tl + 96 v of the state
+            constexpr int NV = (kStateFloats / 4 + kLB - 1) / kLB;  // 11
+            float4 acc[NV];
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+                acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int e = n - 1; e >= 0; --e) {
+                const int ent = m->list[e];
+                const float4* src = reinterpret_cast<const float4*>(
+                    slot_base + static_cast<size_t>(ent >> 1) * kSlotFloats +
+                    ((ent & 1) ? kStateFloats : 0));
+                float4 x[NV];
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+                    if (tl + kLB * v < kStateFloats / 4)
+                        x[v] = __ldcg(src + tl + kLB * v);
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+                    if (tl + kLB * v < kStateFloats / 4)
+                        acc[v].x += x[v].x, acc[v].y += x[v].y, acc[v].z += x[v].z,
+                            acc[v].w += x[v].w;
+            }
+            // S_prev operand image k of the segment: S_in plus the prefix
+            // snapshot before chunk k, as bf16 hi and lo parts of rows 0..64 in
+            // the 128-byte swizzled layout of the output groups' operand slot
+            unsigned char* img0 =
+                p.sprime + (static_cast<size_t>(blockIdx.x) * NSIN + j % NSIN) * p.L * kImgBytes;
+            auto put = [&](unsigned char* img, int f, float4 x) {
+                const int row = f >> 4, q = f & 15;
+                uint32_t h0, l0, h1, l1;
+                split2(x.x, x.y, h0, l0);
+                split2(x.z, x.w, h1, l1);
+                const uint32_t off = sw128_off(row, q >> 1) + (q & 1) * 8;
+                __stcg(reinterpret_cast<uint2*>(img + off), make_uint2(h0, h1));
+                __stcg(reinterpret_cast<uint2*>(img + kImgPart + off), make_uint2(l0, l1));
+            };
+            float4* exc = reinterpret_cast<float4*>(slot_base + static_cast<size_t>(my) * kSlotFloats +
+                                                    kStateFloats);
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const int f = tl + kLB * v;
+                if (f < kStateFloats / 4) {
+                    __stcg(exc + f, acc[v]);
+                    put(img0, f, acc[v]);
+                }
+            }
+            if (lead)
+                TC_TRACE(j, 22);
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            __threadfence();
+            named_bar(barLB, kLB);
+            if (lead) {
+                TC_TRACE(j, 23);
+                st_release(flag_base + my, (static_cast<unsigned>(gi + 1) << 2) | 2u);
+                mbar_arrive(&m->sin_ready[j % NSIN]);
+                TC_TRACE(j, 12);
+            }
+            // the images of the later chunks, from the snapshots
+            for (int k = 1; k < r.nA; ++k) {
+                const float4* sn4 = reinterpret_cast<const float4*>(snap_ptr(j, k - 1));
+                float4 y[NV];
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+                    if (tl + kLB * v < kStateFloats / 4)
+                        y[v] = __ldcg(sn4 + tl + kLB * v);
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    const int f = tl + kLB * v;
+                    if (f < kStateFloats / 4) {
+                        float4 x = acc[v];
+                        x.x += y[v].x, x.y += y[v].y, x.z += y[v].z, x.w += y[v].w;
+                        put(img0 + k * kImgBytes, f, x);
+                    }
+                }
+            }
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            __threadfence();
+            named_bar(barLB, kLB);
+            if (lead)
+                mbar_arrive(&m->sp_ready[j % NSIN]);
+            // every thread has read the snapshots: drop them from L2
+            for (int k = 1; k < r.nA; ++k) {
+                const unsigned char* sb = reinterpret_cast<const unsigned char*>(snap_ptr(j, k - 1));
+                for (int l = tl; l < (kStateFloats * 4) / 128; l += kLB)
+                    l2_discard(sb + 128 * l);
             }
         }
-#endif
     } else if (warp >= 4 && warp < 8) {
         // -------------------------- phase A (warpgroup of warps 4-7) --------
         // phi(K) in place and to the scratch ring; the segment's running
         // [dS^T; dz] on the tensor cores (warp 4 issues), read out after every
-        // chunk as a prefix snapshot, the last as the segment aggregate.  After
-        // each segment's aggregate, the look-back of the segment before it.
+        // chunk as a prefix snapshot, the last as the segment aggregate, which
+        // is published for the look-back warps and the other segments.
         const int tb = tid - 128, wb = warp - 4;
         const bool lead = tb == 0;
         const uint32_t issue = wb == 0 ? elect_one() : 0u;
         const uint32_t a0 = smem_addr(sm + OFF_A);
-        int ai = 0, prev_t = -1;
+        int ai = 0;
         bool ok = true, issued = false;
         // [dS^T; dz] so far (tensor-memory lanes 0..64) copied to dst
         auto readout = [&](int x, float* dst) -> bool {
@@ -649,145 +900,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
             }
             tc_fence_before();
             named_bar(1, 128);
-            return true;
-        };
-        // Decoupled look-back of local segment jl (ticket t): S_in, the state
-        // before it, from the nearest inclusive prefix plus the later
-        // aggregates in segment order; then its own inclusive prefix.
-        auto lookback = [&](int jl, int t) -> bool {
-            if (!group_ok(!lead || jl < NSIN ||
-                              bwait(&m->sin_free[jl % NSIN], ((jl / NSIN) & 1) ^ 1, abort),
-                          1, 128))
-                return false;
-            const Seg g = seg_of(p, t);
-            const int gi = t / p.BH;
-            const unsigned* flag_base = p.flags + static_cast<size_t>(g.s) * p.R;
-            float* slot_base = p.slots + static_cast<size_t>(g.s) * p.R * kSlotFloats;
-            if (lead)
-                TC_TRACE(jl, 5);
-            if (wb == 0) {
-                // Lane l watches segment base - l.  With a wrapping ring only
-                // R-1 slots behind this segment are distinct from its own; a
-                // slot holding another epoch reads as not ready.
-                const int W = p.R >= p.nseg ? 32 : min(32, p.R - 1);
-                const unsigned active = W >= 32 ? 0xffffffffu : ((1u << W) - 1u);
-                int n = 0, base = gi - 1;
-                uint64_t start = 0;
-                while (base >= 0) {
-                    const int pg = base - lane;
-                    bool ready = true, incl = true;
-                    if (lane >= W) {
-                        ready = incl = false;
-                    } else if (pg >= 0) {
-                        const unsigned f = ld_acquire(flag_base + pg % p.R);
-                        ready = (f >> 2) == static_cast<unsigned>(pg + 1) && (f & 3u) != 0u;
-                        incl = ready && (f & 3u) == 2u;
-                    }
-                    const unsigned mi = __ballot_sync(full, incl) & active;
-                    const unsigned mr = __ballot_sync(full, ready) & active;
-                    if (mi) {
-                        const int ls = __ffs(mi) - 1;
-                        const unsigned need = ls == 0 ? 0u : ((1u << ls) - 1u);
-                        if ((mr & need) == need) {
-                            if (n + ls + 1 > kMaxList) {
-                                n = -2;
-                                break;
-                            }
-                            if (lane < ls)
-                                m->list[n + lane] = (pg % p.R) << 1;
-                            if (lane == ls && pg >= 0)
-                                m->list[n + lane] = ((pg % p.R) << 1) | 1;
-                            n += ls + (base - ls >= 0 ? 1 : 0);
-                            break;
-                        }
-                    } else if (mr == active) {
-                        if (n + W > kMaxList) {
-                            n = -2;
-                            break;
-                        }
-                        if (lane < W)
-                            m->list[n + lane] = (pg % p.R) << 1;
-                        n += W;
-                        base -= W;
-                        start = 0;
-                        continue;
-                    }
-                    const uint64_t now = globaltimer();
-                    if (!start)
-                        start = now;
-                    if (__any_sync(full, now - start > kWaitNs || *abort)) {
-                        n = -1;
-                        break;
-                    }
-                    __nanosleep(200);
-                }
-                if (lane == 0) {
-                    m->nlist = n;
-                    if (n < 0) {
-                        set_status(p.status, n == -1 ? LA_ERR_TIMEOUT : LA_ERR_DEVICE_CHECK);
-                        *abort = 1;
-                    }
-                }
-            }
-            named_bar(1, 128);
-            const int n = m->nlist;
-            if (n < 0)
-                return false;
-            if (lead) {
-                TC_TRACE(jl, 11);
-#ifdef LA_TC_TRACE
-                if (g_tc_trace && jl < 64)
-                    g_tc_trace[(static_cast<size_t>(blockIdx.x) * 64 + jl) * 32 + 21] = n;
-#endif
-            }
-            // thread tb owns float4 words tb + 128 v of the state
-            constexpr int NV = (kStateFloats / 4 + 127) / 128;  // 9
-            float4 acc[NV];
-#pragma unroll
-            for (int v = 0; v < NV; ++v)
-                acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int e = n - 1; e >= 0; --e) {
-                const int ent = m->list[e];
-                const float4* src = reinterpret_cast<const float4*>(
-                    slot_base + static_cast<size_t>(ent >> 1) * kSlotFloats +
-                    ((ent & 1) ? kStateFloats : 0));
-#pragma unroll
-                for (int v = 0; v < NV; ++v) {
-                    const int f = tb + 128 * v;
-                    if (f < kStateFloats / 4) {
-                        const float4 x = __ldcg(src + f);
-                        acc[v].x += x.x, acc[v].y += x.y, acc[v].z += x.z, acc[v].w += x.w;
-                    }
-                }
-            }
-            float4* sin = reinterpret_cast<float4*>(
-                p.sin_scratch + (static_cast<size_t>(blockIdx.x) * NSIN + jl % NSIN) * kStateFloats);
-            const int my = gi % p.R;
-            const float4* agg =
-                reinterpret_cast<const float4*>(slot_base + static_cast<size_t>(my) * kSlotFloats);
-            float4* inc = reinterpret_cast<float4*>(slot_base + static_cast<size_t>(my) * kSlotFloats +
-                                                    kStateFloats);
-#pragma unroll
-            for (int v = 0; v < NV; ++v) {
-                const int f = tb + 128 * v;
-                if (f < kStateFloats / 4) {
-                    const float4 a = __ldcg(agg + f);
-                    __stcg(sin + f, acc[v]);
-                    __stcg(inc + f, make_float4(acc[v].x + a.x, acc[v].y + a.y, acc[v].z + a.z,
-                                                acc[v].w + a.w));
-                }
-            }
-            if (lead)
-                TC_TRACE(jl, 22);
-            __threadfence();
-            named_bar(1, 128);
-            if (lead) {
-                TC_TRACE(jl, 23);
-                st_release(const_cast<unsigned*>(flag_base) + my,
-                           (static_cast<unsigned>(gi + 1) << 2) | 2u);
-                mbar_arrive(&m->sin_ready[jl % NSIN]);
-                TC_TRACE(jl, 12);
-            }
             return true;
         };
         RoundWalker w;
@@ -823,13 +935,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                         TC_TRACE(ai, 10);
                 }
                 if (k == r.nA - 1) {  // segment aggregate complete: publish it
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
-                    __threadfence();
-                    named_bar(1, 128);
-                    if (lead) {
-                        mbar_arrive(&m->phik_stored[j % NPH]);
+                    if (lead)
                         TC_TRACE(j, 15);
-                    }
+                    // the phi(K) tiles of the segment, written with plain stores,
+                    // are read by the tensor-copy engine in phase C
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
                     const int gi = r.tA / p.BH;
                     float* agg =
                         p.slots + (static_cast<size_t>(r.gA.s) * p.R + gi % p.R) * kSlotFloats;
@@ -839,18 +949,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                         __threadfence();
                         st_release(p.flags + static_cast<size_t>(r.gA.s) * p.R + gi % p.R,
                                    (static_cast<unsigned>(gi + 1) << 2) | 1u);
-                    }
-                    if (kLag == 1) {  // S_in is needed in the next round
-                        if (!(ok = lookback(j, r.tA)))
-                            break;
+                        mbar_arrive(&m->phik_stored[j % NPH]);
+                        mbar_arrive(&m->agg_ready[j % NSIN]);
+                        TC_TRACE(j, 24);
                     }
                 }
             }
-            // with a longer lag, the look-back runs one segment behind, when
-            // the predecessors have mostly published their inclusive prefixes
-            if (kLag > 1 && ok && prev_t >= 0 && !(ok = lookback(j - 1, prev_t)))
-                break;
-            prev_t = r.nA ? r.tA : -1;
         }
         if (issued && *abort) {
             mma_commit_w(&m->drain[0], issue);
@@ -859,8 +963,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
     } else if (warp >= 8) {
         // ------------------- phase C (warpgroups of warps 8-11 and 12-15) ---
         // Warpgroup wg takes every other chunk ci (ci & 1 == wg) and runs it
-        // through: S_prev, phi(Q), scores, P, [num | den], epilogue.  Its
-        // first warp issues the MMAs.
+        // through: phi(Q), scores, P, [num | den], epilogue; the S_prev
+        // operand arrives with phi(K).  Its first warp issues the MMAs.
         const int wg = (warp - 8) >> 2;
         const int tc = tid - 256 - 128 * wg;   // row of the chunk = tensor-memory lane
         const int wq = tc >> 5;                // 32-row block
@@ -887,79 +991,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
             const int mine = ci0 < ci + r.nC ? (ci + r.nC - ci0 + 1) / 2 : 0;
             for (int e = 0; e < mine && ok; ++e, ++u) {
                 const int c = ci0 + 2 * e, k = c - ci;
-                // S_prev = S_in + the segment's prefix before chunk k, as
-                // [S_prev^T; z_prev] hi/lo (free: this group's previous chunk
-                // is done with it)
-                if (!group_ok(!lead || e > 0 ||
-                                  (bwait(&m->sin_ready[jc % NSIN], (jc / NSIN) & 1, abort) &&
-                                   bwait(&m->phik_stored[jc % NPH], (jc / NPH) & 1, abort)),
-                              barid, 128)) {
-                    ok = false;
-                    break;
-                }
                 if (lead)
                     TC_TRACE(c, 13);
-                {
-                    // 65 rows x 8 chunks of 8 floats: item tc + 128 v is row
-                    // (item >> 3), chunk (item & 7); every load issued first
-                    const float* s_in =
-                        p.sin_scratch +
-                        (static_cast<size_t>(blockIdx.x) * NSIN + jc % NSIN) * kStateFloats;
-                    const float* s_pf = snap_ptr(jc, max(k - 1, 0));
-                    unsigned char* sShi = cw + CW_S;
-                    unsigned char* sSlo = sShi + kSBytes;
-                    // rows 65..79 of the hi part were output staging: zero again
-                    if (tc < 15 * 8)
-                        *reinterpret_cast<uint4*>(sShi + (65 + (tc >> 3)) * 128 + (tc & 7) * 16) =
-                            make_uint4(0, 0, 0, 0);
-                    constexpr int NU = 4;
-                    const int nu = NU + (tc < 8 ? 1 : 0);  // 520 items = 4 x 128 + 8
-                    float4 x[NU + 1][2], y[NU + 1][2];
-#pragma unroll
-                    for (int v = 0; v <= NU; ++v) {
-                        if (v < nu) {
-                            const float4* a4 =
-                                reinterpret_cast<const float4*>(s_in + 8 * (tc + 128 * v));
-                            x[v][0] = __ldcg(a4), x[v][1] = __ldcg(a4 + 1);
-                            if (k >= 1) {
-                                const float4* b4 =
-                                    reinterpret_cast<const float4*>(s_pf + 8 * (tc + 128 * v));
-                                y[v][0] = __ldcg(b4), y[v][1] = __ldcg(b4 + 1);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int v = 0; v <= NU; ++v) {
-                        if (v < nu) {
-                            const int item = tc + 128 * v, row = item >> 3, cc = item & 7;
-                            float4 x0 = x[v][0], x1 = x[v][1];
-                            if (k >= 1) {
-                                x0.x += y[v][0].x, x0.y += y[v][0].y, x0.z += y[v][0].z,
-                                    x0.w += y[v][0].w;
-                                x1.x += y[v][1].x, x1.y += y[v][1].y, x1.z += y[v][1].z,
-                                    x1.w += y[v][1].w;
-                            }
-                            uint4 h, l;
-                            split2(x0.x, x0.y, h.x, l.x);
-                            split2(x0.z, x0.w, h.y, l.y);
-                            split2(x1.x, x1.y, h.z, l.z);
-                            split2(x1.z, x1.w, h.w, l.w);
-                            *reinterpret_cast<uint4*>(sShi + sw128_off(row, cc)) = h;
-                            *reinterpret_cast<uint4*>(sSlo + sw128_off(row, cc)) = l;
-                        }
-                    }
-                }
+                // rows 65..79 of the S_prev operand's hi part were output
+                // staging: zero again (rows 0..64 come with phi(K))
+                if (tc < 15 * 8)
+                    *reinterpret_cast<uint4*>(cw + CW_S + (65 + (tc >> 3)) * 128 + (tc & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
                 // Q and V of chunk c
                 if (!group_ok(!lead || bwait(&m->qv_full[wg], u & 1, abort), barid, 128)) {
                     ok = false;
                     break;
-                }
-                if (k >= 1) {  // every thread has read the snapshot before chunk k
-                    const unsigned char* sp =
-                        reinterpret_cast<const unsigned char*>(snap_ptr(jc, k - 1));
-                    l2_discard(sp + 128 * tc);
-                    if (tc < (kStateFloats * 4) / 128 - 128)
-                        l2_discard(sp + 128 * (128 + tc));
                 }
                 if (lead)
                     TC_TRACE(c, 14);
@@ -1079,6 +1121,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 if (lead) {
                     mbar_arrive(&m->qv_free[wg]);  // Q and V slots free for the next chunk
                     TC_TRACE(c, 7);
+                }
+                {  // the chunk's S_prev operand image has been used
+                    const unsigned char* img =
+                        p.sprime +
+                        ((static_cast<size_t>(blockIdx.x) * NSIN + jc % NSIN) * p.L + k) * kImgBytes;
+                    if (tc < static_cast<int>(kImgBytes / 128))
+                        l2_discard(img + 128 * tc);
+                    if (tc + 128 < static_cast<int>(kImgBytes / 128))
+                        l2_discard(img + 128 * (tc + 128));
                 }
                 // epilogue: o = num / den into the staging area (the phi(K) and S
                 // slots, free now), then two TMA stores of 32 columns
@@ -1230,7 +1281,8 @@ TcGeom tc_geom(int64_t BH, int64_t N, int sms)
     g.flags_off = 256;
     g.slots_off = (g.flags_off + sizeof(unsigned) * (size_t)BH * g.R + 255) & ~(size_t)255;
     g.sin_off = g.slots_off + sizeof(float) * (size_t)BH * g.R * kSlotFloats;
-    g.phi_off = (g.sin_off + sizeof(float) * (size_t)G * NSIN * kStateFloats + 1023) & ~(size_t)1023;
+    g.sin_off = (g.sin_off + 1023) & ~(size_t)1023;
+    g.phi_off = (g.sin_off + (size_t)G * NSIN * g.L * kImgBytes + 1023) & ~(size_t)1023;
     g.snap_off = g.phi_off + (size_t)G * NPH * g.L * kC * kD * 2;
     g.bytes = g.snap_off + sizeof(float) * (size_t)G * NPH * (g.L - 1) * kStateFloats;
     return g;
@@ -1277,7 +1329,7 @@ cudaError_t tc_forward(const FwdArgs& a)
     p.counter = reinterpret_cast<unsigned*>(ws);
     p.flags = reinterpret_cast<unsigned*>(ws + g.flags_off);
     p.slots = reinterpret_cast<float*>(ws + g.slots_off);
-    p.sin_scratch = reinterpret_cast<float*>(ws + g.sin_off);
+    p.sprime = ws + g.sin_off;
     p.phi_scratch = ws + g.phi_off;
     p.snap = reinterpret_cast<float*>(ws + g.snap_off);
     p.out = static_cast<float*>(a.out);
