@@ -97,7 +97,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s for any single wait
 constexpr int kON = 80;                                // output accumulator: num (64), den, pad
 constexpr uint32_t kSBytes = kON * 128;                // [S_prev^T; z_prev] bf16, 80 x 64
 constexpr int NA = 2;                                  // phase-A K,V stages
-// per output warpgroup: Q, V, phi(K), S hi/lo (phi(K) and S later the fp32 output staging)
+// per output warpgroup: Q, V, phi(K), [S_prev^T; z_prev] hi/lo
 constexpr uint32_t CW_Q = 0, CW_V = 16384, CW_K = 32768, CW_S = 49152;
 constexpr uint32_t kCWBytes = CW_S + 2 * kSBytes;
 constexpr uint32_t OFF_CW = 0;                         // 2 x kCWBytes
@@ -106,6 +106,9 @@ constexpr uint32_t OFF_MISC = OFF_A + NA * 32768;
 constexpr uint32_t kMiscBytes = 2048;
 constexpr uint32_t OFF_ONES = OFF_MISC + kMiscBytes;   // 2 KiB: the e rows of [V | e]
 constexpr int kMaxL = 8;       // largest segment (chunks)
+#ifndef LA_TC_SEG_DIV
+#define LA_TC_SEG_DIV 12       // segments per CTA the segment length aims at
+#endif
 constexpr int NPH = 4;         // phi(K) scratch and snapshot ring depth, in segments
 constexpr uint32_t SMEM_BYTES = OFF_ONES + 2048 + 1024;  // + alignment slack
 static_assert(OFF_ONES % 1024 == 0 && kCWBytes % 1024 == 0 && kSBytes % 1024 == 0 &&
@@ -119,7 +122,7 @@ constexpr uint32_t TM_O = 256;     // 2 x 80: [num | den] accumulators
 constexpr uint32_t TM_DSEG = 448;  // segment aggregate so far [dS^T; dz] (lanes 0..64)
 
 struct TcParams {
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     CUtensorMap mphi;  // phi(K) scratch: per CTA NPH x L tiles of 128 x 64 bf16
     int64_t N;
     int BH;
@@ -265,16 +268,6 @@ __device__ __forceinline__ float2 sub2(float2 a, float2 b)
     return r;
 }
 
-__device__ __forceinline__ float2 add2(float2 a, float2 b)
-{
-    float2 r;
-    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
-        "add.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return r;
-}
-
 // split two fp32 into packed bf16 hi and lo parts (hi + lo = x to ~2^-17)
 __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo)
 {
@@ -301,21 +294,24 @@ __device__ __forceinline__ float ex2(float t)
 }
 
 // elu(x)+1 on two packed bf16: max(x,0) + exp(min(x,0)), with
-// exp(u) = 2^(u log2 e) on the hardware base-2 exponential; the fp32 result is
-// rounded once to bf16.
+// exp(u) = 2^(u log2 e) on the hardware base-2 exponential.  For every
+// element one of the two terms is exactly 0 or 1, so the packed bf16 sum of
+// max(x,0) and the rounded exponential is the fp32 value rounded once.
 __device__ __forceinline__ uint32_t phi2(uint32_t w)
 {
-    const float a = bf_lo(w), b = bf_hi(w);
-    const float2 t = mul2(make_float2(fminf(a, 0.f), fminf(b, 0.f)),
+    uint32_t mn, mx, r;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(mn) : "r"(w), "r"(0u));
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(mx) : "r"(w), "r"(0u));
+    const float2 t = mul2(make_float2(bf_lo(mn), bf_hi(mn)),
                           make_float2(1.4426950408889634f, 1.4426950408889634f));
-    const float2 r = add2(make_float2(fmaxf(a, 0.f), fmaxf(b, 0.f)), make_float2(ex2(t.x), ex2(t.y)));
-    return pack_bf16x2(r.x, r.y);
+    const uint32_t e = pack_bf16x2(ex2(t.x), ex2(t.y));
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(mx), "r"(e));
+    return r;
 }
 
 // Feature map in place on a 128 x 64 bf16 tile (128-byte swizzle) by 128
-// threads; rows >= valid become zero.  With gdst, the result is also written
-// to global memory as a plain row-major 128 x 64 tile.
-__device__ __forceinline__ void phi_tile(unsigned char* tile, int t, int valid, bool elu, uint4* gdst)
+// threads; rows >= valid become zero.
+__device__ __forceinline__ void phi_tile(unsigned char* tile, int t, int valid, bool elu)
 {
     const int cc = t & 7, r0 = t >> 3;
 #pragma unroll 2
@@ -333,8 +329,6 @@ __device__ __forceinline__ void phi_tile(unsigned char* tile, int t, int valid, 
                 x[u] = make_uint4(phi2(x[u].x), phi2(x[u].y), phi2(x[u].z), phi2(x[u].w));
             if (r >= valid || elu)
                 *reinterpret_cast<uint4*>(tile + sw128_off(r, cc)) = x[u];
-            if (gdst)
-                gdst[r * 8 + cc] = x[u];
         }
     }
 }
@@ -462,13 +456,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
             mbar_init(&m->seg_empty[i], 2);
         for (int i = 0; i < NSIN; ++i)
             mbar_init(&m->sin_free[i], 2);
+        // a phase-A stage is free once its MMA is done and its phi(K) tile
+        // has been copied out
+        for (int i = 0; i < NA; ++i)
+            mbar_init(&m->a_empty[i], 2);
         m->abort = 0;
         m->trace_done = 0;
         fence_mbar_init();
         tma_prefetch_desc(&p.mq);
         tma_prefetch_desc(&p.mk);
         tma_prefetch_desc(&p.mv);
-        tma_prefetch_desc(&p.mo);
         tma_prefetch_desc(&p.mphi);
     }
     // the e block of [V | e]: element 0 of each of its 16 rows is 1, the rest 0
@@ -514,9 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
         // Three load streams, each advanced as soon as its next step is free:
         // the tickets with the phase-A K,V stages, and the phase-C loads of
         // each output warpgroup.  Chunk ci of phase C goes to warpgroup
-        // ci & 1: Q and V once that group's previous chunk is done with them,
-        // phi(K) once its previous output tile has left the staging area and,
-        // for a segment's first chunk, once phase A has released the tiles.
+        // ci & 1: Q and V, then phi(K) with the chunk's S_prev operand image,
+        // once that group's previous chunk is done with its slots and the
+        // segment's tiles and images are out.
         if (lane == 0) {
             const uint64_t keep = policy_evict_last();
             const uint64_t stream = policy_evict_first();
@@ -854,8 +851,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
             asm volatile("fence.proxy.async.global;" ::: "memory");
             __threadfence();
             named_bar(barLB, kLB);
-            if (lead)
+            if (lead) {
                 mbar_arrive(&m->sp_ready[j % NSIN]);
+                TC_TRACE(j, 27);
+            }
             // every thread has read the snapshots: drop them from L2
             for (int k = 1; k < r.nA; ++k) {
                 const unsigned char* sb = reinterpret_cast<const unsigned char*>(snap_ptr(j, k - 1));
@@ -865,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
         }
     } else if (warp >= 4 && warp < 8) {
         // -------------------------- phase A (warpgroup of warps 4-7) --------
-        // phi(K) in place and to the scratch ring; the segment's running
+        // phi(K) in place, copied to the scratch ring; the segment's running
         // [dS^T; dz] on the tensor cores (warp 4 issues), read out after every
         // chunk as a prefix snapshot, the last as the segment aggregate, which
         // is published for the look-back warps and the other segments.
@@ -873,7 +872,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
         const bool lead = tb == 0;
         const uint32_t issue = wb == 0 ? elect_one() : 0u;
         const uint32_t a0 = smem_addr(sm + OFF_A);
-        int ai = 0;
+        const uint64_t keep = policy_evict_last();
+        int ai = 0, pend_s = -1;
         bool ok = true, issued = false;
         // [dS^T; dz] so far (tensor-memory lanes 0..64) copied to dst
         auto readout = [&](int x, float* dst) -> bool {
@@ -914,16 +914,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 unsigned char* ktile = sm + OFF_A + s * 32768 + 16384;
                 if (lead)
                     TC_TRACE(ai, 9);
-                // phi(K) is kept for phase C in the scratch (plain stores, fenced
-                // before the TMA loads of phase C read it)
-                phi_tile(ktile, tb, chunk_valid(p, r.gA.c0 + k), elu,
-                         reinterpret_cast<uint4*>(p.phi_scratch) +
-                             static_cast<size_t>(phi_index(j, k)) * (kC * kD * 2 / 16));
+                phi_tile(ktile, tb, chunk_valid(p, r.gA.c0 + k), elu);
                 fence_proxy_async_smem();
                 named_bar(1, 128);
+                if (lead) {
+                    // phi(K) is kept for phase C in the scratch; the stage of the
+                    // previous tile is released once its copy has read it
+                    tma_store_3d(&p.mphi, ktile, 0, 0, phi_index(j, k), keep);
+                    bulk_commit();
+                    if (pend_s >= 0) {
+                        bulk_wait_read<1>();
+                        mbar_arrive(&m->a_empty[pend_s]);
+                    }
+                    pend_s = s;
+                    TC_TRACE(ai, 25);
+                }
                 // the state before chunk k of the segment, for phase C
                 if (k >= 1 && !(ok = readout(ai - 1, snap_ptr(j, k - 1))))
                     break;
+                if (lead)
+                    TC_TRACE(ai, 26);
                 if (wb == 0) {
                     tc_fence_after();
                     state_mma(tm + TM_DSEG, a0 + s * 32768, a0 + s * 32768 + 16384, ones, k > 0,
@@ -937,9 +947,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 if (k == r.nA - 1) {  // segment aggregate complete: publish it
                     if (lead)
                         TC_TRACE(j, 15);
-                    // the phi(K) tiles of the segment, written with plain stores,
-                    // are read by the tensor-copy engine in phase C
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
                     const int gi = r.tA / p.BH;
                     float* agg =
                         p.slots + (static_cast<size_t>(r.gA.s) * p.R + gi % p.R) * kSlotFloats;
@@ -949,6 +956,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                         __threadfence();
                         st_release(p.flags + static_cast<size_t>(r.gA.s) * p.R + gi % p.R,
                                    (static_cast<unsigned>(gi + 1) << 2) | 1u);
+                        // the segment's phi(K) tiles are all in the scratch
+                        bulk_wait<0>();
+                        mbar_arrive(&m->a_empty[pend_s]);
+                        pend_s = -1;
                         mbar_arrive(&m->phik_stored[j % NPH]);
                         mbar_arrive(&m->agg_ready[j % NSIN]);
                         TC_TRACE(j, 24);
@@ -956,6 +967,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 }
             }
         }
+        if (lead)  // no copy may still read a stage
+            bulk_wait<0>();
         if (issued && *abort) {
             mma_commit_w(&m->drain[0], issue);
             drain_wait(&m->drain[0], 0);
@@ -973,7 +986,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
         const uint32_t issue = wq == 0 ? elect_one() : 0u;
         unsigned char* cw = sm + OFF_CW + wg * kCWBytes;
         const uint32_t cwa = smem_addr(cw);
-        const uint64_t pol = policy_evict_first();
         const uint32_t id_sc = idesc_bf16_f32(128, 128, false, false);
         const uint32_t id_pv = idesc_bf16_f32(128, kON, false, true);
         const uint32_t id_in = idesc_bf16_f32(128, kON, false, false);
@@ -993,11 +1005,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 const int c = ci0 + 2 * e, k = c - ci;
                 if (lead)
                     TC_TRACE(c, 13);
-                // rows 65..79 of the S_prev operand's hi part were output
-                // staging: zero again (rows 0..64 come with phi(K))
-                if (tc < 15 * 8)
-                    *reinterpret_cast<uint4*>(cw + CW_S + (65 + (tc >> 3)) * 128 + (tc & 7) * 16) =
-                        make_uint4(0, 0, 0, 0);
                 // Q and V of chunk c
                 if (!group_ok(!lead || bwait(&m->qv_full[wg], u & 1, abort), barid, 128)) {
                     ok = false;
@@ -1005,13 +1012,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 }
                 if (lead)
                     TC_TRACE(c, 14);
-                phi_tile(cw + CW_Q, tc, chunk_valid(p, r.gC.c0 + k), elu, nullptr);
+                phi_tile(cw + CW_Q, tc, chunk_valid(p, r.gC.c0 + k), elu);
                 fence_proxy_async_smem();
                 named_bar(barid, 128);
                 if (lead)
                     TC_TRACE(c, 1);
                 // scores into this group's score buffer, once phi(K) is in
                 if (wq == 0 && __all_sync(full, bwait(&m->k_full[wg], u & 1, abort))) {
+                    if (lead)
+                        TC_TRACE(c, 28);
                     tc_fence_after();
                     const uint64_t dq = sdesc_sw128(cwa + CW_Q, 16, 1024);
                     const uint64_t dk = sdesc_sw128(cwa + CW_K, 16, 1024);
@@ -1118,8 +1127,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     break;
                 }
                 tc_fence_after();
-                if (lead) {
-                    mbar_arrive(&m->qv_free[wg]);  // Q and V slots free for the next chunk
+                if (lead) {  // every slot is free for the next chunk
+                    mbar_arrive(&m->qv_free[wg]);
+                    mbar_arrive(&m->k_free[wg]);
                     TC_TRACE(c, 7);
                 }
                 {  // the chunk's S_prev operand image has been used
@@ -1131,50 +1141,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     if (tc + 128 < static_cast<int>(kImgBytes / 128))
                         l2_discard(img + 128 * (tc + 128));
                 }
-                // epilogue: o = num / den into the staging area (the phi(K) and S
-                // slots, free now), then two TMA stores of 32 columns
+                // epilogue: o = num / den straight from registers.  A 16x256b
+                // tensor-memory load gives each quad of threads 8 consecutive
+                // columns of one row, so every store fills whole 32-byte sectors;
+                // each row's 1/den comes from the thread that owns the row.
                 {
-                    const uint32_t o = to + lane_off;
-                    uint32_t rr[4][16];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        tmem_ld16(o + 16 * q, rr[q]);
-                    const uint32_t dn = tmem_ld1(o + kD);
+                    const float dn = __uint_as_float(tmem_ld1(to + lane_off + kD));
                     tmem_ld_wait();
-                    const float inv = norm ? 1.0f / fmaxf(__uint_as_float(dn), FLT_MIN) : 1.0f;
-                    unsigned char* sO = cw + CW_K;  // columns 32..63 land in the S slot
+                    const float inv_row = norm ? 1.0f / fmaxf(dn, FLT_MIN) : 1.0f;
+                    const int valid = chunk_valid(p, r.gC.c0 + k);
+                    float* obase = p.out + (static_cast<size_t>(r.gC.s) * p.N +
+                                            static_cast<size_t>(r.gC.c0 + k) * kC) *
+                                               kD;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t rr[32];
+                        tmem_ld16x256b_x8(to + lane_off + (static_cast<uint32_t>(16 * h) << 16), rr);
+                        tmem_ld_wait();
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const int col4 = 4 * q + v;
-                            const float2 a = mul2(make_float2(__uint_as_float(rr[q][4 * v]),
-                                                              __uint_as_float(rr[q][4 * v + 1])),
-                                                  make_float2(inv, inv));
-                            const float2 bq = mul2(make_float2(__uint_as_float(rr[q][4 * v + 2]),
-                                                               __uint_as_float(rr[q][4 * v + 3])),
-                                                   make_float2(inv, inv));
-                            *reinterpret_cast<float4*>(sO + (col4 >> 3) * 16384 +
-                                                       sw128_off(tc, col4 & 7)) =
-                                make_float4(a.x, a.y, bq.x, bq.y);
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const int rw = 16 * h + 8 * hr + (lane >> 2);  // row within the warp
+                            const float inv = __shfl_sync(full, inv_row, rw);
+                            const int row = 32 * wq + rw;
+                            if (row < valid) {
+                                float* orow = obase + row * kD + 2 * (lane & 3);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    const float2 x = mul2(
+                                        make_float2(__uint_as_float(rr[4 * i + 2 * hr]),
+                                                    __uint_as_float(rr[4 * i + 2 * hr + 1])),
+                                        make_float2(inv, inv));
+                                    __stcs(reinterpret_cast<float2*>(orow + 8 * i), x);
+                                }
+                            }
                         }
                     }
                 }
                 tc_fence_before();
-                fence_proxy_async_smem();
-                named_bar(barid, 128);
-                if (lead) {
-                    const int row = (r.gC.c0 + k) * kC;
-                    tma_store_3d(&p.mo, cw + CW_K, 0, row, r.gC.s, pol);
-                    tma_store_3d(&p.mo, cw + CW_S, 32, row, r.gC.s, pol);
-                    bulk_commit();
+                if (lead)
                     TC_TRACE(c, 8);
-                    // the tile has left the phi(K) and S slots: the next phi(K)
-                    // may land and S_prev may be rebuilt
-                    bulk_wait_read<0>();
-                    mbar_arrive(&m->k_free[wg]);
-                }
-                named_bar(barid, 128);
             }
             // this group is done with the segment's S_in and ticket slot
             if (ok && lead) {
@@ -1183,12 +1188,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
             }
             ci += r.nC;
         }
-        if (lead) {
-            bulk_wait<0>();
 #ifdef LA_TC_TRACE
+        if (lead)
             atomicAdd(const_cast<int*>(&m->trace_done), 1);
 #endif
-        }
         if (issued && *abort) {
             mma_commit_w(&m->drain[1 + wg], issue);
             drain_wait(&m->drain[1 + wg], 0);
@@ -1266,7 +1269,7 @@ TcGeom tc_geom(int64_t BH, int64_t N, int sms)
     const int64_t chunks = BH * g.nchunk;
     // about a dozen segments per CTA keeps the tail short; long segments make
     // the look-back rare
-    g.L = (int)std::max<int64_t>(1, std::min<int64_t>(kMaxL, chunks / ((int64_t)sms * 12)));
+    g.L = (int)std::max<int64_t>(1, std::min<int64_t>(kMaxL, chunks / ((int64_t)sms * LA_TC_SEG_DIV)));
     g.nseg = (g.nchunk + g.L - 1) / g.L;
     g.total = (int)(BH * g.nseg);
     int G = sms;
@@ -1311,8 +1314,7 @@ cudaError_t tc_forward(const FwdArgs& a)
     memset(&p, 0, sizeof p);
     if (!make_map(&p.mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, a.N, BH, 64) ||
         !make_map(&p.mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, a.N, BH, 64) ||
-        !make_map(&p.mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, a.N, BH, 64) ||
-        !make_map(&p.mo, a.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 64, a.N, BH, 32))
+        !make_map(&p.mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, a.N, BH, 64))
         return cudaErrorInvalidValue;
     unsigned char* ws = static_cast<unsigned char*>(a.ws);
     if (!make_map(&p.mphi, ws + g.phi_off, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, kC,
