@@ -90,7 +90,7 @@ constexpr int kStateFloats = kD * kD + kD;         // S^T (dv x d) then z (d)
 constexpr int kSlotFloats = 2 * kStateFloats;      // aggregate, inclusive
 constexpr int kMaxList = 128;                      // look-back entries
 constexpr uint32_t kImgPart = 65 * 128;            // rows 0..64 of one bf16 part (hi or lo)
-constexpr uint32_t kImgBytes = 2 * kImgPart;       // one S_prev operand image: hi, then lo
+constexpr uint32_t kImgBytes = 2 * kImgPart;       // one state operand image: hi, then lo
 constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s for any single wait
 
 // shared memory (offsets from a 1024-byte aligned base)
@@ -110,8 +110,9 @@ constexpr int kMaxL = 8;       // largest segment (chunks)
 #define LA_TC_SEG_DIV 12       // segments per CTA the segment length aims at
 #endif
 constexpr int NPH = 4;         // phi(K) scratch and snapshot ring depth, in segments
-constexpr uint32_t SMEM_BYTES = OFF_ONES + 2048 + 1024;  // + alignment slack
-static_assert(OFF_ONES % 1024 == 0 && kCWBytes % 1024 == 0 && kSBytes % 1024 == 0 &&
+constexpr uint32_t OFF_SIN = OFF_ONES + 2048;           // [S_in^T; z_in] hi/lo, shared by both groups
+constexpr uint32_t SMEM_BYTES = OFF_SIN + 2 * kSBytes + 1024;  // + alignment slack
+static_assert(OFF_ONES % 1024 == 0 && OFF_SIN % 1024 == 0 && kCWBytes % 1024 == 0 && kSBytes % 1024 == 0 &&
                   CW_S == CW_K + 16384 && CW_S + 16384 <= kCWBytes,
               "layout");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -135,9 +136,9 @@ struct TcParams {
     unsigned* counter;
     unsigned* flags;
     float* slots;
-    unsigned char* sprime;  // per CTA: NSIN x L images of [S_prev^T; z_prev] hi, lo (kImgBytes)
+    unsigned char* sin_img;  // per CTA: NSIN operand images of [S_in^T; z_in] (kImgBytes)
     void* phi_scratch;   // the tiles mphi describes
-    float* snap;         // per CTA: NPH x (L-1) prefix snapshots [S^T; z]
+    unsigned char* snap;  // per CTA: NPH x (L-1) operand images of the prefix snapshots
     float* out;          // [BH][N][64] fp32
     int* status;
 };
@@ -147,7 +148,7 @@ struct Misc {
     uint64_t a_full[NA], a_empty[NA];
     uint64_t qv_full[2], k_full[2], k_free[2], qv_free[2], s_done[2], o_done[2];
     uint64_t phik_stored[NPH], dseg_done, sin_ready[NSIN], sin_free[NSIN], agg_ready[NSIN],
-        sp_ready[NSIN];
+        sin_full, sinslot_free;
     uint64_t drain[3];
     uint32_t tmem;
     int abort;
@@ -460,6 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
         // has been copied out
         for (int i = 0; i < NA; ++i)
             mbar_init(&m->a_empty[i], 2);
+        // the shared S_in slot is free once both groups are done with it
+        mbar_init(&m->sinslot_free, 2);
         m->abort = 0;
         m->trace_done = 0;
         fence_mbar_init();
@@ -477,12 +480,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
             w.x = 0x3F80u;  // bf16 1.0 in the low half
         *reinterpret_cast<uint4*>(sm + OFF_ONES + r * 128 + c * 16) = w;
     }
-    // rows 65..79 of the [S_prev^T; z_prev] operands (hi and lo, both
-    // warpgroups) stay zero
-    for (int i = tid; i < 4 * 15 * 8; i += kThreads) {
+    // rows 65..79 of the state operands (hi and lo of both groups' prefix
+    // slots and of the shared S_in slot) stay zero
+    for (int i = tid; i < 6 * 15 * 8; i += kThreads) {
         const int t = i / 120, rr = 65 + (i % 120) / 8, c = i % 8;
-        *reinterpret_cast<uint4*>(sm + OFF_CW + (t >> 1) * kCWBytes + CW_S + (t & 1) * kSBytes +
-                                  rr * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+        unsigned char* base = t < 4 ? sm + OFF_CW + (t >> 1) * kCWBytes + CW_S : sm + OFF_SIN;
+        *reinterpret_cast<uint4*>(base + (t & 1) * kSBytes + rr * 128 + c * 16) =
+            make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();
     if (warp == 0) {
@@ -499,18 +503,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
     auto phi_index = [&](int jj, int k) {
         return (static_cast<int>(blockIdx.x) * NPH + jj % NPH) * p.L + k;
     };
-    // prefix snapshot [S^T; z] after chunk k of local segment jj
-    auto snap_ptr = [&](int jj, int k) {
+    // operand image of the prefix [S^T; z] after chunk k of local segment jj
+    auto snap_img = [&](int jj, int k) {
         return p.snap +
                (static_cast<size_t>((static_cast<int>(blockIdx.x) * NPH + jj % NPH) * Ls + k)) *
-                   kStateFloats;
+                   kImgBytes;
+    };
+    // operand image of S_in of local segment jj
+    auto sin_img = [&](int jj) {
+        return p.sin_img + (static_cast<size_t>(blockIdx.x) * NSIN + jj % NSIN) * kImgBytes;
     };
 
     if (warp == 0) {
         // ------------------------------------------ producer (one thread) --
-        // Three load streams, each advanced as soon as its next step is free:
-        // the tickets with the phase-A K,V stages, and the phase-C loads of
-        // each output warpgroup.  Chunk ci of phase C goes to warpgroup
+        // Four load streams, each advanced as soon as its next step is free:
+        // the tickets with the phase-A K,V stages, the phase-C loads of each
+        // output warpgroup, and the S_in images for the shared slot.  Chunk ci of phase C goes to warpgroup
         // ci & 1: Q and V, then phi(K) with the chunk's S_prev operand image,
         // once that group's previous chunk is done with its slots and the
         // segment's tiles and images are out.
@@ -529,9 +537,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 bool seg = false, kphase = false, done = false;
                 Seg g{};
             } cs[2];
+            // S_in image of local segment js into the shared slot, once its
+            // look-back is done and both groups are done with the previous one
+            int js = 0, sin_last = -1;
+            bool sin_done = false;
             uint64_t idle_since = 0;
-            while (!(a_done && cs[0].done && cs[1].done)) {
+            while (!(a_done && cs[0].done && cs[1].done && sin_done)) {
                 bool prog = false;
+                if (!sin_done && js < nt) {
+                    if (m->seg_ticket[js % NS] >= p.total) {
+                        sin_done = true;
+                        prog = true;
+                    } else if (mbar_test_wait(&m->sin_ready[js % NSIN], (js / NSIN) & 1) &&
+                               (js == 0 || mbar_test_wait(&m->sinslot_free, (js - 1) & 1))) {
+                        const unsigned char* img = sin_img(js);
+                        mbar_arrive_expect_tx(&m->sin_full, kImgBytes);
+                        bulk_load(sm + OFF_SIN, img, kImgPart, &m->sin_full, stream);
+                        bulk_load(sm + OFF_SIN + kSBytes, img + kImgPart, kImgPart, &m->sin_full,
+                                  stream);
+                        sin_last = js++;
+                        prog = true;
+                    }
+                }
                 if (!a_done) {
                     if (!a_seg) {
                         const int ss = ja % NS;
@@ -609,19 +636,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     if (c.kphase &&
                         (c.e > 0 ||
                          mbar_test_wait(&m->phik_stored[c.jc % NPH], (c.jc / NPH) & 1)) &&
-                        mbar_test_wait(kk == 0 ? &m->sin_ready[c.jc % NSIN] : &m->sp_ready[c.jc % NSIN],
-                                       (c.jc / NSIN) & 1) &&
                         (c.u == 0 || mbar_test_wait(&m->k_free[wg], (c.u - 1) & 1))) {
-                        mbar_arrive_expect_tx(&m->k_full[wg], kC * kD * 2 + kImgBytes);
+                        // phi(K) and, past the segment's first chunk, the image
+                        // of the prefix before it
+                        mbar_arrive_expect_tx(&m->k_full[wg], kC * kD * 2 + (kk ? kImgBytes : 0));
                         tma_load_3d(cw + CW_K, &p.mphi, 0, 0, phi_index(c.jc, kk), &m->k_full[wg],
                                     stream);
-                        const unsigned char* img =
-                            p.sprime +
-                            ((static_cast<size_t>(blockIdx.x) * NSIN + c.jc % NSIN) * p.L + kk) *
-                                kImgBytes;
-                        bulk_load(cw + CW_S, img, kImgPart, &m->k_full[wg], stream);
-                        bulk_load(cw + CW_S + kSBytes, img + kImgPart, kImgPart, &m->k_full[wg],
-                                  stream);
+                        if (kk) {
+                            const unsigned char* img = snap_img(c.jc, kk - 1);
+                            bulk_load(cw + CW_S, img, kImgPart, &m->k_full[wg], stream);
+                            bulk_load(cw + CW_S + kSBytes, img + kImgPart, kImgPart,
+                                      &m->k_full[wg], stream);
+                        }
                         c.k_last = c.u;
                         c.kphase = false;
                         ++c.u;
@@ -659,6 +685,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     if (cs[wg].k_last >= 0)
                         drain_wait(&m->k_full[wg], cs[wg].k_last & 1);
                 }
+                if (sin_last >= 0)
+                    drain_wait(&m->sin_full, sin_last & 1);
             }
         }
     } else if (warp < 4) {
@@ -795,20 +823,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                         acc[v].x += x[v].x, acc[v].y += x[v].y, acc[v].z += x[v].z,
                             acc[v].w += x[v].w;
             }
-            // S_prev operand image k of the segment: S_in plus the prefix
-            // snapshot before chunk k, as bf16 hi and lo parts of rows 0..64 in
-            // the 128-byte swizzled layout of the output groups' operand slot
-            unsigned char* img0 =
-                p.sprime + (static_cast<size_t>(blockIdx.x) * NSIN + j % NSIN) * p.L * kImgBytes;
-            auto put = [&](unsigned char* img, int f, float4 x) {
-                const int row = f >> 4, q = f & 15;
-                uint32_t h0, l0, h1, l1;
-                split2(x.x, x.y, h0, l0);
-                split2(x.z, x.w, h1, l1);
-                const uint32_t off = sw128_off(row, q >> 1) + (q & 1) * 8;
-                __stcg(reinterpret_cast<uint2*>(img + off), make_uint2(h0, h1));
-                __stcg(reinterpret_cast<uint2*>(img + kImgPart + off), make_uint2(l0, l1));
-            };
+            // S_in as the operand image the output groups read: bf16 hi and lo
+            // parts of rows 0..64 in the 128-byte swizzled slot layout
+            unsigned char* img = sin_img(j);
             float4* exc = reinterpret_cast<float4*>(slot_base + static_cast<size_t>(my) * kSlotFloats +
                                                     kStateFloats);
 #pragma unroll
@@ -816,7 +833,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 const int f = tl + kLB * v;
                 if (f < kStateFloats / 4) {
                     __stcg(exc + f, acc[v]);
-                    put(img0, f, acc[v]);
+                    const int row = f >> 4, q = f & 15;
+                    uint32_t h0, l0, h1, l1;
+                    split2(acc[v].x, acc[v].y, h0, l0);
+                    split2(acc[v].z, acc[v].w, h1, l1);
+                    const uint32_t off = sw128_off(row, q >> 1) + (q & 1) * 8;
+                    __stcg(reinterpret_cast<uint2*>(img + off), make_uint2(h0, h1));
+                    __stcg(reinterpret_cast<uint2*>(img + kImgPart + off), make_uint2(l0, l1));
                 }
             }
             if (lead)
@@ -830,44 +853,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 mbar_arrive(&m->sin_ready[j % NSIN]);
                 TC_TRACE(j, 12);
             }
-            // the images of the later chunks, from the snapshots
-            for (int k = 1; k < r.nA; ++k) {
-                const float4* sn4 = reinterpret_cast<const float4*>(snap_ptr(j, k - 1));
-                float4 y[NV];
-#pragma unroll
-                for (int v = 0; v < NV; ++v)
-                    if (tl + kLB * v < kStateFloats / 4)
-                        y[v] = __ldcg(sn4 + tl + kLB * v);
-#pragma unroll
-                for (int v = 0; v < NV; ++v) {
-                    const int f = tl + kLB * v;
-                    if (f < kStateFloats / 4) {
-                        float4 x = acc[v];
-                        x.x += y[v].x, x.y += y[v].y, x.z += y[v].z, x.w += y[v].w;
-                        put(img0 + k * kImgBytes, f, x);
-                    }
-                }
-            }
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            __threadfence();
-            named_bar(barLB, kLB);
-            if (lead) {
-                mbar_arrive(&m->sp_ready[j % NSIN]);
-                TC_TRACE(j, 27);
-            }
-            // every thread has read the snapshots: drop them from L2
-            for (int k = 1; k < r.nA; ++k) {
-                const unsigned char* sb = reinterpret_cast<const unsigned char*>(snap_ptr(j, k - 1));
-                for (int l = tl; l < (kStateFloats * 4) / 128; l += kLB)
-                    l2_discard(sb + 128 * l);
-            }
         }
     } else if (warp >= 4 && warp < 8) {
         // -------------------------- phase A (warpgroup of warps 4-7) --------
         // phi(K) in place, copied to the scratch ring; the segment's running
         // [dS^T; dz] on the tensor cores (warp 4 issues), read out after every
-        // chunk as a prefix snapshot, the last as the segment aggregate, which
-        // is published for the look-back warps and the other segments.
+        // chunk as the operand image of a prefix, the last as the segment
+        // aggregate, which is published for the look-back warps and the other
+        // segments.
         const int tb = tid - 128, wb = warp - 4;
         const bool lead = tb == 0;
         const uint32_t issue = wb == 0 ? elect_one() : 0u;
@@ -875,8 +868,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
         const uint64_t keep = policy_evict_last();
         int ai = 0, pend_s = -1;
         bool ok = true, issued = false;
-        // [dS^T; dz] so far (tensor-memory lanes 0..64) copied to dst
-        auto readout = [&](int x, float* dst) -> bool {
+        // [dS^T; dz] so far (tensor-memory lanes 0..64) copied to dst as fp32,
+        // or to img as the bf16 hi/lo operand image of the output groups
+        auto readout = [&](int x, float* dst, unsigned char* img) -> bool {
             if (!group_ok(!lead || bwait(&m->dseg_done, x & 1, abort), 1, 128))
                 return false;
             tc_fence_after();
@@ -886,7 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 for (int q = 0; q < 4; ++q)
                     tmem_ld16(tm + TM_DSEG + lane_off + 16 * q, rr[q]);
                 tmem_ld_wait();
-                if (tb <= kD) {
+                if (tb <= kD && dst) {
                     float4* d4 = reinterpret_cast<float4*>(dst + tb * kD);
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
@@ -896,6 +890,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                                                                __uint_as_float(rr[q][4 * u + 1]),
                                                                __uint_as_float(rr[q][4 * u + 2]),
                                                                __uint_as_float(rr[q][4 * u + 3])));
+                } else if (tb <= kD) {
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const uint32_t* x8 = &rr[cc >> 1][(cc & 1) * 8];
+                        uint4 h, l;
+                        split2(__uint_as_float(x8[0]), __uint_as_float(x8[1]), h.x, l.x);
+                        split2(__uint_as_float(x8[2]), __uint_as_float(x8[3]), h.y, l.y);
+                        split2(__uint_as_float(x8[4]), __uint_as_float(x8[5]), h.z, l.z);
+                        split2(__uint_as_float(x8[6]), __uint_as_float(x8[7]), h.w, l.w);
+                        __stcg(reinterpret_cast<uint4*>(img + sw128_off(tb, cc)), h);
+                        __stcg(reinterpret_cast<uint4*>(img + kImgPart + sw128_off(tb, cc)), l);
+                    }
                 }
             }
             tc_fence_before();
@@ -930,7 +936,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     TC_TRACE(ai, 25);
                 }
                 // the state before chunk k of the segment, for phase C
-                if (k >= 1 && !(ok = readout(ai - 1, snap_ptr(j, k - 1))))
+                if (k >= 1 && !(ok = readout(ai - 1, nullptr, snap_img(j, k - 1))))
                     break;
                 if (lead)
                     TC_TRACE(ai, 26);
@@ -947,10 +953,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 if (k == r.nA - 1) {  // segment aggregate complete: publish it
                     if (lead)
                         TC_TRACE(j, 15);
+                    // the segment's prefix images, written with plain stores, are
+                    // read by the tensor-copy engine in phase C
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
                     const int gi = r.tA / p.BH;
                     float* agg =
                         p.slots + (static_cast<size_t>(r.gA.s) * p.R + gi % p.R) * kSlotFloats;
-                    if (!(ok = readout(ai, agg)))
+                    if (!(ok = readout(ai, agg, nullptr)))
                         break;
                     if (lead) {
                         __threadfence();
@@ -1001,6 +1010,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
             // this group's chunks of the segment: ci0, ci0 + 2, ...
             const int ci0 = ci + ((ci & 1) != wg ? 1 : 0);
             const int mine = ci0 < ci + r.nC ? (ci + r.nC - ci0 + 1) / 2 : 0;
+            if (mine == 0 && lead && bwait(&m->sin_full, jc & 1, abort))
+                mbar_arrive(&m->sinslot_free);  // no chunk here: done with the slot
             for (int e = 0; e < mine && ok; ++e, ++u) {
                 const int c = ci0 + 2 * e, k = c - ci;
                 if (lead)
@@ -1017,8 +1028,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 named_bar(barid, 128);
                 if (lead)
                     TC_TRACE(c, 1);
-                // scores into this group's score buffer, once phi(K) is in
-                if (wq == 0 && __all_sync(full, bwait(&m->k_full[wg], u & 1, abort))) {
+                // scores into this group's score buffer, once phi(K) and the
+                // segment's S_in are in
+                if (wq == 0 && __all_sync(full, bwait(&m->k_full[wg], u & 1, abort) &&
+                                                    bwait(&m->sin_full, jc & 1, abort))) {
                     if (lead)
                         TC_TRACE(c, 28);
                     tc_fence_after();
@@ -1028,16 +1041,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     for (int kk = 0; kk < 4; ++kk)
                         mma_bf16_ss_w(tp, dq + 2 * kk, dk + 2 * kk, id_sc, kk > 0, issue);
                     mma_commit_w(&m->s_done[wg], issue);
-                    // phi(Q) [S_prev^T; z_prev] (hi, lo) starts the output
-                    // accumulator while P is prepared
-                    const uint64_t ds = sdesc_sw128(cwa + CW_S, 16, 1024);
+                    // phi(Q) [S_in^T; z_in] (hi, lo) starts the output
+                    // accumulator while P is prepared; past the segment's first
+                    // chunk phi(Q) times the prefix before the chunk adds to it
+                    const uint64_t di = sdesc_sw128(smem_addr(sm + OFF_SIN), 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ss_w(to, dq + 2 * kk, ds + 2 * kk, id_in, kk > 0, issue);
+                        mma_bf16_ss_w(to, dq + 2 * kk, di + 2 * kk, id_in, kk > 0, issue);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ss_w(to, dq + 2 * kk, ds + (kSBytes >> 4) + 2 * kk, id_in, 1,
+                        mma_bf16_ss_w(to, dq + 2 * kk, di + (kSBytes >> 4) + 2 * kk, id_in, 1,
                                       issue);
+                    if (e == mine - 1)  // this group's last read of the shared slot
+                        mma_commit_w(&m->sinslot_free, issue);
+                    if (k >= 1) {
+                        const uint64_t ds = sdesc_sw128(cwa + CW_S, 16, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ss_w(to, dq + 2 * kk, ds + 2 * kk, id_in, 1, issue);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ss_w(to, dq + 2 * kk, ds + (kSBytes >> 4) + 2 * kk, id_in, 1,
+                                          issue);
+                    }
                     issued = true;
                     if (lead)
                         TC_TRACE(c, 2);
@@ -1132,10 +1158,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     mbar_arrive(&m->k_free[wg]);
                     TC_TRACE(c, 7);
                 }
-                {  // the chunk's S_prev operand image has been used
-                    const unsigned char* img =
-                        p.sprime +
-                        ((static_cast<size_t>(blockIdx.x) * NSIN + jc % NSIN) * p.L + k) * kImgBytes;
+                if (k >= 1) {  // the image of the prefix before the chunk has been used
+                    const unsigned char* img = snap_img(jc, k - 1);
                     if (tc < static_cast<int>(kImgBytes / 128))
                         l2_discard(img + 128 * tc);
                     if (tc + 128 < static_cast<int>(kImgBytes / 128))
@@ -1285,9 +1309,9 @@ TcGeom tc_geom(int64_t BH, int64_t N, int sms)
     g.slots_off = (g.flags_off + sizeof(unsigned) * (size_t)BH * g.R + 255) & ~(size_t)255;
     g.sin_off = g.slots_off + sizeof(float) * (size_t)BH * g.R * kSlotFloats;
     g.sin_off = (g.sin_off + 1023) & ~(size_t)1023;
-    g.phi_off = (g.sin_off + (size_t)G * NSIN * g.L * kImgBytes + 1023) & ~(size_t)1023;
+    g.phi_off = (g.sin_off + (size_t)G * NSIN * kImgBytes + 1023) & ~(size_t)1023;
     g.snap_off = g.phi_off + (size_t)G * NPH * g.L * kC * kD * 2;
-    g.bytes = g.snap_off + sizeof(float) * (size_t)G * NPH * (g.L - 1) * kStateFloats;
+    g.bytes = g.snap_off + (size_t)G * NPH * (g.L - 1) * kImgBytes;
     return g;
 }
 
@@ -1331,9 +1355,9 @@ cudaError_t tc_forward(const FwdArgs& a)
     p.counter = reinterpret_cast<unsigned*>(ws);
     p.flags = reinterpret_cast<unsigned*>(ws + g.flags_off);
     p.slots = reinterpret_cast<float*>(ws + g.slots_off);
-    p.sprime = ws + g.sin_off;
+    p.sin_img = ws + g.sin_off;
     p.phi_scratch = ws + g.phi_off;
-    p.snap = reinterpret_cast<float*>(ws + g.snap_off);
+    p.snap = ws + g.snap_off;
     p.out = static_cast<float*>(a.out);
     p.status = a.status;
     cudaError_t e = cudaMemsetAsync(ws, 0, g.slots_off, a.stream);
