@@ -110,9 +110,8 @@ constexpr int kMaxL = 8;       // largest segment (chunks)
 #define LA_TC_SEG_DIV 12       // segments per CTA the segment length aims at
 #endif
 constexpr int NPH = 4;         // phi(K) scratch and snapshot ring depth, in segments
-constexpr uint32_t OFF_SIN = OFF_ONES + 2048;           // [S_in^T; z_in] hi/lo, shared by both groups
-constexpr uint32_t SMEM_BYTES = OFF_SIN + 2 * kSBytes + 1024;  // + alignment slack
-static_assert(OFF_ONES % 1024 == 0 && OFF_SIN % 1024 == 0 && kCWBytes % 1024 == 0 && kSBytes % 1024 == 0 &&
+constexpr uint32_t SMEM_BYTES = OFF_ONES + 2048 + 1024;  // + alignment slack
+static_assert(OFF_ONES % 1024 == 0 && kCWBytes % 1024 == 0 && kSBytes % 1024 == 0 &&
                   CW_S == CW_K + 16384 && CW_S + 16384 <= kCWBytes,
               "layout");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -138,7 +137,6 @@ struct TcParams {
     float* slots;
     unsigned char* sin_img;  // per CTA: NSIN operand images of [S_in^T; z_in] (kImgBytes)
     void* phi_scratch;   // the tiles mphi describes
-    unsigned char* snap;  // per CTA: NPH x (L-1) operand images of the prefix snapshots
     float* out;          // [BH][N][64] fp32
     int* status;
 };
@@ -146,9 +144,8 @@ struct TcParams {
 struct Misc {
     uint64_t seg_full[NS], seg_empty[NS];
     uint64_t a_full[NA], a_empty[NA];
-    uint64_t qv_full[2], k_full[2], k_free[2], qv_free[2], s_done[2], o_done[2];
-    uint64_t phik_stored[NPH], dseg_done, sin_ready[NSIN], sin_free[NSIN], agg_ready[NSIN],
-        sin_full, sinslot_free;
+    uint64_t q_full[2], v_full[2], k_full[2], qs_free[2], ds_done[2], s_done[2], o_done[2];
+    uint64_t phik_stored[NPH], dseg_done, sin_ready[NSIN], sin_free[NSIN], agg_ready[NSIN];
     uint64_t drain[3];
     uint32_t tmem;
     int abort;
@@ -444,7 +441,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool norm = p.fm != LA_FM_NONE;
     const bool elu = p.fm == LA_FM_ELU1;
-    const int Ls = max(p.L - 1, 1);  // prefix snapshots per segment
     const unsigned full = 0xffffffffu;
 
     if (tid == 0) {
@@ -452,17 +448,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
         const int nbars = static_cast<int>((reinterpret_cast<uint64_t*>(&m->drain[2]) - bars) + 1);
         for (int i = 0; i < nbars; ++i)
             mbar_init(&bars[i], 1);
-        // both output warpgroups release a ticket slot and an S_in buffer
-        for (int i = 0; i < NS; ++i)
-            mbar_init(&m->seg_empty[i], 2);
-        for (int i = 0; i < NSIN; ++i)
-            mbar_init(&m->sin_free[i], 2);
         // a phase-A stage is free once its MMA is done and its phi(K) tile
         // has been copied out
         for (int i = 0; i < NA; ++i)
             mbar_init(&m->a_empty[i], 2);
-        // the shared S_in slot is free once both groups are done with it
-        mbar_init(&m->sinslot_free, 2);
         m->abort = 0;
         m->trace_done = 0;
         fence_mbar_init();
@@ -480,13 +469,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
             w.x = 0x3F80u;  // bf16 1.0 in the low half
         *reinterpret_cast<uint4*>(sm + OFF_ONES + r * 128 + c * 16) = w;
     }
-    // rows 65..79 of the state operands (hi and lo of both groups' prefix
-    // slots and of the shared S_in slot) stay zero
-    for (int i = tid; i < 6 * 15 * 8; i += kThreads) {
+    // rows 65..79 of both groups' [S_prev^T; z_prev] operands (hi and lo)
+    // stay zero
+    for (int i = tid; i < 4 * 15 * 8; i += kThreads) {
         const int t = i / 120, rr = 65 + (i % 120) / 8, c = i % 8;
-        unsigned char* base = t < 4 ? sm + OFF_CW + (t >> 1) * kCWBytes + CW_S : sm + OFF_SIN;
-        *reinterpret_cast<uint4*>(base + (t & 1) * kSBytes + rr * 128 + c * 16) =
-            make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sm + OFF_CW + (t >> 1) * kCWBytes + CW_S + (t & 1) * kSBytes +
+                                  rr * 128 + c * 16) = make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();
     if (warp == 0) {
@@ -503,12 +491,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
     auto phi_index = [&](int jj, int k) {
         return (static_cast<int>(blockIdx.x) * NPH + jj % NPH) * p.L + k;
     };
-    // operand image of the prefix [S^T; z] after chunk k of local segment jj
-    auto snap_img = [&](int jj, int k) {
-        return p.snap +
-               (static_cast<size_t>((static_cast<int>(blockIdx.x) * NPH + jj % NPH) * Ls + k)) *
-                   kImgBytes;
-    };
     // operand image of S_in of local segment jj
     auto sin_img = [&](int jj) {
         return p.sin_img + (static_cast<size_t>(blockIdx.x) * NSIN + jj % NSIN) * kImgBytes;
@@ -516,12 +498,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
 
     if (warp == 0) {
         // ------------------------------------------ producer (one thread) --
-        // Four load streams, each advanced as soon as its next step is free:
-        // the tickets with the phase-A K,V stages, the phase-C loads of each
-        // output warpgroup, and the S_in images for the shared slot.  Chunk ci of phase C goes to warpgroup
-        // ci & 1: Q and V, then phi(K) with the chunk's S_prev operand image,
-        // once that group's previous chunk is done with its slots and the
-        // segment's tiles and images are out.
+        // Three load streams, each advanced as soon as its next step is free:
+        // the tickets with the phase-A K,V stages, and the phase-C loads of
+        // each output warpgroup.  Local segment jc goes to output group jc & 1,
+        // whose chunk loads are: Q once its previous scores and phi(Q)
+        // products are done; phi(K) (with the segment's S_in image for its
+        // first chunk) and V once its previous chunk's last MMA is done and
+        // the segment's phi(K) tiles and S_in are out.
         if (lane == 0) {
             const uint64_t keep = policy_evict_last();
             const uint64_t stream = policy_evict_first();
@@ -532,33 +515,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
             bool a_seg = false, a_done = false;
             Seg ga{};
             struct CStream {
-                int jc = 0, cbase = 0, e = 0, mine = 0, k0 = 0, u = 0;
-                int qv_last = -1, k_last = -1;
-                bool seg = false, kphase = false, done = false;
+                int jc = 0, k = 0, u = 0, step = 0;
+                int q_last = -1, k_last = -1, v_last = -1;
+                bool seg = false, done = false;
                 Seg g{};
             } cs[2];
-            // S_in image of local segment js into the shared slot, once its
-            // look-back is done and both groups are done with the previous one
-            int js = 0, sin_last = -1;
-            bool sin_done = false;
+            cs[1].jc = 1;
             uint64_t idle_since = 0;
-            while (!(a_done && cs[0].done && cs[1].done && sin_done)) {
+            while (!(a_done && cs[0].done && cs[1].done)) {
                 bool prog = false;
-                if (!sin_done && js < nt) {
-                    if (m->seg_ticket[js % NS] >= p.total) {
-                        sin_done = true;
-                        prog = true;
-                    } else if (mbar_test_wait(&m->sin_ready[js % NSIN], (js / NSIN) & 1) &&
-                               (js == 0 || mbar_test_wait(&m->sinslot_free, (js - 1) & 1))) {
-                        const unsigned char* img = sin_img(js);
-                        mbar_arrive_expect_tx(&m->sin_full, kImgBytes);
-                        bulk_load(sm + OFF_SIN, img, kImgPart, &m->sin_full, stream);
-                        bulk_load(sm + OFF_SIN + kSBytes, img + kImgPart, kImgPart, &m->sin_full,
-                                  stream);
-                        sin_last = js++;
-                        prog = true;
-                    }
-                }
                 if (!a_done) {
                     if (!a_seg) {
                         const int ss = ja % NS;
@@ -599,9 +564,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     CStream& c = cs[wg];
                     if (c.done)
                         continue;
-                    if (!c.seg) {  // the next segment, once its ticket is out
-                        if (c.jc >= nt)
+                    if (!c.seg) {  // this group's next segment, once its ticket is out
+                        if (c.jc >= nt) {
+                            if (a_done)  // past the last ticket
+                                c.done = true;
                             continue;
+                        }
                         const int t = m->seg_ticket[c.jc % NS];
                         prog = true;
                         if (t >= p.total) {
@@ -609,53 +577,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                             continue;
                         }
                         c.g = seg_of(p, t);
-                        const int ci0 = c.cbase + ((c.cbase & 1) != wg ? 1 : 0);
-                        c.k0 = ci0 - c.cbase;
-                        c.mine = ci0 < c.cbase + c.g.n ? (c.cbase + c.g.n - ci0 + 1) / 2 : 0;
-                        c.e = 0;
-                        c.seg = c.mine > 0;
-                        if (!c.seg) {
-                            c.cbase += c.g.n;
-                            ++c.jc;
-                            continue;
-                        }
+                        c.k = 0;
+                        c.seg = true;
                     }
                     unsigned char* cw = sm + OFF_CW + wg * kCWBytes;
-                    const int row = (c.g.c0 + c.k0 + 2 * c.e) * kC;
-                    if (!c.kphase &&
-                        (c.u == 0 || mbar_test_wait(&m->qv_free[wg], (c.u - 1) & 1))) {
-                        mbar_arrive_expect_tx(&m->qv_full[wg], 2 * kC * kD * 2);
-                        tma_load_3d(cw + CW_Q, &p.mq, 0, row, c.g.s, &m->qv_full[wg], stream);
-                        tma_load_3d(cw + CW_V, &p.mv, 0, row, c.g.s, &m->qv_full[wg], stream);
-                        c.qv_last = c.u;
-                        c.kphase = true;
+                    const int row = (c.g.c0 + c.k) * kC;
+                    if (c.step == 0 &&
+                        (c.u == 0 || mbar_test_wait(&m->qs_free[wg], (c.u - 1) & 1))) {
+                        mbar_arrive_expect_tx(&m->q_full[wg], kC * kD * 2);
+                        tma_load_3d(cw + CW_Q, &p.mq, 0, row, c.g.s, &m->q_full[wg], stream);
+                        c.q_last = c.u;
+                        c.step = 1;
                         prog = true;
-                        TC_TRACE(c.cbase + c.k0 + 2 * c.e, 0);
                     }
-                    const int kk = c.k0 + 2 * c.e;
-                    if (c.kphase &&
-                        (c.e > 0 ||
-                         mbar_test_wait(&m->phik_stored[c.jc % NPH], (c.jc / NPH) & 1)) &&
-                        (c.u == 0 || mbar_test_wait(&m->k_free[wg], (c.u - 1) & 1))) {
-                        // phi(K) and, past the segment's first chunk, the image
-                        // of the prefix before it
-                        mbar_arrive_expect_tx(&m->k_full[wg], kC * kD * 2 + (kk ? kImgBytes : 0));
-                        tma_load_3d(cw + CW_K, &p.mphi, 0, 0, phi_index(c.jc, kk), &m->k_full[wg],
+                    if (c.step == 1 &&
+                        (c.u == 0 || mbar_test_wait(&m->ds_done[wg], (c.u - 1) & 1)) &&
+                        (c.k > 0 ||
+                         (mbar_test_wait(&m->phik_stored[c.jc % NPH], (c.jc / NPH) & 1) &&
+                          mbar_test_wait(&m->sin_ready[c.jc % NSIN], (c.jc / NSIN) & 1)))) {
+                        mbar_arrive_expect_tx(&m->k_full[wg], kC * kD * 2 + (c.k ? 0 : kImgBytes));
+                        tma_load_3d(cw + CW_K, &p.mphi, 0, 0, phi_index(c.jc, c.k), &m->k_full[wg],
                                     stream);
-                        if (kk) {
-                            const unsigned char* img = snap_img(c.jc, kk - 1);
+                        if (c.k == 0) {  // the segment's S_in starts the running state
+                            const unsigned char* img = sin_img(c.jc);
                             bulk_load(cw + CW_S, img, kImgPart, &m->k_full[wg], stream);
                             bulk_load(cw + CW_S + kSBytes, img + kImgPart, kImgPart,
                                       &m->k_full[wg], stream);
                         }
-                        c.k_last = c.u;
-                        c.kphase = false;
+                        mbar_arrive_expect_tx(&m->v_full[wg], kC * kD * 2);
+                        tma_load_3d(cw + CW_V, &p.mv, 0, row, c.g.s, &m->v_full[wg], stream);
+                        c.k_last = c.v_last = c.u;
+                        c.step = 0;
                         ++c.u;
                         prog = true;
-                        if (++c.e == c.mine) {
+                        if (++c.k == c.g.n) {
                             c.seg = false;
-                            c.cbase += c.g.n;
-                            ++c.jc;
+                            c.jc += 2;
                         }
                     }
                 }
@@ -680,13 +637,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     if (a_last[i] >= 0)
                         drain_wait(&m->a_full[i], a_last[i] & 1);
                 for (int wg = 0; wg < 2; ++wg) {
-                    if (cs[wg].qv_last >= 0)
-                        drain_wait(&m->qv_full[wg], cs[wg].qv_last & 1);
+                    if (cs[wg].q_last >= 0)
+                        drain_wait(&m->q_full[wg], cs[wg].q_last & 1);
                     if (cs[wg].k_last >= 0)
                         drain_wait(&m->k_full[wg], cs[wg].k_last & 1);
+                    if (cs[wg].v_last >= 0)
+                        drain_wait(&m->v_full[wg], cs[wg].v_last & 1);
                 }
-                if (sin_last >= 0)
-                    drain_wait(&m->sin_full, sin_last & 1);
             }
         }
     } else if (warp < 4) {
@@ -857,10 +814,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
     } else if (warp >= 4 && warp < 8) {
         // -------------------------- phase A (warpgroup of warps 4-7) --------
         // phi(K) in place, copied to the scratch ring; the segment's running
-        // [dS^T; dz] on the tensor cores (warp 4 issues), read out after every
-        // chunk as the operand image of a prefix, the last as the segment
-        // aggregate, which is published for the look-back warps and the other
-        // segments.
+        // [dS^T; dz] on the tensor cores (warp 4 issues), read out at the end
+        // of the segment as its aggregate, which is published for the
+        // look-back warps and the other segments.
         const int tb = tid - 128, wb = warp - 4;
         const bool lead = tb == 0;
         const uint32_t issue = wb == 0 ? elect_one() : 0u;
@@ -868,9 +824,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
         const uint64_t keep = policy_evict_last();
         int ai = 0, pend_s = -1;
         bool ok = true, issued = false;
-        // [dS^T; dz] so far (tensor-memory lanes 0..64) copied to dst as fp32,
-        // or to img as the bf16 hi/lo operand image of the output groups
-        auto readout = [&](int x, float* dst, unsigned char* img) -> bool {
+        // [dS^T; dz] so far (tensor-memory lanes 0..64) copied to dst
+        auto readout = [&](int x, float* dst) -> bool {
             if (!group_ok(!lead || bwait(&m->dseg_done, x & 1, abort), 1, 128))
                 return false;
             tc_fence_after();
@@ -880,7 +835,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 for (int q = 0; q < 4; ++q)
                     tmem_ld16(tm + TM_DSEG + lane_off + 16 * q, rr[q]);
                 tmem_ld_wait();
-                if (tb <= kD && dst) {
+                if (tb <= kD) {
                     float4* d4 = reinterpret_cast<float4*>(dst + tb * kD);
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
@@ -890,18 +845,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                                                                __uint_as_float(rr[q][4 * u + 1]),
                                                                __uint_as_float(rr[q][4 * u + 2]),
                                                                __uint_as_float(rr[q][4 * u + 3])));
-                } else if (tb <= kD) {
-#pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        const uint32_t* x8 = &rr[cc >> 1][(cc & 1) * 8];
-                        uint4 h, l;
-                        split2(__uint_as_float(x8[0]), __uint_as_float(x8[1]), h.x, l.x);
-                        split2(__uint_as_float(x8[2]), __uint_as_float(x8[3]), h.y, l.y);
-                        split2(__uint_as_float(x8[4]), __uint_as_float(x8[5]), h.z, l.z);
-                        split2(__uint_as_float(x8[6]), __uint_as_float(x8[7]), h.w, l.w);
-                        __stcg(reinterpret_cast<uint4*>(img + sw128_off(tb, cc)), h);
-                        __stcg(reinterpret_cast<uint4*>(img + kImgPart + sw128_off(tb, cc)), l);
-                    }
                 }
             }
             tc_fence_before();
@@ -935,11 +878,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     pend_s = s;
                     TC_TRACE(ai, 25);
                 }
-                // the state before chunk k of the segment, for phase C
-                if (k >= 1 && !(ok = readout(ai - 1, nullptr, snap_img(j, k - 1))))
-                    break;
-                if (lead)
-                    TC_TRACE(ai, 26);
                 if (wb == 0) {
                     tc_fence_after();
                     state_mma(tm + TM_DSEG, a0 + s * 32768, a0 + s * 32768 + 16384, ones, k > 0,
@@ -953,13 +891,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 if (k == r.nA - 1) {  // segment aggregate complete: publish it
                     if (lead)
                         TC_TRACE(j, 15);
-                    // the segment's prefix images, written with plain stores, are
-                    // read by the tensor-copy engine in phase C
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
                     const int gi = r.tA / p.BH;
                     float* agg =
                         p.slots + (static_cast<size_t>(r.gA.s) * p.R + gi % p.R) * kSlotFloats;
-                    if (!(ok = readout(ai, agg, nullptr)))
+                    if (!(ok = readout(ai, agg)))
                         break;
                     if (lead) {
                         __threadfence();
@@ -984,9 +919,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
         }
     } else if (warp >= 8) {
         // ------------------- phase C (warpgroups of warps 8-11 and 12-15) ---
-        // Warpgroup wg takes every other chunk ci (ci & 1 == wg) and runs it
-        // through: phi(Q), scores, P, [num | den], epilogue; the S_prev
-        // operand arrives with phi(K).  Its first warp issues the MMAs.
+        // Warpgroup wg takes the segments jc with jc & 1 == wg and runs their
+        // chunks in order through: phi(Q), scores, P, [num | den], epilogue.
+        // Its operand slot holds [S_prev^T; z_prev] as bf16 hi/lo: S_in of
+        // the segment at first, then after each chunk but the last the chunk's
+        // [dS^T; dz] (computed on the tensor cores) is added in place.  Its
+        // first warp issues the MMAs.
         const int wg = (warp - 8) >> 2;
         const int tc = tid - 256 - 128 * wg;   // row of the chunk = tensor-memory lane
         const int wq = tc >> 5;                // 32-row block
@@ -999,41 +937,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
         const uint32_t id_pv = idesc_bf16_f32(128, kON, false, true);
         const uint32_t id_in = idesc_bf16_f32(128, kON, false, false);
         const uint32_t tp = tm + TM_P + 128 * wg, to = tm + TM_O + kON * wg;
-        int ci = 0, u = 0;
+        int u = 0;
         bool ok = true, issued = false;
         RoundWalker w;
         Round r;
         for (int j = 0; ok && w.next(p, m, r, j, lead, barid, 128, abort); ++j) {
-            if (!r.nC)
-                continue;
             const int jc = j - kLag;
-            // this group's chunks of the segment: ci0, ci0 + 2, ...
-            const int ci0 = ci + ((ci & 1) != wg ? 1 : 0);
-            const int mine = ci0 < ci + r.nC ? (ci + r.nC - ci0 + 1) / 2 : 0;
-            if (mine == 0 && lead && bwait(&m->sin_full, jc & 1, abort))
-                mbar_arrive(&m->sinslot_free);  // no chunk here: done with the slot
-            for (int e = 0; e < mine && ok; ++e, ++u) {
-                const int c = ci0 + 2 * e, k = c - ci;
-                if (lead)
-                    TC_TRACE(c, 13);
-                // Q and V of chunk c
-                if (!group_ok(!lead || bwait(&m->qv_full[wg], u & 1, abort), barid, 128)) {
+            if (!r.nC || (jc & 1) != wg)
+                continue;
+            for (int k = 0; k < r.nC && ok; ++k, ++u) {
+                const bool last = k == r.nC - 1;
+                // phi(Q) of the chunk in place
+                if (!group_ok(!lead || bwait(&m->q_full[wg], u & 1, abort), barid, 128)) {
                     ok = false;
                     break;
                 }
-                if (lead)
-                    TC_TRACE(c, 14);
                 phi_tile(cw + CW_Q, tc, chunk_valid(p, r.gC.c0 + k), elu);
                 fence_proxy_async_smem();
                 named_bar(barid, 128);
-                if (lead)
-                    TC_TRACE(c, 1);
-                // scores into this group's score buffer, once phi(K) and the
-                // segment's S_in are in
-                if (wq == 0 && __all_sync(full, bwait(&m->k_full[wg], u & 1, abort) &&
-                                                    bwait(&m->sin_full, jc & 1, abort))) {
-                    if (lead)
-                        TC_TRACE(c, 28);
+                // scores, then phi(Q) [S_prev^T; z_prev] (hi, lo) starts the
+                // output accumulator while P is prepared
+                if (wq == 0 && __all_sync(full, bwait(&m->k_full[wg], u & 1, abort))) {
                     tc_fence_after();
                     const uint64_t dq = sdesc_sw128(cwa + CW_Q, 16, 1024);
                     const uint64_t dk = sdesc_sw128(cwa + CW_K, 16, 1024);
@@ -1041,42 +965,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     for (int kk = 0; kk < 4; ++kk)
                         mma_bf16_ss_w(tp, dq + 2 * kk, dk + 2 * kk, id_sc, kk > 0, issue);
                     mma_commit_w(&m->s_done[wg], issue);
-                    // phi(Q) [S_in^T; z_in] (hi, lo) starts the output
-                    // accumulator while P is prepared; past the segment's first
-                    // chunk phi(Q) times the prefix before the chunk adds to it
-                    const uint64_t di = sdesc_sw128(smem_addr(sm + OFF_SIN), 16, 1024);
+                    const uint64_t ds = sdesc_sw128(cwa + CW_S, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ss_w(to, dq + 2 * kk, di + 2 * kk, id_in, kk > 0, issue);
+                        mma_bf16_ss_w(to, dq + 2 * kk, ds + 2 * kk, id_in, kk > 0, issue);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ss_w(to, dq + 2 * kk, di + (kSBytes >> 4) + 2 * kk, id_in, 1,
+                        mma_bf16_ss_w(to, dq + 2 * kk, ds + (kSBytes >> 4) + 2 * kk, id_in, 1,
                                       issue);
-                    if (e == mine - 1)  // this group's last read of the shared slot
-                        mma_commit_w(&m->sinslot_free, issue);
-                    if (k >= 1) {
-                        const uint64_t ds = sdesc_sw128(cwa + CW_S, 16, 1024);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ss_w(to, dq + 2 * kk, ds + 2 * kk, id_in, 1, issue);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ss_w(to, dq + 2 * kk, ds + (kSBytes >> 4) + 2 * kk, id_in, 1,
-                                          issue);
-                    }
+                    mma_commit_w(&m->qs_free[wg], issue);  // the Q slot may refill
                     issued = true;
-                    if (lead)
-                        TC_TRACE(c, 2);
                 }
                 if (!group_ok(!lead || bwait(&m->s_done[wg], u & 1, abort), barid, 128)) {
                     ok = false;
                     break;
                 }
-                if (lead)
-                    TC_TRACE(c, 3);
-                // the scores were the last reader of the chunk's phi(K) tile
-                l2_discard(static_cast<unsigned char*>(p.phi_scratch) +
-                           static_cast<size_t>(phi_index(jc, k)) * (kC * kD * 2) + 128 * tc);
                 tc_fence_after();
                 // P = tril(scores) as bf16 hi/lo, in place: keys 32q..32q+31 of
                 // row tc move to columns 32q..32q+15 (hi) and 32q+16..32q+31 (lo).
@@ -1125,10 +1028,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 }
                 tc_fence_before();
                 named_bar(barid, 128);
-                if (lead)
-                    TC_TRACE(c, 4);
-                // [num | den] += P [V | e] (P hi/lo pairs)
-                if (wq == 0) {
+                // [num | den] += P [V | e] (P hi/lo pairs), once V is in
+                if (wq == 0 && __all_sync(full, bwait(&m->v_full[wg], u & 1, abort))) {
                     tc_fence_after();
                     const uint32_t vs = cwa + CW_V;
                     const uint64_t bv = sdesc_sw128(vs, ones - vs, 1024);
@@ -1145,25 +1046,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                                       bv + step - (step << 16), id_pv, 1, issue);
                     }
                     mma_commit_w(&m->o_done[wg], issue);
-                    if (lead)
-                        TC_TRACE(c, 6);
                 }
                 if (!group_ok(!lead || bwait(&m->o_done[wg], u & 1, abort), barid, 128)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (lead) {  // every slot is free for the next chunk
-                    mbar_arrive(&m->qv_free[wg]);
-                    mbar_arrive(&m->k_free[wg]);
-                    TC_TRACE(c, 7);
-                }
-                if (k >= 1) {  // the image of the prefix before the chunk has been used
-                    const unsigned char* img = snap_img(jc, k - 1);
-                    if (tc < static_cast<int>(kImgBytes / 128))
-                        l2_discard(img + 128 * tc);
-                    if (tc + 128 < static_cast<int>(kImgBytes / 128))
-                        l2_discard(img + 128 * (tc + 128));
+                // the chunk's [dS^T; dz] = [V | e]^T phi(K) into the score
+                // columns (free now) while the epilogue runs; after a segment's
+                // last chunk only the slots are handed back
+                if (wq == 0) {
+                    if (!last)
+                        state_mma(tp, cwa + CW_V, cwa + CW_K, ones, false, issue);
+                    mma_commit_w(&m->ds_done[wg], issue);
                 }
                 // epilogue: o = num / den straight from registers.  A 16x256b
                 // tensor-memory load gives each quad of threads 8 consecutive
@@ -1191,26 +1086,70 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                                 float* orow = obase + row * kD + 2 * (lane & 3);
 #pragma unroll
                                 for (int i = 0; i < 8; ++i) {
-                                    const float2 x = mul2(
+                                    const float2 xo = mul2(
                                         make_float2(__uint_as_float(rr[4 * i + 2 * hr]),
                                                     __uint_as_float(rr[4 * i + 2 * hr + 1])),
                                         make_float2(inv, inv));
-                                    __stcs(reinterpret_cast<float2*>(orow + 8 * i), x);
+                                    __stcs(reinterpret_cast<float2*>(orow + 8 * i), xo);
                                 }
                             }
                         }
                     }
                 }
+                if (!last) {
+                    // S_prev += [dS^T; dz] in the operand slot: row tc (0..64) of
+                    // the hi and lo parts, added in fp32 and split again
+                    if (!group_ok(!lead || bwait(&m->ds_done[wg], u & 1, abort), barid, 128)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (wq < 3) {
+                        uint32_t dd[4][16];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            tmem_ld16(tp + lane_off + 16 * q, dd[q]);
+                        tmem_ld_wait();
+                        if (tc <= kD) {
+                            unsigned char* shi = cw + CW_S;
+                            unsigned char* slo = shi + kSBytes;
+#pragma unroll
+                            for (int cc = 0; cc < 8; ++cc) {
+                                const uint32_t off = sw128_off(tc, cc);
+                                const uint4 h = *reinterpret_cast<const uint4*>(shi + off);
+                                const uint4 l = *reinterpret_cast<const uint4*>(slo + off);
+                                const uint32_t* d8 = &dd[cc >> 1][(cc & 1) * 8];
+                                const uint32_t hv[4] = {h.x, h.y, h.z, h.w};
+                                const uint32_t lv[4] = {l.x, l.y, l.z, l.w};
+                                uint32_t nh[4], nl[4];
+#pragma unroll
+                                for (int t2 = 0; t2 < 4; ++t2) {
+                                    const float a = bf_lo(hv[t2]) + bf_lo(lv[t2]) +
+                                                    __uint_as_float(d8[2 * t2]);
+                                    const float b = bf_hi(hv[t2]) + bf_hi(lv[t2]) +
+                                                    __uint_as_float(d8[2 * t2 + 1]);
+                                    split2(a, b, nh[t2], nl[t2]);
+                                }
+                                *reinterpret_cast<uint4*>(shi + off) =
+                                    make_uint4(nh[0], nh[1], nh[2], nh[3]);
+                                *reinterpret_cast<uint4*>(slo + off) =
+                                    make_uint4(nl[0], nl[1], nl[2], nl[3]);
+                            }
+                        }
+                    }
+                    fence_proxy_async_smem();
+                }
                 tc_fence_before();
-                if (lead)
-                    TC_TRACE(c, 8);
+                named_bar(barid, 128);
+                // the chunk's phi(K) tile has had its last reader
+                l2_discard(static_cast<unsigned char*>(p.phi_scratch) +
+                           static_cast<size_t>(phi_index(jc, k)) * (kC * kD * 2) + 128 * tc);
             }
-            // this group is done with the segment's S_in and ticket slot
+            // done with the segment's S_in and ticket slot
             if (ok && lead) {
                 mbar_arrive(&m->sin_free[jc % NSIN]);
                 mbar_arrive(&m->seg_empty[jc % NS]);
             }
-            ci += r.nC;
         }
 #ifdef LA_TC_TRACE
         if (lead)
@@ -1272,7 +1211,7 @@ struct TcGeom {
     int nseg;
     int R;       // ring slots per sequence
     int total;   // segment tickets
-    size_t flags_off, slots_off, sin_off, phi_off, snap_off, bytes;
+    size_t flags_off, slots_off, sin_off, phi_off, bytes;
 };
 
 int sm_count()
@@ -1310,8 +1249,7 @@ TcGeom tc_geom(int64_t BH, int64_t N, int sms)
     g.sin_off = g.slots_off + sizeof(float) * (size_t)BH * g.R * kSlotFloats;
     g.sin_off = (g.sin_off + 1023) & ~(size_t)1023;
     g.phi_off = (g.sin_off + (size_t)G * NSIN * kImgBytes + 1023) & ~(size_t)1023;
-    g.snap_off = g.phi_off + (size_t)G * NPH * g.L * kC * kD * 2;
-    g.bytes = g.snap_off + (size_t)G * NPH * (g.L - 1) * kImgBytes;
+    g.bytes = g.phi_off + (size_t)G * NPH * g.L * kC * kD * 2;
     return g;
 }
 
@@ -1357,7 +1295,6 @@ cudaError_t tc_forward(const FwdArgs& a)
     p.slots = reinterpret_cast<float*>(ws + g.slots_off);
     p.sin_img = ws + g.sin_off;
     p.phi_scratch = ws + g.phi_off;
-    p.snap = ws + g.snap_off;
     p.out = static_cast<float*>(a.out);
     p.status = a.status;
     cudaError_t e = cudaMemsetAsync(ws, 0, g.slots_off, a.stream);
