@@ -822,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
         const uint32_t issue = wb == 0 ? elect_one() : 0u;
         const uint32_t a0 = smem_addr(sm + OFF_A);
         const uint64_t keep = policy_evict_last();
-        int ai = 0, pend_s = -1;
+        int ai = 0;
         bool ok = true, issued = false;
         // [dS^T; dz] so far (tensor-memory lanes 0..64) copied to dst
         auto readout = [&](int x, float* dst) -> bool {
@@ -866,16 +866,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 phi_tile(ktile, tb, chunk_valid(p, r.gA.c0 + k), elu);
                 fence_proxy_async_smem();
                 named_bar(1, 128);
-                if (lead) {
-                    // phi(K) is kept for phase C in the scratch; the stage of the
-                    // previous tile is released once its copy has read it
+                if (lead) {  // phi(K) is kept for phase C in the scratch
                     tma_store_3d(&p.mphi, ktile, 0, 0, phi_index(j, k), keep);
                     bulk_commit();
-                    if (pend_s >= 0) {
-                        bulk_wait_read<1>();
-                        mbar_arrive(&m->a_empty[pend_s]);
-                    }
-                    pend_s = s;
                     TC_TRACE(ai, 25);
                 }
                 if (wb == 0) {
@@ -887,6 +880,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     issued = true;
                     if (lead)
                         TC_TRACE(ai, 10);
+                }
+                if (lead) {  // the stage is free once its copy has read it
+                    bulk_wait_read<0>();
+                    mbar_arrive(&m->a_empty[s]);
                 }
                 if (k == r.nA - 1) {  // segment aggregate complete: publish it
                     if (lead)
@@ -902,8 +899,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                                    (static_cast<unsigned>(gi + 1) << 2) | 1u);
                         // the segment's phi(K) tiles are all in the scratch
                         bulk_wait<0>();
-                        mbar_arrive(&m->a_empty[pend_s]);
-                        pend_s = -1;
                         mbar_arrive(&m->phik_stored[j % NPH]);
                         mbar_arrive(&m->agg_ready[j % NSIN]);
                         TC_TRACE(j, 24);
@@ -1082,15 +1077,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                             const int rw = 16 * h + 8 * hr + (lane >> 2);  // row within the warp
                             const float inv = __shfl_sync(full, inv_row, rw);
                             const int row = 32 * wq + rw;
-                            if (row < valid) {
-                                float* orow = obase + row * kD + 2 * (lane & 3);
+                            // thread q of a quad holds columns 8i + 2q, 8i + 2q + 1;
+                            // neighbours swap one pair so the even thread owns
+                            // columns 8i + 2q .. 8i + 2q + 3 and the odd one those
+                            // of group i + 1, and every store is 16 bytes
+                            const bool odd = lane & 1;
+                            float* orow = obase + row * kD + 2 * ((lane & 3) & ~1);
 #pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-                                    const float2 xo = mul2(
-                                        make_float2(__uint_as_float(rr[4 * i + 2 * hr]),
-                                                    __uint_as_float(rr[4 * i + 2 * hr + 1])),
-                                        make_float2(inv, inv));
-                                    __stcs(reinterpret_cast<float2*>(orow + 8 * i), xo);
+                            for (int i = 0; i < 8; i += 2) {
+                                const float2 g0 = mul2(
+                                    make_float2(__uint_as_float(rr[4 * i + 2 * hr]),
+                                                __uint_as_float(rr[4 * i + 2 * hr + 1])),
+                                    make_float2(inv, inv));
+                                const float2 g1 = mul2(
+                                    make_float2(__uint_as_float(rr[4 * (i + 1) + 2 * hr]),
+                                                __uint_as_float(rr[4 * (i + 1) + 2 * hr + 1])),
+                                    make_float2(inv, inv));
+                                const float2 give = odd ? g0 : g1;
+                                const float2 got = make_float2(__shfl_xor_sync(full, give.x, 1),
+                                                               __shfl_xor_sync(full, give.y, 1));
+                                if (row < valid) {
+                                    const float4 v4 = odd ? make_float4(got.x, got.y, g1.x, g1.y)
+                                                          : make_float4(g0.x, g0.y, got.x, got.y);
+                                    __stcs(reinterpret_cast<float4*>(orow + 8 * (i + (odd ? 1 : 0))),
+                                           v4);
                                 }
                             }
                         }
