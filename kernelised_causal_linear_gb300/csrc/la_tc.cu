@@ -146,7 +146,7 @@ struct Misc {
     uint64_t a_full[NA], a_empty[NA];
     uint64_t q_full[2], v_full[2], k_full[2], qs_free[2], ds_done[2], s_done[2], o_done[2];
     uint64_t phik_stored[NPH], dseg_done, sin_ready[NSIN], sin_free[NSIN], agg_ready[NSIN];
-    uint64_t drain[3];
+    uint64_t drain[5];
     uint32_t tmem;
     int abort;
     int seg_ticket[NS];
@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
 
     if (tid == 0) {
         uint64_t* bars = reinterpret_cast<uint64_t*>(m);
-        const int nbars = static_cast<int>((reinterpret_cast<uint64_t*>(&m->drain[2]) - bars) + 1);
+        const int nbars = static_cast<int>((reinterpret_cast<uint64_t*>(&m->drain[4]) - bars) + 1);
         for (int i = 0; i < nbars; ++i)
             mbar_init(&bars[i], 1);
         // a phase-A stage is free once its MMA is done and its phi(K) tile
@@ -926,6 +926,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
         const bool lead = tc == 0;
         const int barid = 2 + wg;
         const uint32_t issue = wq == 0 ? elect_one() : 0u;
+        const uint32_t issue3 = wq == 3 ? elect_one() : 0u;
+        bool issued3 = false;
         unsigned char* cw = sm + OFF_CW + wg * kCWBytes;
         const uint32_t cwa = smem_addr(cw);
         const uint32_t id_sc = idesc_bf16_f32(128, 128, false, false);
@@ -1050,10 +1052,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 // the chunk's [dS^T; dz] = [V | e]^T phi(K) into the score
                 // columns (free now) while the epilogue runs; after a segment's
                 // last chunk only the slots are handed back
-                if (wq == 0) {
+                if (wq == 3) {  // the warp with no state rows to update issues it
                     if (!last)
-                        state_mma(tp, cwa + CW_V, cwa + CW_K, ones, false, issue);
-                    mma_commit_w(&m->ds_done[wg], issue);
+                        state_mma(tp, cwa + CW_V, cwa + CW_K, ones, false, issue3);
+                    mma_commit_w(&m->ds_done[wg], issue3);
+                    issued3 = true;
                 }
                 // epilogue: o = num / den straight from registers.  A 16x256b
                 // tensor-memory load gives each quad of threads 8 consecutive
@@ -1115,20 +1118,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     }
                     tc_fence_after();
                     if (wq < 3) {
-                        uint32_t dd[4][16];
+                        unsigned char* shi = cw + CW_S;
+                        unsigned char* slo = shi + kSBytes;
+#pragma unroll 1
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t dd[16];
+                            tmem_ld16(tp + lane_off + 16 * q, dd);
+                            tmem_ld_wait();
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            tmem_ld16(tp + lane_off + 16 * q, dd[q]);
-                        tmem_ld_wait();
-                        if (tc <= kD) {
-                            unsigned char* shi = cw + CW_S;
-                            unsigned char* slo = shi + kSBytes;
-#pragma unroll
-                            for (int cc = 0; cc < 8; ++cc) {
+                            for (int hh = 0; hh < 2; ++hh) {
+                                if (tc > kD)
+                                    break;
+                                const int cc = 2 * q + hh;
                                 const uint32_t off = sw128_off(tc, cc);
                                 const uint4 h = *reinterpret_cast<const uint4*>(shi + off);
                                 const uint4 l = *reinterpret_cast<const uint4*>(slo + off);
-                                const uint32_t* d8 = &dd[cc >> 1][(cc & 1) * 8];
+                                const uint32_t* d8 = &dd[8 * hh];
                                 const uint32_t hv[4] = {h.x, h.y, h.z, h.w};
                                 const uint32_t lv[4] = {l.x, l.y, l.z, l.w};
                                 uint32_t nh[4], nl[4];
@@ -1168,6 +1173,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
         if (issued && *abort) {
             mma_commit_w(&m->drain[1 + wg], issue);
             drain_wait(&m->drain[1 + wg], 0);
+        }
+        if (issued3 && *abort) {
+            mma_commit_w(&m->drain[3 + wg], issue3);
+            drain_wait(&m->drain[3 + wg], 0);
         }
     }
 
