@@ -973,10 +973,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     mma_commit_w(&m->qs_free[wg], issue);  // the Q slot may refill
                     issued = true;
                 }
-                if (!group_ok(!lead || bwait(&m->s_done[wg], u & 1, abort), barid, 128)) {
-                    ok = false;
-                    break;
-                }
+                // each warp starts its part of P as soon as the scores are in
+                // (the issuing warp may still be issuing); verdicts merge below
+                const bool okw = __all_sync(full, bwait(&m->s_done[wg], u & 1, abort));
                 tc_fence_after();
                 // P = tril(scores) as bf16 hi/lo, in place: keys 32q..32q+31 of
                 // row tc move to columns 32q..32q+15 (hi) and 32q+16..32q+31 (lo).
@@ -985,7 +984,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 {
                     const uint32_t pb = tp + lane_off;
 #pragma unroll 1
-                    for (int q = 0; q <= wq; ++q) {
+                    for (int q = 0; q <= (okw ? wq : -1); ++q) {
                         uint32_t v0[16], v1[16], hi[16], lo[16];
                         tmem_ld16(pb + 32 * q, v0);
                         tmem_ld16(pb + 32 * q + 16, v1);
@@ -1024,7 +1023,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     tmem_st_wait();
                 }
                 tc_fence_before();
-                named_bar(barid, 128);
+                if (!group_ok(okw, barid, 128)) {
+                    ok = false;
+                    break;
+                }
                 // [num | den] += P [V | e] (P hi/lo pairs), once V is in
                 if (wq == 0 && __all_sync(full, bwait(&m->v_full[wg], u & 1, abort))) {
                     tc_fence_after();
