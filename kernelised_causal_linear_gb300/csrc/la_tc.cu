@@ -944,14 +944,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                 continue;
             for (int k = 0; k < r.nC && ok; ++k, ++u) {
                 const bool last = k == r.nC - 1;
-                // phi(Q) of the chunk in place
-                if (!group_ok(!lead || bwait(&m->q_full[wg], u & 1, abort), barid, 128)) {
+                // phi(Q) of the chunk in place, each warp as soon as Q is in
+                const bool okq = __all_sync(full, bwait(&m->q_full[wg], u & 1, abort));
+                if (okq) {
+                    phi_tile(cw + CW_Q, tc, chunk_valid(p, r.gC.c0 + k), elu);
+                    fence_proxy_async_smem();
+                }
+                if (!group_ok(okq, barid, 128)) {
                     ok = false;
                     break;
                 }
-                phi_tile(cw + CW_Q, tc, chunk_valid(p, r.gC.c0 + k), elu);
-                fence_proxy_async_smem();
-                named_bar(barid, 128);
                 // scores, then phi(Q) [S_prev^T; z_prev] (hi, lo) starts the
                 // output accumulator while P is prepared
                 if (wq == 0 && __all_sync(full, bwait(&m->k_full[wg], u & 1, abort))) {
@@ -1111,15 +1113,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                         }
                     }
                 }
+                bool okd = true;
                 if (!last) {
                     // S_prev += [dS^T; dz] in the operand slot: row tc (0..64) of
                     // the hi and lo parts, added in fp32 and split again
-                    if (!group_ok(!lead || bwait(&m->ds_done[wg], u & 1, abort), barid, 128)) {
-                        ok = false;
-                        break;
-                    }
+                    // each warp with state rows starts once the chunk's update is in
+                    okd = wq == 3 || __all_sync(full, bwait(&m->ds_done[wg], u & 1, abort));
                     tc_fence_after();
-                    if (wq < 3) {
+                    if (wq < 3 && okd) {
                         unsigned char* shi = cw + CW_S;
                         unsigned char* slo = shi + kSBytes;
 #pragma unroll 1
@@ -1157,7 +1158,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     fence_proxy_async_smem();
                 }
                 tc_fence_before();
-                named_bar(barid, 128);
+                if (!group_ok(okd, barid, 128)) {
+                    ok = false;
+                    break;
+                }
                 // the chunk's phi(K) tile has had its last reader
                 l2_discard(static_cast<unsigned char*>(p.phi_scratch) +
                            static_cast<size_t>(phi_index(jc, k)) * (kC * kD * 2) + 128 * tc);
