@@ -21,22 +21,21 @@
 //
 // Chunks are grouped into segments of L consecutive chunks of one sequence.
 // One persistent CTA per SM takes segments in ticket order (segment-major over
-// the B*H sequences) and runs each in two phases:
-//   A  K, V of every chunk (V kept in L2 with an evict-last hint); phi(K),
-//      also kept in a scratch ring for phase C; the segment's running sum of
-//      [dS^T; dz] accumulated on the tensor cores and, after every chunk but
-//      the last, copied out as a prefix snapshot; the total (the aggregate) is
-//      published to a ring of per-segment slots in global memory;
-//   C  the outputs: Q, phi(K) (scratch) and V (L2); S_prev of chunk k is
-//      S_in + the snapshot after chunk k-1, so the chunks of a segment do not
-//      wait on each other.
+// the B*H sequences) and runs each in two phases, one round apart:
+//   A  K, V of every chunk (V kept in L2 with an evict-last hint); phi(K), also
+//      copied to a scratch ring for phase C; the segment's [dS^T; dz] summed
+//      on the tensor cores; the total (the aggregate) is published to a ring of
+//      per-segment slots in global memory;
+//   C  the outputs, by the output group that owns the segment: Q, phi(K)
+//      (scratch) and V (L2); S_prev of the first chunk is S_in, and after each
+//      chunk but the last the chunk's [dS^T; dz] is added to the group's
+//      S_prev operand in place.
 // Between them a decoupled look-back over the predecessors' slots gives S_in,
-// the state before the segment, and publishes the segment's inclusive prefix.
-// Round j interleaves phase A of local segment j with phase C of segment j-1,
-// chunk by chunk, so the look-back of a segment is hidden behind a round.
-// The look-back starts from the nearest inclusive prefix and adds later
-// aggregates in segment order, so every prefix is the same left-to-right fp32
-// sum whatever the timing: results are bitwise reproducible.
+// the state before the segment, and publishes it as the segment's exclusive
+// prefix.  It adds the nearest exclusive prefix, that segment's aggregate and
+// the later aggregates farthest first, so every prefix is the same
+// left-to-right fp32 sum whatever the timing: results are bitwise
+// reproducible.
 //
 // [V | e] (V and a constant 2 KiB block e whose first column is all ones)
 // is read in two places: as the A operand of the state MMAs, where D =
@@ -45,20 +44,19 @@
 //
 // The CTA is warp-specialised; work flows through shared-memory stages and
 // tensor-memory buffers, synchronised by mbarriers:
-//   warp 0      producer: segment tickets, phase-A loads (K, V)
-//   warps 2, 3  producers: phase-C loads (Q, phi(K), V) of output warpgroup
-//               0 and 1
-//   warps 4-7   phase A: phi(K) in place and to the scratch ring; the
-//               segment's running [dS^T; dz] on the tensor cores and its
-//               snapshots; the aggregate; then the look-back that yields
-//               S_in and the inclusive prefix
+//   warp 0      producer (one thread): segment tickets and every TMA load,
+//               advancing three streams (phase A, output group 0, output
+//               group 1) as their slots free up
+//   warps 1-3   look-back: S_in of each segment from the predecessors'
+//               slots, published as its exclusive prefix and written once as
+//               the bf16 hi/lo operand image the output group loads
+//   warps 4-7   phase A: phi(K) in place, copied out by TMA; the segment's
+//               running [dS^T; dz] on the tensor cores; the aggregate
 //   warps 8-11, 12-15
-//               output warpgroups 0 and 1, taking alternate chunks: S_prev
-//               from S_in and the snapshot, phi(Q), scores, P (causal mask,
-//               bf16 hi/lo in place), [num | den], epilogue and TMA store,
-//               each issuing its own MMAs.  Two chunks are in flight at once,
-//               so one group's MMAs and loads overlap the other's arithmetic.
-//   warp 1      idle
+//               output groups 0 and 1, each owning every other segment:
+//               phi(Q), scores, P (causal mask, bf16 hi/lo in place),
+//               [num | den], epilogue (16-byte stores), then the chunk's
+//               [dS^T; dz] into the S_prev operand.  Each issues its own MMAs.
 //
 // Precision: phi(Q), phi(K) and V enter the MMAs as bf16 (phi rounded once);
 // P and S_prev are fp32 and enter as a bf16 hi/lo pair (two MMAs each), so
@@ -85,9 +83,9 @@ constexpr int kC = 128;        // tokens per chunk
 constexpr int kD = 64;         // d = dv
 constexpr int kThreads = 512;  // 16 warps
 constexpr int NS = 4;          // segment-ticket ring
-constexpr int NSIN = 4;        // S_in ring (a segment's S_in lives through its phase C)
+constexpr int NSIN = 4;        // S_in image ring (an image lives until its segment's phase C is done)
 constexpr int kStateFloats = kD * kD + kD;         // S^T (dv x d) then z (d)
-constexpr int kSlotFloats = 2 * kStateFloats;      // aggregate, inclusive
+constexpr int kSlotFloats = 2 * kStateFloats;      // aggregate, exclusive prefix
 constexpr int kMaxList = 128;                      // look-back entries
 constexpr uint32_t kImgPart = 65 * 128;            // rows 0..64 of one bf16 part (hi or lo)
 constexpr uint32_t kImgBytes = 2 * kImgPart;       // one state operand image: hi, then lo
@@ -109,7 +107,7 @@ constexpr int kMaxL = 8;       // largest segment (chunks)
 #ifndef LA_TC_SEG_DIV
 #define LA_TC_SEG_DIV 12       // segments per CTA the segment length aims at
 #endif
-constexpr int NPH = 4;         // phi(K) scratch and snapshot ring depth, in segments
+constexpr int NPH = 4;         // phi(K) scratch ring depth, in segments
 constexpr uint32_t SMEM_BYTES = OFF_ONES + 2048 + 1024;  // + alignment slack
 static_assert(OFF_ONES % 1024 == 0 && kCWBytes % 1024 == 0 && kSBytes % 1024 == 0 &&
                   CW_S == CW_K + 16384 && CW_S + 16384 <= kCWBytes,
@@ -374,8 +372,9 @@ __device__ __forceinline__ int chunk_valid(const TcParams& p, int c)
 }
 
 // Job order shared by every role.  Round j holds phase A of local segment j
-// and phase C of local segment j-kLag, interleaved chunk by chunk
-// (A0 C0 A1 C1 ...); the rounds between a segment's phases hide its look-back.
+// and phase C of local segment j-kLag (run by output group (j-kLag) & 1, which
+// may still be on it in the next round); the round between a segment's phases
+// hides its look-back.
 constexpr int kLag = 1;
 struct Round {
     int j;        // round = local index of the A segment
