@@ -28,7 +28,8 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - All tensor arguments are DEVICE pointers on the current CUDA device,
- *    owned by the caller, contiguous row-major, 16-byte aligned:
+ *    owned by the caller, contiguous row-major, 16-byte aligned (workspaces:
+ *    256-byte aligned):
  *        q, k   [B, H, N, d]     (dtype: bf16 or fp32, see la_dtype)
  *        v      [B, H, N, dv]
  *        out    [B, H, N, dv]    always fp32
@@ -118,8 +119,10 @@ LA_API size_t la_forward_workspace_size(int64_t B, int64_t H, int64_t N, int d, 
  *   causal = 0 : every o_i reads the full-sequence state (gamma must be NULL).
  *   feature_map: la_feature_map.  dtype: la_dtype of q, k, v.
  *   workspace  : device buffer of at least la_forward_workspace_size() bytes,
- *                16-byte aligned, owned by the caller; must not be used by
- *                another call that runs concurrently.
+ *                256-byte aligned (cudaMalloc and PyTorch allocations are),
+ *                owned by the caller; must not be used by another call that
+ *                runs concurrently.  A missing, short or misaligned workspace
+ *                returns LA_ERR_WORKSPACE before anything is enqueued.
  * Returns LA_OK once the work is enqueued on `stream`.
  */
 LA_API la_status la_forward(const void* q, const void* k, const void* v, float* out, int64_t B,
@@ -136,7 +139,8 @@ LA_API la_status la_forward(const void* q, const void* k, const void* v, float* 
 LA_API const char* la_forward_path(int64_t B, int64_t H, int64_t N, int d, int dv, int causal,
                                    int feature_map, int has_decay, int dtype);
 
-/* Bytes of device workspace la_state needs (0 for N = 0). */
+/* Bytes of device workspace la_state needs (0 for N = 0); the workspace must be
+ * 256-byte aligned, as for la_forward. */
 LA_API size_t la_state_workspace_size(int64_t B, int64_t H, int64_t N, int d, int dv, int dtype);
 
 /*

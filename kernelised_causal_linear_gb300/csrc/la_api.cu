@@ -40,6 +40,9 @@ int* status_ptr()
 
 bool dim_ok(int x) { return x == 32 || x == 64 || x == 128; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Workspaces hold 128-byte lines that kernels drop from L2 and 1024-byte
+// aligned TMA regions laid out from the base, so the base must be 256-aligned.
+bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 
 la_status check_sizes(int64_t B, int64_t H, int64_t N, int d, int dv, int fm, int dtype)
 {
@@ -172,7 +175,7 @@ la_status la_forward(const void* q, const void* k, const void* v, float* out, in
     const bool tc = tc_forward_eligible(a);
     const size_t need = tc ? tc_forward_workspace(B * H, N)
                            : simt_forward_workspace(B * H, N, d, dv, causal);
-    if (!workspace || workspace_bytes < need || !aligned16(workspace))
+    if (!workspace || workspace_bytes < need || !aligned256(workspace))
         return LA_ERR_WORKSPACE;
     return from_cuda(tc ? tc_forward(a) : simt_forward(a));
 }
@@ -199,7 +202,7 @@ la_status la_state(const void* k, const void* v, float* S, float* z, int64_t B, 
     if (!k || !v || !aligned16(k) || !aligned16(v))
         return LA_ERR_INVALID_ARG;
     const size_t need = simt_state_workspace(B * H, N, d, dv);
-    if (!workspace || workspace_bytes < need || !aligned16(workspace))
+    if (!workspace || workspace_bytes < need || !aligned256(workspace))
         return LA_ERR_WORKSPACE;
 
     FwdArgs a{};

@@ -44,7 +44,7 @@ def test_status_strings_and_version(lib):
 
 
 I64, I, SZ, VP = ctypes.c_int64, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
-FAKE = VP(0x10000)  # aligned, never dereferenced: every call below fails validation first
+FAKE = VP(0x10000)  # 256-aligned, never dereferenced: every call below fails validation first
 
 
 def fwd(lib, q=FAKE, B=1, H=1, N=8, d=64, dv=64, causal=1, fm=0, gamma=None, dtype=0,
@@ -68,6 +68,9 @@ def test_forward_argument_errors(lib):
     assert fwd(lib, q=VP(0x10004)) == 1                # misaligned
     assert fwd(lib, ws=None) == 6
     assert fwd(lib, ws_bytes=16) == 6
+    # a workspace 16-aligned but not 256-aligned is refused before any launch
+    assert fwd(lib, ws=VP(0x10010)) == 6
+    assert fwd(lib, ws=VP(0x10080)) == 6
     g = (ctypes.c_float * 1)(0.5)
     assert fwd(lib, causal=0, gamma=g) == 2             # decay undefined non-causal
     bad = (ctypes.c_float * 1)(1.5)
