@@ -13,8 +13,9 @@ upcast to fp64 without rounding) and returns fp64 results.
 Page citations for each computation are in the header of ``la_oracle.c``:
 the causal recurrence ("Efficient Attention Variants", section 5), the
 non-causal reassociation (same page, section 4), the RetNet scalar decay
-(same page, section 7.1) and the explicit masked kernel matrix (same page,
-section 10).
+(same page, section 7.1), the GLA per-channel decay (same page, section
+7.2), the Performer positive random features (same page, section 6) and the
+explicit masked kernel matrix (same page, section 10).
 """
 from __future__ import annotations
 
@@ -75,12 +76,14 @@ class Oracle:
         L, I = ctypes.c_long, ctypes.c_int
         lib.orc_phi.argtypes = [dp, dp, L, I]
         lib.orc_phi.restype = None
-        lib.orc_forward.argtypes = [dp, dp, dp, dp, L, L, L, L, L, I, I, dp, I]
+        lib.orc_forward.argtypes = [dp, dp, dp, dp, L, L, L, L, L, I, I, dp, dp, dp, dp, I]
         lib.orc_forward.restype = I
-        lib.orc_state.argtypes = [dp, dp, dp, dp, L, L, L, L, L, I, dp, I, I]
+        lib.orc_state.argtypes = [dp, dp, dp, dp, L, L, L, L, L, I, dp, dp, I, I]
         lib.orc_state.restype = I
-        lib.orc_decode_step.argtypes = [dp, dp, dp, dp, dp, dp, L, L, L, L, I, dp, I]
+        lib.orc_decode_step.argtypes = [dp, dp, dp, dp, dp, dp, L, L, L, L, I, dp, dp, I]
         lib.orc_decode_step.restype = I
+        lib.orc_favor.argtypes = [dp, dp, dp, L, L, L]
+        lib.orc_favor.restype = None
         lib.orc_dense.argtypes = [dp, dp, dp, dp, dp, L, L, L, I, I, ctypes.c_double]
         lib.orc_dense.restype = I
         self.lib = lib
@@ -122,50 +125,71 @@ class Oracle:
         self.lib.orc_phi(self._p(x), self._p(y), x.size, self._fm(fm))
         return y
 
-    def forward(self, q, k, v, causal=True, fm="elu1", gamma=None, nthreads=0,
-                allow_nonpositive_den=False) -> np.ndarray:
-        """q, k: [B,H,N,d]; v: [B,H,N,dv] -> out [B,H,N,dv] (fp64)."""
+    def forward(self, q, k, v, causal=True, fm="elu1", gamma=None, alpha=None, S0=None,
+                z0=None, nthreads=0, allow_nonpositive_den=False) -> np.ndarray:
+        """q, k: [B,H,N,d]; v: [B,H,N,dv] -> out [B,H,N,dv] (fp64).
+
+        gamma: [H] scalar decay per head; alpha: [B,H,N,d] per-key-channel
+        decay; S0, z0: [B,H,d,dv], [B,H,d] state before the first token."""
         q, k, v = self._arr(q), self._arr(k), self._arr(v)
         B, H, N, d = q.shape
         dv = v.shape[-1]
         assert k.shape == (B, H, N, d) and v.shape == (B, H, N, dv)
         g = None if gamma is None else self._arr(gamma).reshape(H)
+        a = None if alpha is None else self._arr(alpha).reshape(B, H, N, d)
+        s0 = None if S0 is None else self._arr(S0).reshape(B, H, d, dv)
+        zz0 = None if z0 is None else self._arr(z0).reshape(B, H, d)
         out = np.empty((B, H, N, dv), dtype=np.float64)
         rc = self.lib.orc_forward(self._p(q), self._p(k), self._p(v), self._p(out), B, H, N, d,
-                                  dv, int(bool(causal)), self._fm(fm), self._p(g), nthreads)
+                                  dv, int(bool(causal)), self._fm(fm), self._p(g), self._p(a),
+                                  self._p(s0), self._p(zz0), nthreads)
         self._check(rc, allow_nonpositive_den)
         return out
 
-    def state(self, k, v, fm="elu1", gamma=None, S0=None, z0=None, nthreads=0):
+    def state(self, k, v, fm="elu1", gamma=None, alpha=None, S0=None, z0=None, nthreads=0):
         """State (S [B,H,d,dv], z [B,H,d]) after the N tokens of k, v [B,H,N,*],
         starting from zero or from (S0, z0)."""
         k, v = self._arr(k), self._arr(v)
         B, H, N, d = k.shape
         dv = v.shape[-1]
         g = None if gamma is None else self._arr(gamma).reshape(H)
+        a = None if alpha is None else self._arr(alpha).reshape(B, H, N, d)
         init = S0 is not None
         S = self._arr(S0).copy() if init else np.zeros((B, H, d, dv))
         z = self._arr(z0).copy() if init else np.zeros((B, H, d))
         rc = self.lib.orc_state(self._p(k), self._p(v), self._p(S), self._p(z), B, H, N, d, dv,
-                                self._fm(fm), self._p(g), int(init), nthreads)
+                                self._fm(fm), self._p(g), self._p(a), int(init), nthreads)
         self._check(rc, True)
         return S, z
 
-    def decode_step(self, S, z, q, k, v, fm="elu1", gamma=None, nthreads=0,
+    def decode_step(self, S, z, q, k, v, fm="elu1", gamma=None, alpha=None, nthreads=0,
                     allow_nonpositive_den=False):
-        """One token per sequence: q, k [B,H,d], v [B,H,dv]; returns
-        (out [B,H,dv], S', z') without modifying the arrays passed in."""
+        """One token per sequence: q, k [B,H,d], v [B,H,dv], alpha [B,H,d] or
+        None; returns (out [B,H,dv], S', z') without modifying the arrays
+        passed in."""
         q, k, v = self._arr(q), self._arr(k), self._arr(v)
         S, z = self._arr(S).copy(), self._arr(z).copy()
         B, H, d = q.shape
         dv = v.shape[-1]
         g = None if gamma is None else self._arr(gamma).reshape(H)
+        a = None if alpha is None else self._arr(alpha).reshape(B, H, d)
         out = np.empty((B, H, dv))
         rc = self.lib.orc_decode_step(self._p(S), self._p(z), self._p(q), self._p(k), self._p(v),
                                       self._p(out), B, H, d, dv, self._fm(fm), self._p(g),
-                                      nthreads)
+                                      self._p(a), nthreads)
         self._check(rc, allow_nonpositive_den)
         return out, S, z
+
+    def favor(self, x, w) -> np.ndarray:
+        """Positive random features: x [..., d], w [r, d] -> [..., r]."""
+        x, w = self._arr(x), self._arr(w)
+        d = x.shape[-1]
+        r = w.shape[0]
+        assert w.shape == (r, d)
+        xf = np.ascontiguousarray(x.reshape(-1, d))
+        y = np.empty((xf.shape[0], r))
+        self.lib.orc_favor(self._p(xf), self._p(w), self._p(y), xf.shape[0], d, r)
+        return y.reshape(x.shape[:-1] + (r,))
 
     def dense(self, q, k, v, causal=True, fm="elu1", gamma=1.0, return_weights=False,
               allow_nonpositive_den=False):

@@ -29,6 +29,23 @@
  *     no feature map and no normaliser
  *     ("Efficient Attention Variants", section 7.1 RetNet).
  *
+ *   per-key-channel decay (GLA form): S_t = diag(alpha_t) S_{t-1} + k_t v_t^T,
+ *     alpha_t in (0,1]^d scales row i of the state (key feature i) and is
+ *     broadcast along the value channels
+ *     ("Efficient Attention Variants", section 7.2 GLA; "Linear Attention and
+ *      SSM", list of phi choices, RWKV-5/6 state M_s = diag(w) M_{s-1} + ...).
+ *
+ *   initial state: every recurrence may start from a given (S_0, z_0) instead
+ *     of zero -- the state is the whole summary of the prefix, so a sequence
+ *     can be processed in pieces ("Efficient Attention Variants", sections 1
+ *     and 5: a fixed-size state replaces the history).
+ *
+ *   positive random features (Performer): with x = u / d^(1/4) and Gaussian
+ *     rows w_1..w_r (passed in, drawn by the caller),
+ *     phi(u)_j = exp(w_j^T x - |x|^2 / 2) / sqrt(r), whose inner products
+ *     estimate exp(q^T k / sqrt(d)) without bias
+ *     ("Efficient Attention Variants", section 6 Performer).
+ *
  *   explicit N x N masked kernel matrix (the object the method avoids), used
  *     only as a brute-force cross-check on tiny inputs:
  *     A_ij = phi(q_i)^T phi(k_j) * L_ij,  O = A V / rowsum(A)
@@ -44,7 +61,12 @@
  *   - a decay gamma combined with a normalised map decays z with the same
  *     gamma, i.e. the mask L_ij = gamma^(i-j) multiplies numerator and
  *     denominator alike.
- *   - no 1/sqrt(d) scaling anywhere: the linear forms on the pages have none.
+ *   - no 1/sqrt(d) scaling anywhere: the linear forms on the pages have none
+ *     (the random-feature map scales by d^(-1/4) itself, as its page does).
+ *   - per-channel decay with a normalised map decays z_i with alpha_t,i, as
+ *     the scalar case decays z with gamma.
+ *   - an initial state is continued exactly as if its prefix had been run
+ *     through the recurrence; the non-causal form takes none.
  *
  * Planted-mistake hooks (ORC_PLANT_*) exist only so that the test-suite can
  * build deliberately wrong variants of this file and check that its pins
@@ -105,7 +127,7 @@ static int orc_check_dims(long B, long H, long N, long d, long dv, int fm)
  */
 static int orc_seq_recurrence(const double* q, const double* k, const double* v, double* out,
                               double* S, double* z, long N, long d, long dv, int fm, double gamma,
-                              double* f, double* g, double* num)
+                              const double* alpha, double* f, double* g, double* num)
 {
     int rc = ORC_OK;
     const int norm = orc_normalised(fm);
@@ -130,9 +152,16 @@ static int orc_seq_recurrence(const double* q, const double* k, const double* v,
                 out[t * dv + c] = norm ? num[c] / den : num[c];
         }
 #endif
-        /* write: S <- gamma S + phi(k_t) v_t^T ; z <- gamma z + phi(k_t) */
+        /* write: S <- a S + phi(k_t) v_t^T ; z <- a z + phi(k_t), with a the
+         * scalar gamma or, per row i of the state, alpha_t,i */
         for (long i = 0; i < d; ++i) {
+            if (alpha)
+                gamma = alpha[t * d + i];
             for (long c = 0; c < dv; ++c) {
+#ifdef ORC_PLANT_GLA_ALONG_VALUES
+                if (alpha)
+                    gamma = alpha[t * d + (c % d)];
+#endif
 #ifdef ORC_PLANT_DECAY_AFTER_WRITE
                 S[i * dv + c] = gamma * (S[i * dv + c] + f[i] * v[t * dv + c]);
 #elif defined(ORC_PLANT_TRANSPOSED_UPDATE)
@@ -183,7 +212,7 @@ static int orc_seq_noncausal(const double* q, const double* k, const double* v, 
     const int norm = orc_normalised(fm);
     memset(S, 0, sizeof(double) * d * dv);
     memset(z, 0, sizeof(double) * d);
-    orc_seq_recurrence(NULL, k, v, NULL, S, z, N, d, dv, fm, 1.0, f, g, num);
+    orc_seq_recurrence(NULL, k, v, NULL, S, z, N, d, dv, fm, 1.0, NULL, f, g, num);
     for (long t = 0; t < N; ++t) {
         for (long i = 0; i < d; ++i)
             g[i] = orc_phi1(q[t * d + i], fm);
@@ -211,6 +240,8 @@ typedef struct {
     const double *q, *k, *v;
     double *out, *S, *z;
     const double* gamma;
+    const double* alpha;   /* [B,H,N,d] per-channel decay, or NULL */
+    const double *S0, *z0; /* [B,H,d,dv], [B,H,d] initial state, or NULL */
     long B, H, N, d, dv;
     int fm, causal, init_from_state;
     long next; /* shared work counter */
@@ -235,6 +266,7 @@ static void* orc_worker(void* arg)
             break;
         const long h = s % J->H;
         const double gamma = J->gamma ? J->gamma[h] : 1.0;
+        const double* alpha = J->alpha ? J->alpha + s * N * d : NULL;
         int rc = ORC_OK;
         if (J->kind == JOB_FORWARD) {
             const double* q = J->q + s * N * d;
@@ -242,9 +274,19 @@ static void* orc_worker(void* arg)
             const double* v = J->v + s * N * dv;
             double* o = J->out + s * N * dv;
             if (J->causal) {
-                memset(S, 0, sizeof(double) * d * dv);
-                memset(z, 0, sizeof(double) * d);
-                rc = orc_seq_recurrence(q, k, v, o, S, z, N, d, dv, J->fm, gamma, f, g, num);
+                if (J->S0) {
+                    memcpy(S, J->S0 + s * d * dv, sizeof(double) * d * dv);
+#ifdef ORC_PLANT_IGNORE_Z0
+                    memset(z, 0, sizeof(double) * d);
+#else
+                    memcpy(z, J->z0 + s * d, sizeof(double) * d);
+#endif
+                } else {
+                    memset(S, 0, sizeof(double) * d * dv);
+                    memset(z, 0, sizeof(double) * d);
+                }
+                rc = orc_seq_recurrence(q, k, v, o, S, z, N, d, dv, J->fm, gamma, alpha, f, g,
+                                        num);
             } else {
                 rc = orc_seq_noncausal(q, k, v, o, N, d, dv, J->fm, S, z, f, g, num);
             }
@@ -256,11 +298,11 @@ static void* orc_worker(void* arg)
                 memset(zs, 0, sizeof(double) * d);
             }
             rc = orc_seq_recurrence(NULL, J->k + s * N * d, J->v + s * N * dv, NULL, Ss, zs, N, d,
-                                    dv, J->fm, gamma, f, g, num);
+                                    dv, J->fm, gamma, alpha, f, g, num);
         } else { /* JOB_DECODE: one token per sequence, state in place */
             rc = orc_seq_recurrence(J->q + s * d, J->k + s * d, J->v + s * dv, J->out + s * dv,
-                                    J->S + s * d * dv, J->z + s * d, 1, d, dv, J->fm, gamma, f,
-                                    g, num);
+                                    J->S + s * d * dv, J->z + s * d, 1, d, dv, J->fm, gamma,
+                                    alpha, f, g, num);
         }
         if (rc != ORC_OK) {
             pthread_mutex_lock(&J->lock);
@@ -307,57 +349,67 @@ static int orc_run(orc_job* J, int nthreads)
 /*
  * Forward over B*H independent sequences.
  *   q, k : [B,H,N,d]   v, out : [B,H,N,dv]   gamma : [H] or NULL (= 1)
+ *   alpha : [B,H,N,d] per-channel decay or NULL (not together with gamma)
+ *   S0, z0 : [B,H,d,dv], [B,H,d] state before the first token, or NULL (= 0);
+ *            both or neither
  *   causal = 1: recurrence (write then read); causal = 0: reassociation.
- * Decay with causal = 0 is not defined by the pages and is rejected.
- * nthreads <= 0 uses every online core.
+ * Decay or an initial state with causal = 0 is not defined by the pages and
+ * is rejected.  nthreads <= 0 uses every online core.
  */
 int orc_forward(const double* q, const double* k, const double* v, double* out, long B, long H,
-                long N, long d, long dv, int causal, int fm, const double* gamma, int nthreads)
+                long N, long d, long dv, int causal, int fm, const double* gamma,
+                const double* alpha, const double* S0, const double* z0, int nthreads)
 {
-    if (orc_check_dims(B, H, N, d, dv, fm) != ORC_OK || (!causal && gamma))
+    if (orc_check_dims(B, H, N, d, dv, fm) != ORC_OK || (gamma && alpha) || (!S0 != !z0))
+        return ORC_ERR_ARG;
+    if (!causal && (gamma || alpha || S0))
         return ORC_ERR_ARG;
     orc_job J;
     memset(&J, 0, sizeof J);
     J.kind = JOB_FORWARD;
     J.q = q, J.k = k, J.v = v, J.out = out, J.gamma = gamma;
+    J.alpha = alpha, J.S0 = S0, J.z0 = z0;
     J.B = B, J.H = H, J.N = N, J.d = d, J.dv = dv, J.fm = fm, J.causal = causal;
     return orc_run(&J, nthreads);
 }
 
 /*
- * State after a prefix: S [B,H,d,dv], z [B,H,d].  With init_from_state = 0
+ * State after a prefix: S [B,H,d,dv], z [B,H,d] (alpha: [B,H,N,d] or NULL).
+ * With init_from_state = 0
  * the recurrence starts at S_0 = 0, z_0 = 0 (the arrays are overwritten);
  * with init_from_state = 1 it continues from the values passed in.
  */
 int orc_state(const double* k, const double* v, double* S, double* z, long B, long H, long N,
-              long d, long dv, int fm, const double* gamma, int init_from_state, int nthreads)
+              long d, long dv, int fm, const double* gamma, const double* alpha,
+              int init_from_state, int nthreads)
 {
-    if (orc_check_dims(B, H, N, d, dv, fm) != ORC_OK)
+    if (orc_check_dims(B, H, N, d, dv, fm) != ORC_OK || (gamma && alpha))
         return ORC_ERR_ARG;
     orc_job J;
     memset(&J, 0, sizeof J);
     J.kind = JOB_STATE;
-    J.k = k, J.v = v, J.S = S, J.z = z, J.gamma = gamma;
+    J.k = k, J.v = v, J.S = S, J.z = z, J.gamma = gamma, J.alpha = alpha;
     J.B = B, J.H = H, J.N = N, J.d = d, J.dv = dv, J.fm = fm;
     J.init_from_state = init_from_state;
     return orc_run(&J, nthreads);
 }
 
 /*
- * One decode step for B*H sequences: q, k [B,H,d], v, out [B,H,dv]; S, z are
- * updated in place (write, then read), exactly one iteration of the causal
+ * One decode step for B*H sequences: q, k [B,H,d], v, out [B,H,dv], alpha
+ * [B,H,d] or NULL; S, z are updated in place (write, then read), exactly one iteration of the causal
  * recurrence.
  */
 int orc_decode_step(double* S, double* z, const double* q, const double* k, const double* v,
                     double* out, long B, long H, long d, long dv, int fm, const double* gamma,
-                    int nthreads)
+                    const double* alpha, int nthreads)
 {
-    if (orc_check_dims(B, H, 1, d, dv, fm) != ORC_OK)
+    if (orc_check_dims(B, H, 1, d, dv, fm) != ORC_OK || (gamma && alpha))
         return ORC_ERR_ARG;
     orc_job J;
     memset(&J, 0, sizeof J);
     J.kind = JOB_DECODE;
     J.q = q, J.k = k, J.v = v, J.out = out, J.S = S, J.z = z, J.gamma = gamma;
+    J.alpha = alpha;
     J.B = B, J.H = H, J.N = 1, J.d = d, J.dv = dv, J.fm = fm;
     return orc_run(&J, nthreads);
 }
@@ -411,4 +463,32 @@ int orc_dense(const double* q, const double* k, const double* v, double* out, do
     free(fq);
     free(fk);
     return rc;
+}
+
+/*
+ * Positive random features of n vectors u (rows of x, each d long) with r
+ * Gaussian rows w (r x d, drawn by the caller):
+ *   x' = u / d^(1/4),  y_j = exp(w_j^T x' - |x'|^2 / 2) / sqrt(r)
+ * so that y(q)^T y(k) estimates exp(q^T k / sqrt(d)) without bias
+ * ("Efficient Attention Variants", section 6).  y is n x r.
+ */
+void orc_favor(const double* x, const double* w, double* y, long n, long d, long r)
+{
+    const double s = 1.0 / pow((double)d, 0.25);
+    const double inv_sqrt_r = 1.0 / sqrt((double)r);
+    for (long t = 0; t < n; ++t) {
+        double nrm = 0.0;
+        for (long i = 0; i < d; ++i)
+            nrm += (x[t * d + i] * s) * (x[t * d + i] * s);
+        for (long j = 0; j < r; ++j) {
+            double p = 0.0;
+            for (long i = 0; i < d; ++i)
+                p += w[j * d + i] * (x[t * d + i] * s);
+#ifdef ORC_PLANT_FAVOR_NO_NORM
+            y[t * r + j] = exp(p) * inv_sqrt_r;
+#else
+            y[t * r + j] = exp(p - 0.5 * nrm) * inv_sqrt_r;
+#endif
+        }
+    }
 }

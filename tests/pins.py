@@ -249,6 +249,125 @@ def pin_decode(o):
     _close(z2, z, 1e-13, 1e-13, "continued normaliser")
 
 
+# ------------------------------------------------------ initial state ------
+def pin_initial_state(o):
+    """A forward continued from the state of a prefix equals the same rows of
+    the forward over the whole sequence, and the explicit matrix over it
+    (the state summarises the prefix, "Efficient Attention Variants" s.5)."""
+    rng = np.random.default_rng(21)
+    B, H, P, M, d, dv = 2, 2, 11, 9, 5, 3
+    q = rng.normal(size=(B, H, P + M, d))
+    k = rng.normal(size=(B, H, P + M, d))
+    v = rng.normal(size=(B, H, P + M, dv))
+    alpha = rng.uniform(0.6, 1.0, size=(B, H, P + M, d))
+    for fm, gam, al in (("elu1", None, None), ("none", np.array([0.9, 0.6]), None),
+                        ("elu1", np.array([0.8, 1.0]), None), ("elu1", None, alpha)):
+        full = o.forward(q, k, v, fm=fm, gamma=gam, alpha=al)
+        S0, z0 = o.state(k[:, :, :P], v[:, :, :P], fm=fm, gamma=gam,
+                         alpha=None if al is None else al[:, :, :P])
+        tail = o.forward(q[:, :, P:], k[:, :, P:], v[:, :, P:], fm=fm, gamma=gam,
+                         alpha=None if al is None else al[:, :, P:], S0=S0, z0=z0)
+        _close(tail, full[:, :, P:], 1e-12, 1e-12, f"continued forward ({fm})")
+        if al is None:
+            for b in range(B):
+                for h in range(H):
+                    bf = brute_force(q[b, h], k[b, h], v[b, h], fm=fm,
+                                     gamma=1.0 if gam is None else gam[h])
+                    _close(tail[b, h], bf[P:], 1e-11, 1e-11, f"continued vs explicit {(b, h)}")
+    try:
+        o.forward(q, k, v, causal=False, S0=np.zeros((B, H, d, dv)), z0=np.zeros((B, H, d)))
+    except Exception:
+        pass
+    else:
+        raise AssertionError("an initial state with the non-causal form must be rejected")
+
+
+# ------------------------------------------------ per-channel decay -------
+def gla_brute_force(q, k, v, alpha, fm="none"):
+    """o_i = sum_{j<=i} sum_r fq_ir fk_jr (prod_{s=j+1..i} alpha_sr) v_j,
+    written out with explicit products ("Efficient Attention Variants" s.7.2:
+    alpha_t scales row r of the state, broadcast along the values)."""
+    fq, fk = (lib_phi(q), lib_phi(k)) if fm == "elu1" else (q, k)
+    n, d = q.shape
+    out = np.zeros((n, v.shape[1]))
+    den = np.zeros(n)
+    for i in range(n):
+        for j in range(i + 1):
+            w = np.ones(d)
+            for s_ in range(j + 1, i + 1):
+                w = w * alpha[s_]
+            a = float(np.sum(fq[i] * fk[j] * w))
+            out[i] += a * v[j]
+            den[i] += a
+    return out if fm == "none" else out / den[:, None]
+
+
+def pin_gla(o):
+    rng = np.random.default_rng(23)
+    B, H, N, d, dv = 1, 2, 14, 4, 6
+    q = rng.normal(size=(B, H, N, d))
+    k = rng.normal(size=(B, H, N, d))
+    v = rng.normal(size=(B, H, N, dv))
+    alpha = rng.uniform(0.3, 1.0, size=(B, H, N, d))
+    for fm in ("none", "elu1"):
+        out = o.forward(q, k, v, fm=fm, alpha=alpha)
+        for h in range(H):
+            _close(out[0, h], gla_brute_force(q[0, h], k[0, h], v[0, h], alpha[0, h], fm),
+                   1e-12, 1e-12, f"per-channel decay head {h} ({fm})")
+    # a constant alpha is the scalar decay of the same value; alpha = 1 is none
+    gam = np.array([0.85, 0.55])
+    const = np.broadcast_to(gam[None, :, None, None], (B, H, N, d)).copy()
+    _close(o.forward(q, k, v, fm="none", alpha=const), o.forward(q, k, v, fm="none", gamma=gam),
+           0, 0, "constant alpha equals gamma")
+    _close(o.forward(q, k, v, alpha=np.ones((B, H, N, d))), o.forward(q, k, v), 0, 0,
+           "alpha = 1 equals no decay")
+    # the state: S = sum_j diag(prod_{s>j} alpha_s) phi(k_j) v_j^T
+    S, z = o.state(k, v, fm="elu1", alpha=alpha)
+    fk = lib_phi(k[0, 1])
+    w = np.ones((N, d))
+    for j in range(N):
+        for s_ in range(j + 1, N):
+            w[j] *= alpha[0, 1, s_]
+    _close(S[0, 1], (fk * w).T @ v[0, 1], 1e-12, 1e-12, "per-channel decayed state")
+    _close(z[0, 1], (fk * w).sum(axis=0), 1e-12, 1e-12, "per-channel decayed normaliser")
+    # decode continues it token by token
+    S0, z0 = o.state(k[:, :, :8], v[:, :, :8], fm="none", alpha=alpha[:, :, :8])
+    full = o.forward(q, k, v, fm="none", alpha=alpha)
+    for t in range(8, N):
+        ot, S0, z0 = o.decode_step(S0, z0, q[:, :, t], k[:, :, t], v[:, :, t], fm="none",
+                                   alpha=alpha[:, :, t])
+        _close(ot, full[:, :, t], 1e-12, 1e-12, f"per-channel decode step {t}")
+
+
+# ------------------------------------------------- random features --------
+def pin_favor(o):
+    """Positive random features estimate the exponential kernel without bias
+    ("Efficient Attention Variants" s.6): the mean of phi(q).phi(k) over many
+    Gaussian rows approaches exp(q.k / sqrt(d)), within a few standard errors
+    of the sample itself; every feature is positive."""
+    rng = np.random.default_rng(29)
+    d, r = 4, 200_000
+    q = np.array([0.7, -0.3, 0.5, 0.2])
+    k = np.array([0.4, 0.6, -0.2, 0.8])
+    w = rng.normal(size=(r, d))
+    fq, fk = o.favor(q[None], w)[0], o.favor(k[None], w)[0]
+    assert np.all(fq > 0) and np.all(fk > 0), "features must be positive"
+    prod = fq * fk * r          # one unbiased estimate per Gaussian row
+    est, se = prod.mean(), prod.std() / math.sqrt(r)
+    exact = math.exp(float(q @ k) / math.sqrt(d))
+    assert abs(est - exact) < 5 * se, (est, exact, se)
+    assert abs(fq @ fk - est) <= 1e-12 * est
+    # for given features the state form equals the explicit kernel matrix
+    Q = rng.normal(size=(9, d)) * 0.5
+    K = rng.normal(size=(9, d)) * 0.5
+    V = rng.normal(size=(9, 3))
+    w8 = rng.normal(size=(8, d))
+    FQ, FK = o.favor(Q, w8), o.favor(K, w8)
+    rec = o.forward(FQ[None, None], FK[None, None], V[None, None], fm="identity_norm")[0, 0]
+    _close(rec, brute_force(FQ, FK, V, fm="identity_norm"), 1e-12, 1e-12,
+           "random-feature state form vs explicit matrix")
+
+
 ALL_PINS = [
     pin_phi_library,
     pin_worked_example,
@@ -260,4 +379,7 @@ ALL_PINS = [
     pin_decay_dense,
     pin_additive_vs_normalised,
     pin_decode,
+    pin_initial_state,
+    pin_gla,
+    pin_favor,
 ]

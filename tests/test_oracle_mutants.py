@@ -16,6 +16,9 @@ PLANTS = [
     "ORC_PLANT_TRANSPOSED_UPDATE",   # key feature paired with the wrong value channel
     "ORC_PLANT_Z_NO_DECAY",          # normaliser left undecayed
     "ORC_PLANT_DROP_NORMALISER",     # division by phi(q)^T z dropped
+    "ORC_PLANT_GLA_ALONG_VALUES",    # per-channel decay applied along the values
+    "ORC_PLANT_IGNORE_Z0",           # the initial normaliser state dropped
+    "ORC_PLANT_FAVOR_NO_NORM",       # random features without the -|x|^2/2 term
 ]
 
 
