@@ -131,10 +131,41 @@ LA_API la_status la_forward(const void* q, const void* k, const void* v, float* 
                      la_stream_t stream);
 
 /*
+ * Causal forward continued from a given state and/or returning the final
+ * state: the prefill of a long prompt in pieces, and the hand-off of a
+ * prefill to la_decode_step at any point ("Efficient Attention Variants",
+ * sections 1 and 5: the fixed-size state S_t, z_t is the whole summary of
+ * the tokens before t).
+ *   S0 [B,H,d,dv], z0 [B,H,d] : fp32 state before the first token, or both
+ *                               NULL for S_0 = 0, z_0 = 0.  With decay, S0
+ *                               and z0 are decayed like any earlier token.
+ *   S_out, z_out              : fp32 buffers that receive the state after
+ *                               the last token, or both NULL.  They may be
+ *                               the same buffers as S0, z0 (in-place update).
+ *   out                       : [B,H,N,dv] outputs, or NULL together with q
+ *                               for a state-only call (then S_out is
+ *                               required).
+ * Every other argument is as for la_forward (causal form only); the
+ * workspace must hold la_forward_workspace_size(B, H, N, d, dv, 1, dtype)
+ * bytes.  With N = 0 the final state is S0, z0 (or zero).
+ */
+LA_API la_status la_forward_with_state(const void* q, const void* k, const void* v, float* out,
+                                       const float* S0, const float* z0, float* S_out,
+                                       float* z_out, int64_t B, int64_t H, int64_t N, int d,
+                                       int dv, int feature_map, const float* gamma, int dtype,
+                                       void* workspace, size_t workspace_bytes,
+                                       la_stream_t stream);
+
+/*
  * Diagnostic: the kernel path la_forward takes for these arguments --
- * "tcgen05" (the tensor-core single-pass kernel: bf16, d = dv = 64, causal,
- * no decay) or "simt" (CUDA cores, fp32, every other case); "invalid" for
- * arguments la_forward would reject.  has_decay: 1 if gamma will be non-NULL.
+ * "tcgen05" (the single-pass tensor-core kernel: bf16, d = dv = 64, causal,
+ * no decay), "tcgen05_chunked" (the chunked tensor-core path: bf16, d and dv
+ * in {64, 128}; decay only with LA_FM_NONE) or "simt" (CUDA cores, fp32,
+ * every other case); "invalid" for arguments la_forward would reject.
+ * has_decay: 1 if gamma will be non-NULL.  la_forward_with_state and
+ * la_state take the chunked tensor-core path wherever its sizes and dtype
+ * allow (la_state also with decay and a normalised map), else the CUDA-core
+ * path.
  */
 LA_API const char* la_forward_path(int64_t B, int64_t H, int64_t N, int d, int dv, int causal,
                                    int feature_map, int has_decay, int dtype);

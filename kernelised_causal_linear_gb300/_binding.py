@@ -51,6 +51,9 @@ _lib.la_state.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _i, _fp,
 _lib.la_decode_step.restype = _i
 _lib.la_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _i, _i, _fp, _i,
                                 _vp]
+_lib.la_forward_with_state.restype = _i
+_lib.la_forward_with_state.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
+                                       _i, _i, _i, _fp, _i, _vp, _sz, _vp]
 _lib.la_forward_noalloc.restype = _i
 _lib.la_forward_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _i, _i, _fp,
                                     _i, _vp]
@@ -169,6 +172,35 @@ def la_forward_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: t
                                    _fm(feature_map), gp, _dtype(q), _stream_handle(stream))
     _check(code, "la_forward_noalloc")
     return out
+
+
+def la_forward_with_state(q: torch.Tensor | None, k: torch.Tensor, v: torch.Tensor,
+                          out: torch.Tensor | None = None, *, S0: torch.Tensor | None = None,
+                          z0: torch.Tensor | None = None, S_out: torch.Tensor | None = None,
+                          z_out: torch.Tensor | None = None, return_state: bool = True,
+                          feature_map="elu1", gamma=None, workspace: torch.Tensor | None = None,
+                          stream=None):
+    """Causal forward continued from (S0, z0) [B,H,d,dv] / [B,H,d] (None: zero
+    state), returning (out, S_out, z_out).  q = None computes the final state
+    only (out is then None).  S_out / z_out may be S0 / z0 (in-place)."""
+    B, H, N, d = k.shape
+    dv = v.shape[-1]
+    if q is not None and out is None:
+        out = torch.empty((B, H, N, dv), dtype=torch.float32, device=k.device)
+    if return_state and S_out is None:
+        S_out = torch.empty((B, H, d, dv), dtype=torch.float32, device=k.device)
+        z_out = torch.empty((B, H, d), dtype=torch.float32, device=k.device)
+    need = la_forward_workspace_size(B, H, N, d, dv, True, k.dtype) if k.dtype in DTYPES else 0
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=k.device)
+    gp, _keep = _gamma_arg(gamma, H)
+    code = _lib.la_forward_with_state(
+        _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(out, "out"),
+        _dev_ptr(S0, "S0"), _dev_ptr(z0, "z0"), _dev_ptr(S_out, "S_out"), _dev_ptr(z_out, "z_out"),
+        B, H, N, d, dv, _fm(feature_map), gp, _dtype(k), _dev_ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(code, "la_forward_with_state")
+    return out, S_out, z_out
 
 
 def la_state(k: torch.Tensor, v: torch.Tensor, S: torch.Tensor | None = None,

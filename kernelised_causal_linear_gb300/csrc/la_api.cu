@@ -106,15 +106,58 @@ const char* la_status_string(la_status s)
     return "unknown la_status";
 }
 
-// Which kernel path serves a forward: the tcgen05 kernel where it applies,
-// else the CUDA-core path.
-static bool use_tc(int64_t N, int d, int dv, int causal, int has_decay, int dtype)
+// The kernel paths, in order of preference: the single-pass tcgen05 kernel
+// (bf16, d = dv = 64, causal, no decay, no state in or out), the chunked
+// tcgen05 path (bf16, d and dv in {64, 128}), the CUDA-core path.
+enum Path { PATH_TC = 0, PATH_TG = 1, PATH_SIMT = 2 };
+
+static Path choose_path(const FwdArgs& a)
+{
+    if (a.out && !a.S0 && !a.S_out && tc_forward_eligible(a))
+        return PATH_TC;
+    if (tg_eligible(a))
+        return PATH_TG;
+    return PATH_SIMT;
+}
+
+static FwdArgs probe_args(int64_t B, int64_t H, int64_t N, int d, int dv, int causal, int fm,
+                          int dtype, GammaTable* g, bool out, bool state)
 {
     FwdArgs a{};
-    GammaTable g{};
-    g.has_decay = has_decay;
-    a.N = N, a.d = d, a.dv = dv, a.causal = causal, a.dtype = dtype, a.gamma = &g;
-    return tc_forward_eligible(a);
+    a.B = B, a.H = H, a.N = N, a.d = d, a.dv = dv, a.causal = causal, a.fm = fm;
+    a.dtype = dtype, a.gamma = g;
+    // placeholders that only mark which results are wanted
+    a.out = out ? reinterpret_cast<float*>(uintptr_t(256)) : nullptr;
+    a.S_out = state ? reinterpret_cast<float*>(uintptr_t(256)) : nullptr;
+    return a;
+}
+
+static size_t path_workspace(const FwdArgs& a, Path path)
+{
+    switch (path) {
+    case PATH_TC: return tc_forward_workspace(a.B * a.H, a.N);
+    case PATH_TG: return tg_workspace(a.B * a.H, a.N, a.d, a.dv, a.fm, a.causal);
+    default:
+        return a.out ? simt_forward_workspace(a.B * a.H, a.N, a.d, a.dv, a.causal)
+                     : simt_state_workspace(a.B * a.H, a.N, a.d, a.dv);
+    }
+}
+
+// Workspace that covers every path a call with these sizes may take (the
+// feature map and the decay are not known here).
+static size_t max_workspace(int64_t B, int64_t H, int64_t N, int d, int dv, int causal,
+                            int dtype, bool out, bool state)
+{
+    size_t n = 0;
+    for (int fm = 0; fm < 3; ++fm)
+        for (int decay = 0; decay < 2; ++decay) {
+            GammaTable g{};
+            g.has_decay = decay;
+            const FwdArgs a = probe_args(B, H, N, d, dv, causal, fm, dtype, &g, out, state);
+            const size_t w = path_workspace(a, choose_path(a));
+            n = w > n ? w : n;
+        }
+    return n;
 }
 
 size_t la_forward_workspace_size(int64_t B, int64_t H, int64_t N, int d, int dv, int causal,
@@ -122,9 +165,12 @@ size_t la_forward_workspace_size(int64_t B, int64_t H, int64_t N, int d, int dv,
 {
     if (check_sizes(B, H, N, d, dv, LA_FM_ELU1, dtype) != LA_OK || N == 0)
         return 0;
-    size_t n = simt_forward_workspace(B * H, N, d, dv, causal);
-    if (use_tc(N, d, dv, causal, 0, dtype))  // gamma unknown here: cover both paths
-        n = n > tc_forward_workspace(B * H, N) ? n : tc_forward_workspace(B * H, N);
+    // the forward alone, and with states in or out (causal only)
+    size_t n = max_workspace(B, H, N, d, dv, causal, dtype, true, false);
+    if (causal) {
+        const size_t w = max_workspace(B, H, N, d, dv, causal, dtype, true, true);
+        n = w > n ? w : n;
+    }
     return n;
 }
 
@@ -133,14 +179,35 @@ const char* la_forward_path(int64_t B, int64_t H, int64_t N, int d, int dv, int 
 {
     if (check_sizes(B, H, N, d, dv, feature_map, dtype) != LA_OK)
         return "invalid";
-    return use_tc(N, d, dv, causal, has_decay, dtype) ? "tcgen05" : "simt";
+    GammaTable g{};
+    g.has_decay = has_decay;
+    const FwdArgs a = probe_args(B, H, N, d, dv, causal, feature_map, dtype, &g, true, false);
+    switch (choose_path(a)) {
+    case PATH_TC: return "tcgen05";
+    case PATH_TG: return "tcgen05_chunked";
+    default: return "simt";
+    }
 }
 
 size_t la_state_workspace_size(int64_t B, int64_t H, int64_t N, int d, int dv, int dtype)
 {
-    if (check_sizes(B, H, N, d, dv, LA_FM_ELU1, dtype) != LA_OK)
+    if (check_sizes(B, H, N, d, dv, LA_FM_ELU1, dtype) != LA_OK || N == 0)
         return 0;
-    return simt_state_workspace(B * H, N, d, dv);
+    return max_workspace(B, H, N, d, dv, 1, dtype, false, true);
+}
+
+// Runs a validated forward and/or state request on its path.
+static la_status run_path(const FwdArgs& a)
+{
+    const Path path = choose_path(a);
+    const size_t need = path_workspace(a, path);
+    if (!a.ws || a.ws_bytes < need || !aligned256(a.ws))
+        return LA_ERR_WORKSPACE;
+    switch (path) {
+    case PATH_TC: return from_cuda(tc_forward(a));
+    case PATH_TG: return from_cuda(tg_run(a));
+    default: return from_cuda(a.out ? simt_forward(a) : simt_state(a));
+    }
 }
 
 la_status la_forward(const void* q, const void* k, const void* v, float* out, int64_t B,
@@ -172,12 +239,58 @@ la_status la_forward(const void* q, const void* k, const void* v, float* out, in
     a.ws = workspace, a.ws_bytes = workspace_bytes;
     a.status = status_ptr();
     a.stream = reinterpret_cast<cudaStream_t>(stream);
-    const bool tc = tc_forward_eligible(a);
-    const size_t need = tc ? tc_forward_workspace(B * H, N)
-                           : simt_forward_workspace(B * H, N, d, dv, causal);
-    if (!workspace || workspace_bytes < need || !aligned256(workspace))
-        return LA_ERR_WORKSPACE;
-    return from_cuda(tc ? tc_forward(a) : simt_forward(a));
+    return run_path(a);
+}
+
+la_status la_forward_with_state(const void* q, const void* k, const void* v, float* out,
+                                const float* S0, const float* z0, float* S_out, float* z_out,
+                                int64_t B, int64_t H, int64_t N, int d, int dv, int feature_map,
+                                const float* gamma, int dtype, void* workspace,
+                                size_t workspace_bytes, la_stream_t stream)
+{
+    la_status st = check_sizes(B, H, N, d, dv, feature_map, dtype);
+    if (st != LA_OK)
+        return st;
+    GammaTable gt;
+    if ((st = make_gamma(gamma, H, &gt)) != LA_OK)
+        return st;
+    if (!S0 != !z0 || !S_out != !z_out || (!out && !S_out) || (!q != !out))
+        return LA_ERR_INVALID_ARG;
+    if ((S0 && (!aligned16(S0) || !aligned16(z0))) ||
+        (S_out && (!aligned16(S_out) || !aligned16(z_out))))
+        return LA_ERR_INVALID_ARG;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (N == 0) {  // no tokens: the final state is the initial one
+        if (!S_out)
+            return LA_OK;
+        const size_t sb = sizeof(float) * (size_t)(B * H) * d * dv;
+        const size_t zb = sizeof(float) * (size_t)(B * H) * d;
+        cudaError_t e;
+        if (S0) {
+            e = S0 == S_out ? cudaSuccess : cudaMemcpyAsync(S_out, S0, sb, cudaMemcpyDeviceToDevice, cs);
+            if (e == cudaSuccess && z0 != z_out)
+                e = cudaMemcpyAsync(z_out, z0, zb, cudaMemcpyDeviceToDevice, cs);
+        } else {
+            e = cudaMemsetAsync(S_out, 0, sb, cs);
+            if (e == cudaSuccess)
+                e = cudaMemsetAsync(z_out, 0, zb, cs);
+        }
+        return from_cuda(e);
+    }
+    if (!k || !v || !aligned16(k) || !aligned16(v))
+        return LA_ERR_INVALID_ARG;
+    if (out && (!aligned16(q) || !aligned16(out)))
+        return LA_ERR_INVALID_ARG;
+    FwdArgs a{};
+    a.q = q, a.k = k, a.v = v, a.out = out;
+    a.B = B, a.H = H, a.N = N, a.d = d, a.dv = dv;
+    a.causal = 1, a.fm = feature_map, a.dtype = dtype;
+    a.gamma = &gt;
+    a.ws = workspace, a.ws_bytes = workspace_bytes;
+    a.S0 = S0, a.z0 = z0, a.S_out = S_out, a.z_out = z_out;
+    a.status = status_ptr();
+    a.stream = cs;
+    return run_path(a);
 }
 
 la_status la_state(const void* k, const void* v, float* S, float* z, int64_t B, int64_t H,
@@ -201,10 +314,6 @@ la_status la_state(const void* k, const void* v, float* S, float* z, int64_t B, 
     }
     if (!k || !v || !aligned16(k) || !aligned16(v))
         return LA_ERR_INVALID_ARG;
-    const size_t need = simt_state_workspace(B * H, N, d, dv);
-    if (!workspace || workspace_bytes < need || !aligned256(workspace))
-        return LA_ERR_WORKSPACE;
-
     FwdArgs a{};
     a.k = k, a.v = v;
     a.B = B, a.H = H, a.N = N, a.d = d, a.dv = dv;
@@ -214,7 +323,7 @@ la_status la_state(const void* k, const void* v, float* S, float* z, int64_t B, 
     a.S_out = S, a.z_out = z;
     a.status = status_ptr();
     a.stream = cs;
-    return from_cuda(simt_state(a));
+    return run_path(a);
 }
 
 la_status la_decode_step(float* S, float* z, const void* q, const void* k, const void* v,

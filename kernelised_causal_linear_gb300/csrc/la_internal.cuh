@@ -2,6 +2,7 @@
 // liblinattn.so (not part of the public ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -80,8 +81,10 @@ struct FwdArgs {
     GammaTable* gamma;  // host copy; passed by value to kernels
     void* ws;
     size_t ws_bytes;
-    float* S_out;       // la_state: final state (else NULL)
-    float* z_out;
+    float* S_out;       // final state [B,H,d,dv] (else NULL)
+    float* z_out;       // final normaliser state [B,H,d] (else NULL)
+    const float* S0;    // state before the first token [B,H,d,dv] (else NULL = 0)
+    const float* z0;
     int* status;        // device status word
     cudaStream_t stream;
 };
@@ -95,6 +98,20 @@ cudaError_t simt_state(const FwdArgs& a);
 bool tc_forward_eligible(const FwdArgs& a);
 size_t tc_forward_workspace(int64_t BH, int64_t N);
 cudaError_t tc_forward(const FwdArgs& a);
+
+// tcgen05 chunkwise path (bf16, d and dv in {64, 128}): segment aggregates,
+// scan, outputs.  Serves forwards (a.out), final states (a.S_out) and initial
+// states (a.S0); decay only with the unnormalised map when outputs are wanted.
+bool tg_eligible(const FwdArgs& a);
+size_t tg_workspace(int64_t BH, int64_t N, int d, int dv, int fm, int causal);
+cudaError_t tg_run(const FwdArgs& a);
+
+// A 3D TMA descriptor over a bf16 tensor [depth][rows][cols] (row-major),
+// boxes of 128 rows x 64 columns with the 128-byte swizzle.
+bool tma_map_bf16_3d(CUtensorMap* m, const void* base, int64_t cols, int64_t rows,
+                     int64_t depth);
+// Streaming multiprocessors of the current device (0 if unknown).
+int device_sm_count();
 
 struct DecodeArgs {
     float* S;

@@ -119,11 +119,15 @@ __global__ void __launch_bounds__(kThreads)
 
 // ---------------------------------------------------------------- step 2 ---
 // mode 0: exclusive prefix over the blocks of each sequence, in place.
-// mode 1: total only, written to tot_S [BH][D*DV] and tot_z [BH][D]
-//         (tot_z == NULL: packed into tot_S as [BH][D*DV + D]).
+// mode 1: no prefix is written.
+// The prefix starts from init_S [BH][D*DV] / init_z [BH][D] (the state before
+// the first token) or from zero; the total, if tot_S is given, is written to
+// tot_S [BH][D*DV] and tot_z [BH][D] (tot_z == NULL: packed into tot_S as
+// [BH][D*DV + D]).
 __global__ void __launch_bounds__(kThreads)
     k_block_scan(float* __restrict__ ws, int nblk, int64_t N, int H, int D, int DV, int mode,
-                 GammaTable g, float* __restrict__ tot_S, float* __restrict__ tot_z)
+                 GammaTable g, const float* init_S, const float* init_z, float* tot_S,
+                 float* tot_z)
 {
     const int E = D * DV + D;
     const int per_seq = (E + kThreads - 1) / kThreads;
@@ -134,6 +138,8 @@ __global__ void __launch_bounds__(kThreads)
     const int head = (int)(seq % H);
     float* base = ws + seq * (int64_t)nblk * E + e;
     float acc = 0.f;
+    if (init_S)
+        acc = e < D * DV ? init_S[seq * (int64_t)(D * DV) + e] : init_z[seq * (int64_t)D + (e - D * DV)];
     constexpr int kBatch = 16;  // independent loads in flight per thread
     for (int b0 = 0; b0 < nblk; b0 += kBatch) {
         float x[kBatch];
@@ -151,7 +157,7 @@ __global__ void __launch_bounds__(kThreads)
             }
         }
     }
-    if (mode == 1) {
+    if (tot_S) {
         if (!tot_z)
             tot_S[seq * (int64_t)E + e] = acc;
         else if (e < D * DV)
@@ -355,17 +361,17 @@ cudaError_t run_forward(const FwdArgs& a, bool state_only)
     const unsigned scan_grid = (unsigned)(BH * per_seq);
     if (state_only) {
         k_block_scan<<<scan_grid, kThreads, 0, a.stream>>>(ws, nblk, a.N, H, D, DV, 1, *a.gamma,
-                                                          a.S_out, a.z_out);
+                                                          a.S0, a.z0, a.S_out, a.z_out);
         count_launches(1);
         return cudaGetLastError();
     }
     float* tot = ws + BH * (int64_t)nblk * E;  // non-causal totals [BH][E]
     if (a.causal)
         k_block_scan<<<scan_grid, kThreads, 0, a.stream>>>(ws, nblk, a.N, H, D, DV, 0, *a.gamma,
-                                                          nullptr, nullptr);
+                                                          a.S0, a.z0, a.S_out, a.z_out);
     else
         k_block_scan<<<scan_grid, kThreads, 0, a.stream>>>(ws, nblk, a.N, H, D, DV, 1, *a.gamma,
-                                                          tot, nullptr);
+                                                          nullptr, nullptr, tot, nullptr);
     count_launches(1);
     err = cudaGetLastError();
     if (err != cudaSuccess)

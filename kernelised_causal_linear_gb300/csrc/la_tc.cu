@@ -73,11 +73,13 @@
 
 #include "la_internal.cuh"
 #include "la_sm100.cuh"
+#include "la_tc_common.cuh"
 
 namespace la {
 namespace {
 
 using namespace sm100;
+using namespace tcc;
 
 constexpr int kC = 128;        // tokens per chunk
 constexpr int kD = 64;         // d = dv
@@ -169,37 +171,6 @@ __device__ unsigned long long* g_tc_trace;
     } while (0)
 #endif
 
-__device__ __forceinline__ uint64_t globaltimer()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void st_release(unsigned* p, unsigned v)
-{
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p)
-{
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Drop a 128-byte L2 line without writing it back (scratch read for the last
-// time).
-__device__ __forceinline__ void l2_discard(const void* ptr)
-{
-    asm volatile("discard.global.L2 [%0], 128;" ::"l"(ptr) : "memory");
-}
-
-__device__ __forceinline__ void named_bar(int id, int count)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // Bounded wait that also gives up as soon as another role has aborted.  The
 // first test is inline; the sleeping loop is one shared out-of-line copy.
 __device__ __noinline__ bool bwait_slow(uint64_t* bar, uint32_t parity, volatile int* abort)
@@ -227,20 +198,6 @@ __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile i
     return mbar_test_wait(bar, parity) || bwait_slow(bar, parity, abort);
 }
 
-// A thread group waits through one leader; bar.red hands every thread the
-// same verdict, so the group never splits on an abort.
-__device__ __forceinline__ bool group_ok(int ok, int barid, int count)
-{
-    int res;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %1, 0;\n\t"
-        "bar.red.and.pred p, %2, %3, p;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(res)
-        : "r"(ok), "r"(barid), "r"(count)
-        : "memory");
-    return res != 0;
-}
-
 // Bounded wait used only while draining (ignores the abort flag).
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity)
 {
@@ -248,85 +205,6 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity)
     while (!mbar_try_wait(bar, parity))
         if (globaltimer() - t0 > kWaitNs)
             return;
-}
-
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Packed fp32 pair arithmetic (two lanes of work per instruction).
-__device__ __forceinline__ float2 sub2(float2 a, float2 b)
-{
-    float2 r;
-    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
-        "sub.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return r;
-}
-
-// split two fp32 into packed bf16 hi and lo parts (hi + lo = x to ~2^-17)
-__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo)
-{
-    hi = pack_bf16x2(a, b);
-    const float2 r = sub2(make_float2(a, b), make_float2(bf_lo(hi), bf_hi(hi)));
-    lo = pack_bf16x2(r.x, r.y);
-}
-
-__device__ __forceinline__ float2 mul2(float2 a, float2 b)
-{
-    float2 r;
-    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
-        "mul.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return r;
-}
-
-__device__ __forceinline__ float ex2(float t)
-{
-    float r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
-    return r;
-}
-
-// elu(x)+1 on two packed bf16: max(x,0) + exp(min(x,0)), with
-// exp(u) = 2^(u log2 e) on the hardware base-2 exponential.  For every
-// element one of the two terms is exactly 0 or 1, so the packed bf16 sum of
-// max(x,0) and the rounded exponential is the fp32 value rounded once.
-__device__ __forceinline__ uint32_t phi2(uint32_t w)
-{
-    uint32_t mn, mx, r;
-    asm("min.bf16x2 %0, %1, %2;" : "=r"(mn) : "r"(w), "r"(0u));
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(mx) : "r"(w), "r"(0u));
-    const float2 t = mul2(make_float2(bf_lo(mn), bf_hi(mn)),
-                          make_float2(1.4426950408889634f, 1.4426950408889634f));
-    const uint32_t e = pack_bf16x2(ex2(t.x), ex2(t.y));
-    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(mx), "r"(e));
-    return r;
-}
-
-// Feature map in place on a 128 x 64 bf16 tile (128-byte swizzle) by 128
-// threads; rows >= valid become zero.
-__device__ __forceinline__ void phi_tile(unsigned char* tile, int t, int valid, bool elu)
-{
-    const int cc = t & 7, r0 = t >> 3;
-#pragma unroll 2
-    for (int mm = 0; mm < 8; mm += 2) {
-        uint4 x[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u)
-            x[u] = *reinterpret_cast<const uint4*>(tile + sw128_off(r0 + 16 * (mm + u), cc));
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int r = r0 + 16 * (mm + u);
-            if (r >= valid)
-                x[u] = make_uint4(0, 0, 0, 0);
-            else if (elu)
-                x[u] = make_uint4(phi2(x[u].x), phi2(x[u].y), phi2(x[u].z), phi2(x[u].w));
-            if (r >= valid || elu)
-                *reinterpret_cast<uint4*>(tile + sw128_off(r, cc)) = x[u];
-        }
-    }
 }
 
 // D (+)= [V | e]^T phi(K) over one 128-token stage: V at vaddr and phi(K) at
@@ -1332,6 +1210,13 @@ cudaError_t tc_forward(const FwdArgs& a)
     count_launches(1);
     return cudaGetLastError();
 }
+
+bool tma_map_bf16_3d(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t depth)
+{
+    return make_map(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cols, rows, depth, 64);
+}
+
+int device_sm_count() { return sm_count(); }
 
 #ifdef LA_TC_TRACE
 extern "C" __attribute__((visibility("default"))) int la_debug_set_tc_trace(void* buf)

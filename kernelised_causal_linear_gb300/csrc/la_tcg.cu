@@ -1,0 +1,1539 @@
+// la_tcg.cu -- general chunkwise path on the tcgen05 tensor cores:
+// bf16 q/k/v with d, dv in {64, 128}; causal or not; any feature map; the
+// scalar per-head decay (with the unnormalised map); an initial state; the
+// final state.
+//
+// The sequence is cut into chunks of C = 128 tokens and the chunks into
+// segments of L chunks ("Efficient Attention Variants", section 8: parallel
+// inside a chunk, a state carried between chunks; "Linear Attention and SSM",
+// eq. attn-linssm-ssd: inside a chunk the output is the masked form
+// ((phi(Q) phi(K)^T) o L) V, with L_ij = gamma^(i-j) for i >= j).  Three
+// launches:
+//
+//   1. k_tg_state   the aggregate of every segment g of tokens [T0, T1):
+//                     U_g = sum_t gamma^(T1-1-t) phi(k_t) [v_t | 1]^T
+//                   on the tensor cores, accumulated over the segment's
+//                   chunks in tensor memory ("Linear Attention Kernel",
+//                   section "Rewrite: associativity": phi(K)^T V is the only
+//                   intermediate).
+//   2. k_tg_scan    per sequence, in fp32: P_0 = S_0 (the initial state, or
+//                   0), P_{g+1} = gamma^(T1-T0) P_g + U_g.  P_g is the state
+//                   before segment g ("Efficient Attention Variants",
+//                   section 5: S_t, z_t summarise the prefix); it is written
+//                   as the bf16 hi/lo operand image that step 3 loads, and the
+//                   total P_nseg is the final state.  The non-causal form uses
+//                   the total for every query (same page, section 4).
+//   3. k_tg_out     the outputs of one segment and one 64-channel tile of the
+//                   values per work item, chunk after chunk:
+//                     scores = phi(Q_c) phi(K_c)^T                  (tensor cores)
+//                     P      = scores o L                            (CUDA cores)
+//                     inter  = phi(Q_c) [S^T; z]   intra = P [V_c | 1]  (tensor cores)
+//                     o_i    = (g_i inter_i + intra_i) / (g_i den_i + rowsum_i)
+//                   with g_i = gamma^(i+1) (o unnormalised for the RetNet
+//                   map), then the state for the next chunk,
+//                     S <- gamma^C S + dS_c,  dS_c^T = [V'_c | 1]^T phi(K_c),
+//                   V'_c = diag(gamma^(C-1-t)) V_c, on the tensor cores, added
+//                   to the operand image in shared memory.
+//
+// Every fp32 quantity that enters a bf16 MMA (P, the state, the decayed
+// values) is split into a bf16 hi/lo pair (two MMAs, ~2^-17 relative); phi(Q)
+// and phi(K) are rounded once to bf16; accumulators, states and denominators
+// are fp32.  The ones column of [V | 1] gives the row sums of P and the
+// normaliser increments on the same MMAs.
+//
+// Decay together with a normalised feature map is not taken by this path
+// (the caller routes it to the CUDA-core path).
+#include <cudaTypedefs.h>
+#include <algorithm>
+#include <float.h>
+#include <string.h>
+
+#include "la_internal.cuh"
+#include "la_sm100.cuh"
+#include "la_tc_common.cuh"
+
+namespace la {
+namespace {
+
+using namespace sm100;
+using namespace tcc;
+
+constexpr int kC = 128;        // tokens per chunk
+constexpr int kT = 64;         // value channels per output tile
+constexpr uint64_t kWaitNs = 2000000000ull;  // any single wait gives up after 2 s
+
+// Rows of the [S^T; z] operand image of one value tile: 64 value channels,
+// then (normalised maps) the normaliser row and 15 rows of zeros.
+__host__ __device__ constexpr int img_rows(bool norm) { return norm ? 80 : 64; }
+
+// ------------------------------------------------------------ waits --------
+__device__ __noinline__ bool tg_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort)
+{
+    uint64_t t0 = 0;
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u))
+            return true;
+        if ((n & 3u) == 0u) {
+            if (*abort)
+                return false;
+            const uint64_t now = globaltimer();
+            if (!t0)
+                t0 = now;
+            else if (now - t0 > kWaitNs) {
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait for phase `parity` of `bar`; false on timeout or abort.
+__device__ __forceinline__ bool tg_wait(uint64_t* bar, uint32_t parity, volatile int* abort)
+{
+    return mbar_test_wait(bar, parity) || tg_wait_slow(bar, parity, abort);
+}
+
+// Bounded wait used while draining after an abort.
+__device__ __forceinline__ void tg_drain(uint64_t* bar, uint32_t parity)
+{
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer() - t0 > kWaitNs)
+            return;
+}
+
+// ------------------------------------------------ descriptor helpers -------
+// K-major operand of `nblk` 64-element column blocks (128-byte swizzle), each
+// block `rows` x 128 bytes; descriptor for K step kk (16 elements).
+__device__ __forceinline__ uint64_t kdesc(uint32_t base, int rows, int kk)
+{
+    return sdesc_sw128(base + (uint32_t)(kk >> 2) * (uint32_t)rows * 128u + (uint32_t)(kk & 3) * 32u,
+                       16, 1024);
+}
+
+// MN-major operand of 128 tokens (K) x 128 (M or N) made of two 64-element
+// blocks: `first` holds elements 0..63, `second` 64..127.  A block flagged
+// constant is one 2 KiB block of 16 rows reused for every K step; otherwise
+// it is a 128-row tile whose K step kk starts 2 KiB further.  Both must
+// leave `second` above `first` in shared memory.
+__device__ __forceinline__ uint64_t mndesc(uint32_t first, bool first_const, uint32_t second,
+                                           bool second_const, int kk)
+{
+    const uint32_t a = first + (first_const ? 0u : (uint32_t)kk * 2048u);
+    const uint32_t b = second + (second_const ? 0u : (uint32_t)kk * 2048u);
+    return sdesc_sw128(a, b - a, 1024);
+}
+
+// fp32 x -> bf16 hi/lo parts of 8 consecutive values (4 packed words each).
+__device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo)
+{
+    split2(x[0], x[1], hi.x, lo.x);
+    split2(x[2], x[3], hi.y, lo.y);
+    split2(x[4], x[5], hi.z, lo.z);
+    split2(x[6], x[7], hi.w, lo.w);
+}
+
+__device__ __forceinline__ void unpack8(uint4 w, float* x)
+{
+    x[0] = bf_lo(w.x), x[1] = bf_hi(w.x), x[2] = bf_lo(w.y), x[3] = bf_hi(w.y);
+    x[4] = bf_lo(w.z), x[5] = bf_hi(w.z), x[6] = bf_lo(w.w), x[7] = bf_hi(w.w);
+}
+
+// The constant 2 KiB blocks: Z all zero; E with element 0 of each of its 16
+// rows equal to 1 (128-byte swizzle: 16-byte chunk 0 of row r sits at chunk
+// r & 7).  128 threads.
+__device__ __forceinline__ void init_const_blocks(unsigned char* z, unsigned char* e, int t)
+{
+    const int r = t >> 3, c = t & 7;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(z + r * 128 + c * 16) = w;
+    if (c == (r & 7))
+        w.x = 0x3F80u;  // bf16 1.0 in the low half
+    *reinterpret_cast<uint4*>(e + r * 128 + c * 16) = w;
+}
+
+// Rows of a chunk that hold tokens (the last chunk of a sequence is short).
+__device__ __forceinline__ int chunk_valid(int64_t N, int c)
+{
+    return (int)min((int64_t)kC, N - (int64_t)c * kC);
+}
+
+// ======================================================================
+// 1. segment aggregates
+// ======================================================================
+struct StParams {
+    CUtensorMap mk, mv;  // k [BH][N][D], v [BH][N][DV], boxes of 128 rows x 64 columns
+    int64_t N;
+    int BH, H;
+    int nchunk, L, nseg;
+    int elu, zsum, decay;  // zsum: also the normaliser increments
+    // stage layout (bytes from the stage start): phi(K) hi blocks at 0, phi(K)
+    // lo blocks at off_klo (elu), V blocks at off_v, decayed-V lo blocks at
+    // off_vlo (decay); nst stages of `stage` bytes
+    uint32_t off_klo, off_v, off_vlo, stage;
+    int nst;
+    float* U;  // [BH][nseg][DV*D + D]: S^T (row c = value channel c, D features), then z
+    GammaTable g;
+    int* status;
+};
+
+constexpr uint32_t kStStageBudget = 200 * 1024;  // shared memory for the K, V stages
+
+template <int D, int DV>
+struct StLayout {
+    static constexpr int KB = D / 64, VB = DV / 64;             // 64-column blocks
+    static constexpr uint32_t OFF_ZB = 0, OFF_EB = 2048;        // Z, E below the stages
+    static constexpr uint32_t OFF_ST = 4096;
+    // Z, E above the stages, then the barriers: offsets from the end of the stages
+    static constexpr uint32_t TAIL = 2048 + 2048 + 1024;
+    static constexpr uint32_t SMEM_MAX = OFF_ST + kStStageBudget + TAIL + 1024;
+    // tensor memory: per value tile 64 columns of [dS^T]; for D = 128 the
+    // normaliser increments in 64 more columns
+    static constexpr uint32_t COLS_USED = VB * 64 + (D == 128 ? 64 : 0);
+    static constexpr uint32_t TMEM_COLS = COLS_USED <= 32 ? 32 : COLS_USED <= 64 ? 64
+                                        : COLS_USED <= 128 ? 128 : COLS_USED <= 256 ? 256 : 512;
+    static_assert(SMEM_MAX <= 232448, "shared memory");
+};
+
+// elu(x)+1 of a 128 x 64 bf16 block in fp32, split into bf16 hi (in place)
+// and lo parts; rows >= valid become zero.  128 threads: thread t takes
+// 16-byte chunk t & 7 of rows t/8 + 16 m.
+__device__ __forceinline__ void phi_split_block(unsigned char* hi, unsigned char* lo, int t,
+                                                int valid)
+{
+    const int cc = t & 7, r0 = t >> 3;
+#pragma unroll 2
+    for (int mm = 0; mm < 8; ++mm) {
+        const int r = r0 + 16 * mm;
+        const uint32_t off = sw128_off(r, cc);
+        uint4 h = make_uint4(0, 0, 0, 0), l = h;
+        if (r < valid) {
+            float x[8];
+            unpack8(*reinterpret_cast<const uint4*>(hi + off), x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                x[e] = x[e] > 0.f ? x[e] + 1.0f : ex2(x[e] * 1.4426950408889634f);
+            split8(x, h, l);
+        }
+        *reinterpret_cast<uint4*>(hi + off) = h;
+        *reinterpret_cast<uint4*>(lo + off) = l;
+    }
+}
+
+struct StMisc {
+    uint64_t full[4], prep[4], free_[4], accd, accfree, drain;  // at most 4 stages
+    uint32_t tmem;
+    int abort;
+};
+
+// Decayed copy of a 128 x 64 value block for the state MMA: row t is scaled
+// by w_t and split into bf16 hi (written back in place) and lo parts.  Thread
+// t owns row t.
+__device__ __forceinline__ void decay_block(unsigned char* v, unsigned char* vlo, int t, float w)
+{
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint32_t off = sw128_off(t, c);
+        float x[8];
+        unpack8(*reinterpret_cast<const uint4*>(v + off), x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            x[e] *= w;
+        uint4 hi, lo;
+        split8(x, hi, lo);
+        *reinterpret_cast<uint4*>(v + off) = hi;
+        *reinterpret_cast<uint4*>(vlo + off) = lo;
+    }
+}
+
+template <int D, int DV>
+__global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StParams p)
+{
+    using LY = StLayout<D, DV>;
+    constexpr int KB = LY::KB, VB = LY::VB;
+    const int NST = p.nst;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t OFF_ZT = LY::OFF_ST + (uint32_t)NST * p.stage, OFF_ET = OFF_ZT + 2048;
+    StMisc* m = reinterpret_cast<StMisc*>(sm + OFF_ET + 2048);
+    volatile int* abort = &m->abort;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int items = p.BH * p.nseg;
+
+    if (tid == 0) {
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&m->full[i], 1);
+            mbar_init(&m->prep[i], 1);
+            mbar_init(&m->free_[i], 1);
+        }
+        mbar_init(&m->accd, 1);
+        mbar_init(&m->accfree, 1);
+        mbar_init(&m->drain, 1);
+        m->abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&p.mk);
+        tma_prefetch_desc(&p.mv);
+    }
+    if (tid < 128) {
+        init_const_blocks(sm + LY::OFF_ZB, sm + LY::OFF_EB, tid);
+        init_const_blocks(sm + OFF_ZT, sm + OFF_ET, tid);
+    }
+    fence_proxy_async_smem();
+    if (warp == 0) {
+        tmem_alloc(&m->tmem, LY::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = m->tmem;
+    auto stage = [&](int s) { return sm + LY::OFF_ST + (uint32_t)s * p.stage; };
+
+    if (warp == 0) {
+        // ---------------------------------------------- producer ----------
+        if ((tid & 31) == 0) {
+            const uint64_t stream = policy_evict_first();
+            int u = 0;
+            int last_ph[4] = {-1, -1, -1, -1};
+            bool ok = true;
+            for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+                const int s = it / p.nseg, g = it % p.nseg;
+                const int c0 = g * p.L, n = min(p.L, p.nchunk - c0);
+                for (int k = 0; k < n; ++k, ++u) {
+                    const int st = u % NST;
+                    if (u >= NST && !tg_wait(&m->free_[st], ((u / NST) & 1) ^ 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    unsigned char* b = stage(st);
+                    mbar_arrive_expect_tx(&m->full[st], (uint32_t)(KB + VB) * 16384u);
+                    const int row = (c0 + k) * kC;
+                    for (int kb = 0; kb < KB; ++kb)
+                        tma_load_3d(b + kb * 16384, &p.mk, 64 * kb, row, s, &m->full[st], stream);
+                    for (int vb = 0; vb < VB; ++vb)
+                        tma_load_3d(b + p.off_v + vb * 16384, &p.mv, 64 * vb, row, s,
+                                    &m->full[st], stream);
+                    last_ph[st] = (u / NST) & 1;
+                }
+            }
+            if (!ok)
+                for (int i = 0; i < NST; ++i)
+                    if (last_ph[i] >= 0)
+                        tg_drain(&m->full[i], last_ph[i]);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------ MMA issuer -----------
+        if ((tid & 31) == 0) {
+            const uint32_t id64 = idesc_bf16_f32(128, 64, true, true);
+            const uint32_t zb = smem_addr(sm + LY::OFF_ZB), eb = smem_addr(sm + LY::OFF_EB);
+            const uint32_t zt = smem_addr(sm + OFF_ZT), et = smem_addr(sm + OFF_ET);
+            const int nk = p.elu ? 2 : 1, nv = p.decay ? 2 : 1;
+            const bool dz_mma = p.zsum && !p.decay;  // else the CUDA cores sum dz
+            int u = 0, j = 0;
+            bool ok = true, issued = false;
+            for (int it = blockIdx.x; ok && it < items; it += gridDim.x, ++j) {
+                const int g = it % p.nseg;
+                const int n = min(p.L, p.nchunk - g * p.L);
+                // the previous item's aggregate has been read out
+                if (j > 0 && !tg_wait(&m->accfree, (j - 1) & 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                for (int k = 0; k < n; ++k, ++u) {
+                    const int st = u % NST;
+                    if (!tg_wait(&m->prep[st], (u / NST) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t b = smem_addr(stage(st));
+                    // [dS^T] += [V' | x]^T phi(K) over the hi/lo parts of V'
+                    // (decay) and of phi(K) (elu); accumulate from the item's
+                    // first MMA on
+                    for (int h = 0; h < VB; ++h) {
+                        const uint32_t d = tm + (uint32_t)h * 64u;
+                        for (int pv = 0; pv < nv; ++pv)
+                            for (int pk = 0; pk < nk; ++pk) {
+                                const uint32_t vsrc = b + (pv ? p.off_vlo : p.off_v) + h * 16384u;
+                                const uint32_t ksrc = b + (pk ? p.off_klo : 0u);
+                                const bool acc0 = k > 0 || pv > 0 || pk > 0;
+                                if (D == 64) {
+                                    // lanes 0..63: dS^T; lane 64: dz (E) or nothing (Z)
+                                    const uint32_t x = dz_mma && h == 0 && pv == 0 ? et : zt;
+                                    for (int kk = 0; kk < 8; ++kk)
+                                        mma_bf16_ss(d, mndesc(vsrc, false, x, true, kk),
+                                                    sdesc_sw128(ksrc + kk * 2048, 16, 1024), id64,
+                                                    acc0 || kk > 0);
+                                } else {
+                                    // feature block 0 -> lanes 0..63, block 1 -> 64..127
+                                    for (int kk = 0; kk < 8; ++kk)
+                                        mma_bf16_ss(d, mndesc(vsrc, false, zt, true, kk),
+                                                    sdesc_sw128(ksrc + kk * 2048, 16, 1024), id64,
+                                                    acc0 || kk > 0);
+                                    for (int kk = 0; kk < 8; ++kk)
+                                        mma_bf16_ss(d, mndesc(zb, true, vsrc, false, kk),
+                                                    sdesc_sw128(ksrc + 16384 + kk * 2048, 16, 1024),
+                                                    id64, 1);
+                                }
+                            }
+                    }
+                    if (D == 128 && dz_mma) {
+                        // dz: lane 0 <- features 0..63, lane 64 <- features 64..127
+                        const uint32_t d = tm + (uint32_t)VB * 64u;
+                        for (int pk = 0; pk < nk; ++pk) {
+                            const uint32_t ksrc = b + (pk ? p.off_klo : 0u);
+                            for (int kk = 0; kk < 8; ++kk)
+                                mma_bf16_ss(d, mndesc(eb, true, zt, true, kk),
+                                            sdesc_sw128(ksrc + kk * 2048, 16, 1024), id64,
+                                            k > 0 || pk > 0 || kk > 0);
+                            for (int kk = 0; kk < 8; ++kk)
+                                mma_bf16_ss(d, mndesc(zb, true, et, true, kk),
+                                            sdesc_sw128(ksrc + 16384 + kk * 2048, 16, 1024),
+                                            id64, 1);
+                        }
+                    }
+                    mma_commit(&m->free_[st]);
+                    issued = true;
+                    if (k == n - 1)
+                        mma_commit(&m->accd);
+                }
+            }
+            if (issued && *abort) {
+                mma_commit(&m->drain);
+                tg_drain(&m->drain, 0);
+            }
+        }
+    } else if (warp >= 4) {
+        // ------------------- feature map, decayed values, read-out --------
+        const int t = tid - 128, wq = t >> 5;
+        const bool lead = t == 0;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        int u = 0, j = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; ok && it < items; it += gridDim.x, ++j) {
+            const int s = it / p.nseg, g = it % p.nseg;
+            const int c0 = g * p.L, n = min(p.L, p.nchunk - c0);
+            const int head = s % p.H;
+            const int64_t t0 = (int64_t)c0 * kC;
+            const int seg_len = (int)min((int64_t)p.L * kC, p.N - t0);
+            float zdec = 0.f;
+            for (int k = 0; k < n; ++k, ++u) {
+                const int st = u % NST;
+                const bool okw = tg_wait(&m->full[st], (u / NST) & 1, abort);
+                if (!group_ok(okw, 1, 128)) {
+                    ok = false;
+                    break;
+                }
+                unsigned char* b = stage(st);
+                const int valid = chunk_valid(p.N, c0 + k);
+                if (p.elu)
+                    for (int kb = 0; kb < KB; ++kb)
+                        phi_split_block(b + kb * 16384, b + p.off_klo + kb * 16384, t, valid);
+                if (p.decay) {
+                    // V' = gamma^(T1-1-t) V: weights relative to the segment's end
+                    // (rows past the sequence hold zeros and get weight 0)
+                    const int tl = k * kC + t;
+                    const float l2g = p.g.log2g[head];
+                    const float w = tl < seg_len ? exp2f((float)(seg_len - 1 - tl) * l2g) : 0.f;
+                    for (int vb = 0; vb < VB; ++vb)
+                        decay_block(b + p.off_v + vb * 16384, b + p.off_vlo + vb * 16384, t, w);
+                    if (p.zsum && t < D) {
+                        // the normaliser increment sum_t w_t phi(k_t)_f of feature f = t,
+                        // on the CUDA cores (the ones column of the MMA cannot carry
+                        // w_t); phi(K) is its hi + lo parts
+                        float acc = 0.f;
+                        const int kb = t >> 6, f = t & 63;
+                        const unsigned char* kt = b + kb * 16384;
+                        const unsigned char* kl = b + p.off_klo + kb * 16384;
+                        for (int row = 0; row < valid; ++row) {
+                            const float wr = exp2f((float)(seg_len - 1 - (k * kC + row)) * l2g);
+                            const uint32_t off = sw128_off(row, f >> 3) + (f & 7) * 2;
+                            float x = __uint_as_float(
+                                (uint32_t)*reinterpret_cast<const uint16_t*>(kt + off) << 16);
+                            if (p.elu)
+                                x += __uint_as_float(
+                                    (uint32_t)*reinterpret_cast<const uint16_t*>(kl + off) << 16);
+                            acc = fmaf(wr, x, acc);
+                        }
+                        zdec += acc;
+                    }
+                }
+                fence_proxy_async_smem();
+                named_bar(1, 128);
+                if (lead)
+                    mbar_arrive(&m->prep[st]);
+            }
+            if (!ok)
+                break;
+            // the aggregate: S^T rows and the normaliser, fp32
+            const bool okd = tg_wait(&m->accd, j & 1, abort);
+            if (!group_ok(okd, 1, 128)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float* dst = p.U + ((size_t)s * p.nseg + g) * (size_t)(DV * D + D);
+            if (p.decay && p.zsum && t < D)
+                dst[(size_t)DV * D + t] = zdec;
+            for (int h = 0; h < VB; ++h) {
+                uint32_t r[4][16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    tmem_ld16(tm + lane_off + (uint32_t)(h * 64 + 16 * q), r[q]);
+                tmem_ld_wait();
+                float* row = nullptr;
+                if (D == 64) {
+                    if (t < 64)
+                        row = dst + (size_t)(h * 64 + t) * D;
+                    else if (t == 64 && h == 0 && p.zsum && !p.decay)
+                        row = dst + (size_t)DV * D;
+                } else {
+                    row = dst + (size_t)(h * 64 + (t & 63)) * D + (t >> 6) * 64;
+                }
+                if (row) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            *reinterpret_cast<float4*>(row + 16 * q + 4 * e) =
+                                make_float4(__uint_as_float(r[q][4 * e]),
+                                            __uint_as_float(r[q][4 * e + 1]),
+                                            __uint_as_float(r[q][4 * e + 2]),
+                                            __uint_as_float(r[q][4 * e + 3]));
+                }
+            }
+            if (D == 128 && p.zsum && !p.decay && (wq == 0 || wq == 2)) {
+                uint32_t r[4][16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    tmem_ld16(tm + lane_off + (uint32_t)(VB * 64 + 16 * q), r[q]);
+                tmem_ld_wait();
+                if ((t & 63) == 0) {
+                    float* row = dst + (size_t)DV * D + (t >> 6) * 64;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            *reinterpret_cast<float4*>(row + 16 * q + 4 * e) =
+                                make_float4(__uint_as_float(r[q][4 * e]),
+                                            __uint_as_float(r[q][4 * e + 1]),
+                                            __uint_as_float(r[q][4 * e + 2]),
+                                            __uint_as_float(r[q][4 * e + 3]));
+                }
+            }
+            tc_fence_before();
+            named_bar(1, 128);
+            if (lead)
+                mbar_arrive(&m->accfree);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0 && m->abort)
+        set_status(p.status, LA_ERR_TIMEOUT);
+    if (warp == 0)
+        tmem_dealloc(tm, LY::TMEM_COLS);
+}
+
+// ======================================================================
+// 2. scan over segments
+// ======================================================================
+struct ScanParams {
+    const float* U;        // [BH][nseg][E], or NULL when there is nothing to add
+    int64_t N;
+    int BH, H, nseg, L, D, DV, norm, decay;
+    int zsum;              // the normaliser row is carried (norm, or z_out wanted)
+    const float* S0;       // [BH][D][DV] or NULL
+    const float* z0;       // [BH][D] or NULL
+    unsigned char* img;    // operand images, or NULL
+    int img_per_seg;       // 1: one image per segment (causal), 0: one total image per sequence
+    float* S_out;          // [BH][D][DV] or NULL: the total
+    float* z_out;          // [BH][D] or NULL
+    GammaTable g;
+};
+
+// One thread per (sequence, value tile h, row r, 8 features); rows 0..63 are
+// value channels (S^T), row 64 the normaliser, rows 65..79 of a normalised
+// image zero.  The normaliser row of tiles h > 0 repeats tile 0's (each
+// output tile divides by it).
+__global__ void __launch_bounds__(128) k_tg_scan(const __grid_constant__ ScanParams p)
+{
+    const int ntile = p.DV / kT, IR = img_rows(p.norm), F8 = p.D / 8;
+    const int RR = p.norm ? IR : (p.zsum ? 65 : 64);  // rows carried by threads
+    const int per_seq = ntile * RR * F8;
+    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gid >= (int64_t)p.BH * per_seq)
+        return;
+    const int s = (int)(gid / per_seq);
+    int rem = (int)(gid % per_seq);
+    const int f8 = rem % F8;
+    rem /= F8;
+    const int r = rem % RR, h = rem / RR;
+    const int head = s % p.H;
+    const bool zrow = p.zsum && r == 64;
+    const bool in_img = r < IR;
+    const bool data = r < 64 || zrow;
+    const int c = h * kT + r;  // value channel (r < 64)
+    const size_t E = (size_t)p.DV * p.D + p.D;
+    const size_t src_off = zrow ? (size_t)p.DV * p.D + f8 * 8 : (size_t)c * p.D + f8 * 8;
+
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        acc[e] = 0.f;
+    if (data && p.S0) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int f = f8 * 8 + e;
+            acc[e] = zrow ? p.z0[(size_t)s * p.D + f] : p.S0[((size_t)s * p.D + f) * p.DV + c];
+        }
+    }
+    const size_t part = (size_t)(p.D / 64) * IR * 128;
+    const uint32_t off = (uint32_t)(f8 >> 3) * (uint32_t)IR * 128u + sw128_off(r, f8 & 7);
+    auto write_img = [&](size_t index) {
+        if (!in_img)
+            return;
+        unsigned char* base = p.img + (index * 2) * part;
+        uint4 hi = make_uint4(0, 0, 0, 0), lo = hi;
+        if (data)
+            split8(acc, hi, lo);
+        *reinterpret_cast<uint4*>(base + off) = hi;
+        *reinterpret_cast<uint4*>(base + part + off) = lo;
+    };
+    const float* u = p.U ? p.U + (size_t)s * p.nseg * E + src_off : nullptr;
+    for (int g = 0; g < p.nseg; ++g) {
+        if (p.img && p.img_per_seg)
+            write_img(((size_t)s * p.nseg + g) * ntile + h);
+        if (data && p.U) {
+            const float4 a = *reinterpret_cast<const float4*>(u + (size_t)g * E);
+            const float4 b = *reinterpret_cast<const float4*>(u + (size_t)g * E + 4);
+            float dec = 1.0f;
+            if (p.decay) {
+                const int64_t len = min((int64_t)p.L * kC, p.N - (int64_t)g * p.L * kC);
+                dec = exp2f((float)len * p.g.log2g[head]);
+            }
+            acc[0] = fmaf(dec, acc[0], a.x), acc[1] = fmaf(dec, acc[1], a.y);
+            acc[2] = fmaf(dec, acc[2], a.z), acc[3] = fmaf(dec, acc[3], a.w);
+            acc[4] = fmaf(dec, acc[4], b.x), acc[5] = fmaf(dec, acc[5], b.y);
+            acc[6] = fmaf(dec, acc[6], b.z), acc[7] = fmaf(dec, acc[7], b.w);
+        }
+    }
+    if (p.img && !p.img_per_seg)
+        write_img((size_t)s * ntile + h);
+    if (data && p.S_out) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int f = f8 * 8 + e;
+            if (zrow) {
+                if (p.z_out)
+                    p.z_out[(size_t)s * p.D + f] = acc[e];
+            } else {
+                p.S_out[((size_t)s * p.D + f) * p.DV + c] = acc[e];
+            }
+        }
+    }
+}
+
+// ======================================================================
+// 3. outputs
+// ======================================================================
+struct OutParams {
+    CUtensorMap mq, mk, mv;  // q, k [BH][N][D], v [BH][N][DV]
+    int64_t N;
+    int BH, H, DV;
+    int nchunk, L, nseg, ntile, items;
+    int elu, norm, decay, causal;
+    const unsigned char* img;  // [S^T; z] operand images (per segment, or per sequence)
+    float* out;                // [BH][N][DV]
+    GammaTable g;
+    int* status;
+};
+
+template <int D>
+struct OutLayout {
+    static constexpr int KB = D / 64;
+    static constexpr int NQ = 2;
+    static constexpr int NKV = D == 64 ? 3 : 2;
+    static constexpr uint32_t OFF_ZB = 0, OFF_EB = 2048;       // Z, E below every tile
+    static constexpr uint32_t OFF_Q = 4096;                    // NQ x KB x 16 KiB
+    static constexpr uint32_t OFF_K = OFF_Q + NQ * KB * 16384;  // NKV x KB x 16 KiB
+    static constexpr uint32_t OFF_V = OFF_K + NKV * KB * 16384; // NKV x 16 KiB (one value tile)
+    static constexpr uint32_t OFF_VLO = OFF_V + NKV * 16384;   // lo part of the decayed values
+    static constexpr uint32_t OFF_S = OFF_VLO + 16384;         // [S^T; z] hi then lo
+    static constexpr uint32_t SPART_MAX = KB * 80 * 128;
+    static constexpr uint32_t OFF_ZT = OFF_S + 2 * SPART_MAX;  // Z, E above every tile
+    static constexpr uint32_t OFF_ET = OFF_ZT + 2048;
+    static constexpr uint32_t OFF_PW = OFF_ET + 2048;          // gamma^n, n = 0..127
+    static constexpr uint32_t OFF_MISC = OFF_PW + 512;
+    static constexpr uint32_t SMEM = OFF_MISC + 1024 + 1024;
+    static_assert(SMEM <= 232448, "shared memory");
+};
+
+struct OutMisc {
+    uint64_t qfull[2], qfree[2], phid[2];
+    uint64_t kvfull[3], kvfree[3];
+    uint64_t sdone[2], pdone[2], accfull[2], accfree[2], pvd[2], prepd[2], dsd[2], pfree[2];
+    uint64_t simg, sfree, drain;
+    uint32_t tmem;
+    int abort;
+};
+
+// tensor memory: P[b] (scores, then P hi/lo, then the chunk's state
+// increment) at 128 b; the output accumulators at 256 + 128 b
+constexpr uint32_t TM_P = 0, TM_ACC = 256;
+
+// Walks the work items of this CTA (item = blockIdx.x + j * gridDim.x) and
+// their chunks; u counts chunks over all items.
+struct Iter {
+    int it, j, k, n, u;
+    int s, g, h, c0;
+    bool done;
+    __device__ __forceinline__ void set_item(const OutParams& p)
+    {
+        if (it >= p.items) {
+            done = true;
+            return;
+        }
+        h = it % p.ntile;
+        const int t = it / p.ntile;
+        s = t % p.BH;
+        g = t / p.BH;
+        c0 = g * p.L;
+        n = min(p.L, p.nchunk - c0);
+        k = 0;
+    }
+    __device__ __forceinline__ void start(const OutParams& p)
+    {
+        it = blockIdx.x;
+        j = 0;
+        u = 0;
+        done = false;
+        set_item(p);
+    }
+    __device__ __forceinline__ void advance(const OutParams& p)
+    {
+        ++u;
+        if (++k == n) {
+            it += gridDim.x;
+            ++j;
+            set_item(p);
+        }
+    }
+    __device__ __forceinline__ bool first() const { return k == 0; }
+    __device__ __forceinline__ bool last() const { return k == n - 1; }
+};
+
+template <int D>
+__global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutParams p)
+{
+    using LY = OutLayout<D>;
+    constexpr int KB = LY::KB, NKV = LY::NKV;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    OutMisc* m = reinterpret_cast<OutMisc*>(sm + LY::OFF_MISC);
+    volatile int* abort = &m->abort;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int IR = img_rows(p.norm);
+    const uint32_t spart = (uint32_t)KB * (uint32_t)IR * 128u;
+    const bool causal = p.causal != 0;
+
+    if (tid == 0) {
+        uint64_t* bars = reinterpret_cast<uint64_t*>(m);
+        const int nbars = (int)(offsetof(OutMisc, tmem) / sizeof(uint64_t));
+        for (int i = 0; i < nbars; ++i)
+            mbar_init(&bars[i], 1);
+        m->abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&p.mq);
+        tma_prefetch_desc(&p.mk);
+        tma_prefetch_desc(&p.mv);
+    }
+    if (tid < 128) {
+        init_const_blocks(sm + LY::OFF_ZB, sm + LY::OFF_EB, tid);
+        init_const_blocks(sm + LY::OFF_ZT, sm + LY::OFF_ET, tid);
+    }
+    fence_proxy_async_smem();
+    if (warp == 0) {
+        tmem_alloc(&m->tmem, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = m->tmem;
+    auto qst = [&](int u) { return sm + LY::OFF_Q + (uint32_t)(u & 1) * KB * 16384u; };
+    auto kst = [&](int u) { return sm + LY::OFF_K + (uint32_t)(u % NKV) * KB * 16384u; };
+    auto vst = [&](int u) { return sm + LY::OFF_V + (uint32_t)(u % NKV) * 16384u; };
+    unsigned char* s_hi = sm + LY::OFF_S;
+    unsigned char* s_lo = s_hi + spart;
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer --------
+        // Three load streams advanced as their slots free up: the state image
+        // of each item, Q of each chunk, K and V of each chunk.
+        if (lane == 0) {
+            const uint64_t stream = policy_evict_first();
+            const uint64_t keep = policy_evict_last();
+            Iter iq, ikv;
+            iq.start(p);
+            ikv.start(p);
+            if (!causal)
+                ikv.done = true;
+            int jimg = 0;
+            bool img_done = false;
+            int q_ph[2] = {-1, -1}, kv_ph[3] = {-1, -1, -1}, img_ph = -1;
+            uint64_t idle_since = 0;
+            while (!(iq.done && ikv.done && img_done)) {
+                bool prog = false;
+                if (!img_done) {
+                    const int it = blockIdx.x + jimg * gridDim.x;
+                    if (it >= p.items) {
+                        img_done = true;
+                    } else if (jimg == 0 || mbar_test_wait(&m->sfree, (jimg - 1) & 1)) {
+                        const int h = it % p.ntile, t = it / p.ntile;
+                        const int s = t % p.BH, g = t / p.BH;
+                        const size_t index = causal ? ((size_t)s * p.nseg + g) * p.ntile + h
+                                                    : (size_t)s * p.ntile + h;
+                        const unsigned char* src = p.img + index * 2 * spart;
+                        mbar_arrive_expect_tx(&m->simg, 2 * spart);
+                        bulk_load(s_hi, src, spart, &m->simg, keep);
+                        bulk_load(s_lo, src + spart, spart, &m->simg, keep);
+                        img_ph = jimg & 1;
+                        ++jimg;
+                        prog = true;
+                    }
+                }
+                if (!iq.done) {
+                    const int qs = iq.u & 1;
+                    if (iq.u < 2 || mbar_test_wait(&m->qfree[qs], ((iq.u >> 1) & 1) ^ 1)) {
+                        mbar_arrive_expect_tx(&m->qfull[qs], KB * 16384u);
+                        unsigned char* dst = qst(iq.u);
+                        const int row = (iq.c0 + iq.k) * kC;
+                        for (int kb = 0; kb < KB; ++kb)
+                            tma_load_3d(dst + kb * 16384, &p.mq, 64 * kb, row, iq.s, &m->qfull[qs],
+                                        stream);
+                        q_ph[qs] = (iq.u >> 1) & 1;
+                        iq.advance(p);
+                        prog = true;
+                    }
+                }
+                if (!ikv.done) {
+                    const int ks = ikv.u % NKV;
+                    if (ikv.u < NKV || mbar_test_wait(&m->kvfree[ks], ((ikv.u / NKV) & 1) ^ 1)) {
+                        mbar_arrive_expect_tx(&m->kvfull[ks], (KB + 1) * 16384u);
+                        unsigned char* kd = kst(ikv.u);
+                        const int row = (ikv.c0 + ikv.k) * kC;
+                        for (int kb = 0; kb < KB; ++kb)
+                            tma_load_3d(kd + kb * 16384, &p.mk, 64 * kb, row, ikv.s,
+                                        &m->kvfull[ks], stream);
+                        tma_load_3d(vst(ikv.u), &p.mv, kT * ikv.h, row, ikv.s, &m->kvfull[ks],
+                                    stream);
+                        kv_ph[ks] = (ikv.u / NKV) & 1;
+                        ikv.advance(p);
+                        prog = true;
+                    }
+                }
+                if (prog) {
+                    idle_since = 0;
+                } else {
+                    if (*abort)
+                        break;
+                    const uint64_t now = globaltimer();
+                    if (!idle_since) {
+                        idle_since = now;
+                    } else if (now - idle_since > kWaitNs) {
+                        *abort = 1;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+            if (*abort) {  // every load this thread issued lands before exit
+                for (int i = 0; i < 2; ++i)
+                    if (q_ph[i] >= 0)
+                        tg_drain(&m->qfull[i], q_ph[i]);
+                for (int i = 0; i < NKV; ++i)
+                    if (kv_ph[i] >= 0)
+                        tg_drain(&m->kvfull[i], kv_ph[i]);
+                if (img_ph >= 0)
+                    tg_drain(&m->simg, img_ph);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer ------
+        // Four streams, each in chunk order, issued as their inputs are ready:
+        // SC scores, IN phi(Q) [S^T; z], PV P [V | 1], DS the state increment.
+        if (lane == 0) {
+            const uint32_t id_sc = idesc_bf16_f32(128, 128, false, false);
+            const uint32_t id_in = idesc_bf16_f32(128, IR, false, false);
+            const uint32_t id_pv = idesc_bf16_f32(128, IR, false, true);
+            const uint32_t id64 = idesc_bf16_f32(128, 64, true, true);
+            const uint32_t zb = smem_addr(sm + LY::OFF_ZB), eb = smem_addr(sm + LY::OFF_EB);
+            const uint32_t zt = smem_addr(sm + LY::OFF_ZT), et = smem_addr(sm + LY::OFF_ET);
+            const uint32_t shi = smem_addr(s_hi), slo = smem_addr(s_lo);
+            const uint32_t vlo = smem_addr(sm + LY::OFF_VLO);
+            Iter sc, in, pv, ds;
+            sc.start(p);
+            in.start(p);
+            pv.start(p);
+            ds.start(p);
+            if (!causal)
+                sc.done = pv.done = ds.done = true;
+            bool issued = false;
+            uint64_t idle_since = 0;
+            while (!(sc.done && in.done && pv.done && ds.done)) {
+                bool prog = false;
+                // ---- scores
+                if (!sc.done) {
+                    const int u = sc.u, b = u & 1;
+                    if (mbar_test_wait(&m->qfull[u & 1], (u >> 1) & 1) &&
+                        mbar_test_wait(&m->kvfull[u % NKV], (u / NKV) & 1) &&
+                        (!p.elu || mbar_test_wait(&m->phid[u & 1], (u >> 1) & 1)) &&
+                        (u < 2 || mbar_test_wait(&m->pfree[b], ((u - 2) >> 1) & 1))) {
+                        tc_fence_after();
+                        const uint32_t qa = smem_addr(qst(u)), ka = smem_addr(kst(u));
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            mma_bf16_ss(tm + TM_P + 128 * b, kdesc(qa, 128, kk), kdesc(ka, 128, kk),
+                                        id_sc, kk > 0);
+                        mma_commit(&m->sdone[b]);
+                        if (in.u > u)
+                            mma_commit(&m->qfree[u & 1]);
+                        issued = true;
+                        sc.advance(p);
+                        prog = true;
+                    }
+                }
+                // ---- inter: phi(Q) [S^T; z] (hi, lo)
+                if (!in.done) {
+                    const int u = in.u, b = u & 1;
+                    const bool s_ready =
+                        in.first() ? mbar_test_wait(&m->simg, in.j & 1)
+                                   : mbar_test_wait(&m->pfree[(u - 1) & 1], ((u - 1) >> 1) & 1);
+                    if (mbar_test_wait(&m->qfull[u & 1], (u >> 1) & 1) &&
+                        (!p.elu || mbar_test_wait(&m->phid[u & 1], (u >> 1) & 1)) && s_ready &&
+                        (u < 2 || mbar_test_wait(&m->accfree[b], ((u - 2) >> 1) & 1))) {
+                        tc_fence_after();
+                        const uint32_t qa = smem_addr(qst(u));
+                        const uint32_t d = tm + TM_ACC + 128 * b;
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            mma_bf16_ss(d, kdesc(qa, 128, kk), kdesc(shi, IR, kk), id_in, kk > 0);
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            mma_bf16_ss(d, kdesc(qa, 128, kk), kdesc(slo, IR, kk), id_in, 1);
+                        if (!causal || sc.u > u)
+                            mma_commit(&m->qfree[u & 1]);
+                        if (!causal || pv.u > u)
+                            mma_commit(&m->accfull[b]);
+                        if (in.last())
+                            mma_commit(&m->sfree);
+                        issued = true;
+                        in.advance(p);
+                        prog = true;
+                    }
+                }
+                // ---- intra: P [V | 1] (P hi, lo from tensor memory)
+                if (!pv.done) {
+                    const int u = pv.u, b = u & 1;
+                    const bool acc_ok = p.decay ? (u < 2 || mbar_test_wait(&m->accfree[b],
+                                                                           ((u - 2) >> 1) & 1))
+                                                : in.u > u;
+                    if (acc_ok && mbar_test_wait(&m->pdone[b], (u >> 1) & 1) &&
+                        mbar_test_wait(&m->kvfull[u % NKV], (u / NKV) & 1)) {
+                        tc_fence_after();
+                        const uint32_t va = smem_addr(vst(u));
+                        const uint32_t d = tm + TM_ACC + 128 * b + (p.decay ? 64 : 0);
+                        const uint32_t pa = tm + TM_P + 128 * b;
+                        for (int ps = 0; ps < 2; ++ps)
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint64_t bd = p.norm ? mndesc(va, false, et, true, kk)
+                                                           : sdesc_sw128(va + kk * 2048, 16, 1024);
+                                mma_bf16_ts(d, pa + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * ps, bd,
+                                            id_pv, p.decay ? (ps > 0 || kk > 0) : 1);
+                            }
+                        mma_commit(&m->pvd[b]);
+                        if (in.u > u)
+                            mma_commit(&m->accfull[b]);
+                        if (pv.last()) {  // no state update after an item's last chunk
+                            mma_commit(&m->dsd[b]);
+                            mma_commit(&m->kvfree[u % NKV]);
+                        }
+                        issued = true;
+                        pv.advance(p);
+                        prog = true;
+                    }
+                }
+                // ---- the chunk's state increment [V' | 1]^T phi(K) into P[b]
+                if (!ds.done) {
+                    const int u = ds.u, b = u & 1;
+                    if (ds.last()) {
+                        if (pv.u > u) {
+                            ds.advance(p);
+                            prog = true;
+                        }
+                    } else if (pv.u > u && in.u > u &&
+                               mbar_test_wait(&m->pvd[b], (u >> 1) & 1) &&
+                               (!p.decay || mbar_test_wait(&m->prepd[b], (u >> 1) & 1))) {
+                        tc_fence_after();
+                        const uint32_t ka = smem_addr(kst(u)), va = smem_addr(vst(u));
+                        const uint32_t d = tm + TM_P + 128 * b;
+                        const int npass = p.decay ? 2 : 1;
+                        for (int ps = 0; ps < npass; ++ps) {
+                            const uint32_t vsrc = ps ? vlo : va;
+                            if (D == 64) {
+                                const uint32_t x = (p.norm && ps == 0) ? et : zt;
+                                for (int kk = 0; kk < 8; ++kk)
+                                    mma_bf16_ss(d, mndesc(vsrc, false, x, true, kk),
+                                                sdesc_sw128(ka + kk * 2048, 16, 1024), id64,
+                                                ps > 0 || kk > 0);
+                            } else {
+                                for (int kk = 0; kk < 8; ++kk)
+                                    mma_bf16_ss(d, mndesc(vsrc, false, zt, true, kk),
+                                                sdesc_sw128(ka + kk * 2048, 16, 1024), id64,
+                                                ps > 0 || kk > 0);
+                                for (int kk = 0; kk < 8; ++kk)
+                                    mma_bf16_ss(d, mndesc(zb, true, vsrc, false, kk),
+                                                sdesc_sw128(ka + 16384 + kk * 2048, 16, 1024),
+                                                id64, 1);
+                            }
+                        }
+                        if (D == 128 && p.norm) {
+                            for (int kk = 0; kk < 8; ++kk)
+                                mma_bf16_ss(d + 64, mndesc(eb, true, zt, true, kk),
+                                            sdesc_sw128(ka + kk * 2048, 16, 1024), id64, kk > 0);
+                            for (int kk = 0; kk < 8; ++kk)
+                                mma_bf16_ss(d + 64, mndesc(zb, true, et, true, kk),
+                                            sdesc_sw128(ka + 16384 + kk * 2048, 16, 1024), id64, 1);
+                        }
+                        mma_commit(&m->dsd[b]);
+                        mma_commit(&m->kvfree[u % NKV]);
+                        issued = true;
+                        ds.advance(p);
+                        prog = true;
+                    }
+                }
+                if (prog) {
+                    idle_since = 0;
+                } else {
+                    if (*abort)
+                        break;
+                    const uint64_t now = globaltimer();
+                    if (!idle_since) {
+                        idle_since = now;
+                    } else if (now - idle_since > kWaitNs) {
+                        *abort = 1;
+                        break;
+                    }
+                }
+            }
+            if (issued && *abort) {
+                mma_commit(&m->drain);
+                tg_drain(&m->drain, 0);
+            }
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------ feature map and the P pass --------
+        const int t = tid - 128, wq = t >> 5;
+        const bool lead = t == 0;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        float* pw = reinterpret_cast<float*>(sm + LY::OFF_PW);
+        Iter w;
+        w.start(p);
+        bool ok = true;
+        while (ok && !w.done) {
+            const int u = w.u, b = u & 1;
+            const int valid = chunk_valid(p.N, w.c0 + w.k);
+            if (p.decay && w.first()) {
+                named_bar(1, 128);  // every thread is past the previous item's P pass
+                pw[t] = exp2f((float)t * p.g.log2g[w.s % p.H]);
+                named_bar(1, 128);
+            }
+            if (p.elu) {
+                bool okw = tg_wait(&m->qfull[u & 1], (u >> 1) & 1, abort);
+                if (causal)
+                    okw = okw && tg_wait(&m->kvfull[u % NKV], (u / NKV) & 1, abort);
+                if (!group_ok(okw, 1, 128)) {
+                    ok = false;
+                    break;
+                }
+                unsigned char* q = qst(u);
+                for (int kb = 0; kb < KB; ++kb)
+                    phi_tile(q + kb * 16384, t, valid, true);
+                if (causal) {
+                    unsigned char* k = kst(u);
+                    for (int kb = 0; kb < KB; ++kb)
+                        phi_tile(k + kb * 16384, t, valid, true);
+                }
+                fence_proxy_async_smem();
+                named_bar(1, 128);
+                if (lead)
+                    mbar_arrive(&m->phid[u & 1]);
+            }
+            if (causal) {
+                const bool okw = tg_wait(&m->sdone[b], (u >> 1) & 1, abort);
+                if (!group_ok(okw, 1, 128)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // P = tril(scores) o gamma^(i-j) as bf16 hi/lo, in place: keys
+                // 32q..32q+31 of row t move to columns 32q..32q+15 (hi) and
+                // 32q+16..32q+31 (lo); blocks right of the diagonal become zero.
+                const uint32_t pb = tm + TM_P + 128 * b + lane_off;
+                for (int q = 0; q <= wq; ++q) {
+                    uint32_t v0[16], v1[16], hi[16], lo[16];
+                    tmem_ld16(pb + 32 * q, v0);
+                    tmem_ld16(pb + 32 * q + 16, v1);
+                    tmem_ld_wait();
+                    float x[32];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        x[e] = __uint_as_float(v0[e]);
+                        x[16 + e] = __uint_as_float(v1[e]);
+                    }
+                    if (q == wq) {  // the diagonal block: keys j <= i only
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (e > lane)
+                                x[e] = 0.f;
+                    }
+                    if (p.decay) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int dist = t - (32 * q + e);
+                            x[e] = dist >= 0 ? x[e] * pw[dist] : 0.f;
+                        }
+                    }
+#pragma unroll
+                    for (int mm = 0; mm < 8; ++mm) {
+                        split2(x[2 * mm], x[2 * mm + 1], hi[mm], lo[mm]);
+                        split2(x[16 + 2 * mm], x[16 + 2 * mm + 1], hi[8 + mm], lo[8 + mm]);
+                    }
+                    tmem_st16(pb + 32 * q, hi);
+                    tmem_st16(pb + 32 * q + 16, lo);
+                }
+                uint32_t zz[16];
+#pragma unroll
+                for (int mm = 0; mm < 16; ++mm)
+                    zz[mm] = 0u;
+                for (int q = wq + 1; q < 4; ++q) {
+                    tmem_st16(pb + 32 * q, zz);
+                    tmem_st16(pb + 32 * q + 16, zz);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                named_bar(1, 128);
+                if (lead)
+                    mbar_arrive(&m->pdone[b]);
+            }
+            w.advance(p);
+        }
+    } else if (warp >= 8 && warp < 12) {
+        // ------------------------------------------------ epilogue --------
+        // o = (g inter + intra) / (g den_inter + den_intra) from registers.  A
+        // 16x256b tensor-memory load gives each quad of threads 8 consecutive
+        // columns of one row; neighbours swap one pair so that every store
+        // is 16 bytes and a quad fills whole 32-byte sectors.
+        const int t = tid - 256, wq = t >> 5;
+        const bool lead = t == 0;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const unsigned full = 0xffffffffu;
+        Iter w;
+        w.start(p);
+        bool ok = true;
+        while (ok && !w.done) {
+            const int u = w.u, b = u & 1;
+            const bool okw = tg_wait(&m->accfull[b], (u >> 1) & 1, abort);
+            if (!group_ok(okw, 2, 128)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t acc = tm + TM_ACC + 128 * b + lane_off;
+            float den_row = 1.0f, g_row = 1.0f;
+            if (p.norm) {
+                den_row = __uint_as_float(tmem_ld1(acc + 64));
+                tmem_ld_wait();
+            }
+            if (p.decay)
+                g_row = exp2f((float)(t + 1) * p.g.log2g[w.s % p.H]);
+            const float inv_row = p.norm ? 1.0f / fmaxf(den_row, FLT_MIN) : 1.0f;
+            const int valid = chunk_valid(p.N, w.c0 + w.k);
+            float* obase = p.out + ((size_t)w.s * p.N + (size_t)(w.c0 + w.k) * kC) * p.DV +
+                           kT * w.h;
+#pragma unroll 1
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t rr[32];
+                tmem_ld16x256b_x8(acc + ((uint32_t)(16 * h2) << 16), rr);
+                tmem_ld_wait();
+                if (p.decay) {
+                    uint32_t ra[32];
+                    tmem_ld16x256b_x8(acc + 64 + ((uint32_t)(16 * h2) << 16), ra);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const float gr = __shfl_sync(full, g_row, 16 * h2 + 8 * hr + (lane >> 2));
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int r = 4 * i + 2 * hr + e;
+                                rr[r] = __float_as_uint(
+                                    fmaf(gr, __uint_as_float(rr[r]), __uint_as_float(ra[r])));
+                            }
+                    }
+                }
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int rw = 16 * h2 + 8 * hr + (lane >> 2);  // row within the warp
+                    const float inv = __shfl_sync(full, inv_row, rw);
+                    const int row = 32 * wq + rw;
+                    const bool odd = lane & 1;
+                    float* orow = obase + (size_t)row * p.DV + 2 * ((lane & 3) & ~1);
+#pragma unroll
+                    for (int i = 0; i < 8; i += 2) {
+                        const float2 g0 = mul2(make_float2(__uint_as_float(rr[4 * i + 2 * hr]),
+                                                           __uint_as_float(rr[4 * i + 2 * hr + 1])),
+                                               make_float2(inv, inv));
+                        const float2 g1 =
+                            mul2(make_float2(__uint_as_float(rr[4 * (i + 1) + 2 * hr]),
+                                             __uint_as_float(rr[4 * (i + 1) + 2 * hr + 1])),
+                                 make_float2(inv, inv));
+                        const float2 give = odd ? g0 : g1;
+                        const float2 got = make_float2(__shfl_xor_sync(full, give.x, 1),
+                                                       __shfl_xor_sync(full, give.y, 1));
+                        if (row < valid) {
+                            const float4 v4 = odd ? make_float4(got.x, got.y, g1.x, g1.y)
+                                                  : make_float4(g0.x, g0.y, got.x, got.y);
+                            __stcs(reinterpret_cast<float4*>(orow + 8 * (i + (odd ? 1 : 0))), v4);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            named_bar(2, 128);
+            if (lead)
+                mbar_arrive(&m->accfree[b]);
+            w.advance(p);
+        }
+    } else if (warp >= 12 && causal) {
+        // -------------------------- decayed values and the state update ---
+        const int t = tid - 384, wq = t >> 5;
+        const bool lead = t == 0;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        Iter w;
+        w.start(p);
+        bool ok = true;
+        while (ok && !w.done) {
+            const int u = w.u, b = u & 1;
+            if (w.last()) {  // nothing to carry: P[b] is free once its MMAs are done
+                if (lead && p.decay)  // keep one arrival per chunk on every barrier
+                    mbar_arrive(&m->prepd[b]);
+                const bool okw = !lead || tg_wait(&m->dsd[b], (u >> 1) & 1, abort);
+                if (!group_ok(okw, 3, 128)) {
+                    ok = false;
+                    break;
+                }
+                if (lead)
+                    mbar_arrive(&m->pfree[b]);
+                w.advance(p);
+                continue;
+            }
+            const float l2g = p.decay ? p.g.log2g[w.s % p.H] : 0.f;
+            if (p.decay) {
+                // V' = gamma^(C-1-t) V, hi in place and lo aside, once P [V | 1] is done
+                const bool okw = tg_wait(&m->pvd[b], (u >> 1) & 1, abort);
+                if (!group_ok(okw, 3, 128)) {
+                    ok = false;
+                    break;
+                }
+                decay_block(vst(u), sm + LY::OFF_VLO, t, exp2f((float)(kC - 1 - t) * l2g));
+                fence_proxy_async_smem();
+                named_bar(3, 128);
+                if (lead)
+                    mbar_arrive(&m->prepd[b]);
+            }
+            const bool okw = tg_wait(&m->dsd[b], (u >> 1) & 1, abort);
+            if (!group_ok(okw, 3, 128)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // S <- gamma^C S + dS in the operand image: row r (value channel,
+            // or 64 for the normaliser), 64 features of block fb
+            const float dec = p.decay ? exp2f((float)kC * l2g) : 1.0f;
+            const uint32_t pb = tm + TM_P + 128 * b + lane_off;
+            auto update_row = [&](const uint32_t (&dsv)[4][16], int r, int fb) {
+                unsigned char* hrow = s_hi + (uint32_t)fb * (uint32_t)IR * 128u;
+                unsigned char* lrow = s_lo + (uint32_t)fb * (uint32_t)IR * 128u;
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    const uint32_t off = sw128_off(r, c8);
+                    float o[8], l[8];
+                    unpack8(*reinterpret_cast<const uint4*>(hrow + off), o);
+                    unpack8(*reinterpret_cast<const uint4*>(lrow + off), l);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        o[e] = fmaf(dec, o[e] + l[e], __uint_as_float(dsv[c8 >> 1][8 * (c8 & 1) + e]));
+                    uint4 hi, lo;
+                    split8(o, hi, lo);
+                    *reinterpret_cast<uint4*>(hrow + off) = hi;
+                    *reinterpret_cast<uint4*>(lrow + off) = lo;
+                }
+            };
+            if (D == 64) {
+                if (wq < 3) {
+                    uint32_t dsv[4][16];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        tmem_ld16(pb + 16 * q, dsv[q]);
+                    tmem_ld_wait();
+                    if (t < 64 || (t == 64 && p.norm))
+                        update_row(dsv, t, 0);
+                }
+            } else {
+                {
+                    uint32_t dsv[4][16];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        tmem_ld16(pb + 16 * q, dsv[q]);
+                    tmem_ld_wait();
+                    update_row(dsv, t & 63, t >> 6);
+                }
+                if (p.norm && (wq == 0 || wq == 2)) {
+                    uint32_t dsv[4][16];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        tmem_ld16(pb + 64 + 16 * q, dsv[q]);
+                    tmem_ld_wait();
+                    if ((t & 63) == 0)
+                        update_row(dsv, 64, t >> 6);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_bar(3, 128);
+            if (lead)
+                mbar_arrive(&m->pfree[b]);
+            w.advance(p);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0 && m->abort)
+        set_status(p.status, LA_ERR_TIMEOUT);
+    if (warp == 0)
+        tmem_dealloc(tm, 512);
+}
+
+// ------------------------------------------------------------------ host --
+struct TgGeom {
+    int nchunk, L, nseg, ntile, items;
+    int IR;
+    size_t U_off, img_off, bytes;
+};
+
+TgGeom tg_geom(int64_t BH, int64_t N, int D, int DV, bool norm, bool causal, int sms)
+{
+    TgGeom g{};
+    if (sms <= 0)
+        sms = 148;
+    g.nchunk = (int)((N + kC - 1) / kC);
+    g.ntile = DV / kT;
+    // about six work items per SM keep the tail short; longer segments carry
+    // the state further on chip and make the aggregates fewer
+    const int64_t work = BH * g.nchunk * g.ntile;
+    g.L = (int)std::max<int64_t>(1, std::min<int64_t>(16, work / ((int64_t)sms * 6)));
+    g.L = std::min(g.L, g.nchunk);
+    g.nseg = (g.nchunk + g.L - 1) / g.L;
+    g.items = (int)(BH * g.nseg * g.ntile);
+    g.IR = img_rows(norm);
+    const size_t E = (size_t)DV * D + D;
+    const size_t part = (size_t)(D / 64) * g.IR * 128;
+    g.U_off = 0;
+    g.img_off = (sizeof(float) * (size_t)BH * g.nseg * E + 1023) & ~(size_t)1023;
+    const size_t nimg = causal ? (size_t)BH * g.nseg * g.ntile : (size_t)BH * g.ntile;
+    g.bytes = g.img_off + nimg * 2 * part;
+    return g;
+}
+
+template <typename K>
+cudaError_t set_smem(K kern, uint32_t bytes)
+{
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <int D, int DV>
+cudaError_t launch_state(StParams sp, int grid, cudaStream_t st)
+{
+    using LY = StLayout<D, DV>;
+    sp.off_klo = (uint32_t)LY::KB * 16384u;
+    sp.off_v = sp.off_klo * (sp.elu ? 2u : 1u);
+    sp.off_vlo = sp.off_v + (uint32_t)LY::VB * 16384u;
+    sp.stage = sp.off_vlo + (sp.decay ? (uint32_t)LY::VB * 16384u : 0u);
+    sp.nst = (int)std::min<uint32_t>(4, kStStageBudget / sp.stage);
+    if (sp.nst < 1)
+        return cudaErrorInvalidValue;
+    const uint32_t smem = LY::OFF_ST + (uint32_t)sp.nst * sp.stage + LY::TAIL + 1024;
+    cudaError_t e = set_smem(k_tg_state<D, DV>, LY::SMEM_MAX);
+    if (e != cudaSuccess)
+        return e;
+    k_tg_state<D, DV><<<grid, 256, smem, st>>>(sp);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_state_any(int D, int DV, const StParams& sp, int grid, cudaStream_t st)
+{
+    switch (D * 1000 + DV) {
+    case 64064: return launch_state<64, 64>(sp, grid, st);
+    case 64128: return launch_state<64, 128>(sp, grid, st);
+    case 128064: return launch_state<128, 64>(sp, grid, st);
+    case 128128: return launch_state<128, 128>(sp, grid, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int D>
+cudaError_t launch_out(const OutParams& op, int grid, cudaStream_t st)
+{
+    using LY = OutLayout<D>;
+    cudaError_t e = set_smem(k_tg_out<D>, LY::SMEM);
+    if (e != cudaSuccess)
+        return e;
+    k_tg_out<D><<<grid, 512, LY::SMEM, st>>>(op);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tg_eligible(const FwdArgs& a)
+{
+    const bool dims = (a.d == 64 || a.d == 128) && (a.dv == 64 || a.dv == 128);
+    // decay is carried only with the unnormalised map, except for state-only
+    // calls (the aggregates take any map)
+    const bool decay_ok = !a.gamma->has_decay || a.fm == LA_FM_NONE || !a.out;
+    return a.dtype == LA_BF16 && dims && decay_ok && a.N >= 1 &&
+           a.N <= (int64_t)INT32_MAX - kC && a.B * a.H <= (int64_t)INT32_MAX / 4;
+}
+
+size_t tg_workspace(int64_t BH, int64_t N, int d, int dv, int fm, int causal)
+{
+    return tg_geom(BH, N, d, dv, fm != LA_FM_NONE, causal != 0, device_sm_count()).bytes;
+}
+
+// Forward (a.out != NULL) and/or state (a.S_out != NULL) on the tensor cores;
+// a.S0 / a.z0 give the state before the first token.
+cudaError_t tg_run(const FwdArgs& a)
+{
+    const int64_t BH = a.B * a.H;
+    const bool norm = a.fm != LA_FM_NONE;
+    const bool causal = a.causal != 0;
+    const bool want_out = a.out != nullptr;
+    const bool want_z = a.z_out != nullptr;
+    const TgGeom g = tg_geom(BH, a.N, a.d, a.dv, norm, causal, device_sm_count());
+    if (a.ws_bytes < g.bytes)
+        return cudaErrorInvalidValue;
+    unsigned char* ws = static_cast<unsigned char*>(a.ws);
+    float* U = reinterpret_cast<float*>(ws + g.U_off);
+    unsigned char* img = ws + g.img_off;
+    const int sms = std::max(1, device_sm_count());
+
+    // 1. segment aggregates: needed for any state other than S_0 itself
+    const bool need_U = !want_out || !causal || g.nseg > 1 || a.S_out;
+    const bool zsum = norm || want_z;
+    if (need_U) {
+        StParams sp;
+        memset(&sp, 0, sizeof sp);
+        if (!tma_map_bf16_3d(&sp.mk, a.k, a.d, a.N, BH) ||
+            !tma_map_bf16_3d(&sp.mv, a.v, a.dv, a.N, BH))
+            return cudaErrorInvalidValue;
+        sp.N = a.N;
+        sp.BH = (int)BH;
+        sp.H = (int)a.H;
+        sp.nchunk = g.nchunk;
+        sp.L = g.L;
+        sp.nseg = g.nseg;
+        sp.elu = a.fm == LA_FM_ELU1;
+        sp.zsum = zsum;
+        sp.decay = a.gamma->has_decay;
+        sp.U = U;
+        sp.g = *a.gamma;
+        sp.status = a.status;
+        const int grid = (int)std::min<int64_t>(sms, BH * g.nseg);
+        cudaError_t e = launch_state_any(a.d, a.dv, sp, grid, a.stream);
+        if (e != cudaSuccess)
+            return e;
+    }
+    // 2. scan: operand images of the state before every segment (causal) or
+    //    of the total (non-causal), and the final state
+    {
+        ScanParams cp;
+        memset(&cp, 0, sizeof cp);
+        cp.U = need_U ? U : nullptr;
+        cp.N = a.N;
+        cp.BH = (int)BH;
+        cp.H = (int)a.H;
+        cp.nseg = g.nseg;
+        cp.L = g.L;
+        cp.D = a.d;
+        cp.DV = a.dv;
+        cp.norm = norm;
+        cp.decay = a.gamma->has_decay;
+        cp.zsum = norm || want_z;
+        cp.S0 = a.S0;
+        cp.z0 = a.z0;
+        cp.img = want_out ? img : nullptr;
+        cp.img_per_seg = causal;
+        cp.S_out = a.S_out;
+        cp.z_out = a.z_out;
+        cp.g = *a.gamma;
+        const int RR = norm ? img_rows(true) : (cp.zsum ? 65 : 64);
+        const int64_t threads = BH * (a.dv / kT) * RR * (a.d / 8);
+        const int64_t grid = (threads + 127) / 128;
+        k_tg_scan<<<(unsigned)grid, 128, 0, a.stream>>>(cp);
+        count_launches(1);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+    }
+    if (!want_out)
+        return cudaSuccess;
+    // 3. outputs
+    OutParams op;
+    memset(&op, 0, sizeof op);
+    if (!tma_map_bf16_3d(&op.mq, a.q, a.d, a.N, BH) ||
+        (causal && !tma_map_bf16_3d(&op.mk, a.k, a.d, a.N, BH)) ||
+        (causal && !tma_map_bf16_3d(&op.mv, a.v, a.dv, a.N, BH)))
+        return cudaErrorInvalidValue;
+    if (!causal) {  // unused maps still need valid descriptors for the prefetch
+        op.mk = op.mq;
+        op.mv = op.mq;
+    }
+    op.N = a.N;
+    op.BH = (int)BH;
+    op.H = (int)a.H;
+    op.DV = a.dv;
+    op.nchunk = g.nchunk;
+    op.L = g.L;
+    op.nseg = g.nseg;
+    op.ntile = g.ntile;
+    op.items = g.items;
+    op.elu = a.fm == LA_FM_ELU1;
+    op.norm = norm;
+    op.decay = a.gamma->has_decay;
+    op.causal = causal;
+    op.img = img;
+    op.out = a.out;
+    op.g = *a.gamma;
+    op.status = a.status;
+    const int grid = std::min(sms, g.items);
+    return a.d == 64 ? launch_out<64>(op, grid, a.stream) : launch_out<128>(op, grid, a.stream);
+}
+
+}  // namespace la

@@ -167,12 +167,19 @@ def test_argument_errors_on_device():
 
 
 def test_tensor_core_path_is_taken():
-    """The bf16, d = dv = 64 causal workloads run on the tcgen05 kernel."""
+    """The bf16, d = dv = 64 causal workloads run on the single-pass tcgen05
+    kernel; the RetNet workload and the non-causal form on the chunked one."""
     for name in ("causal_n2048_d64_bf16", "causal_n32768_d64_bf16"):
         w = synth.WORKLOADS[name]
         assert la.la_forward_path(w.B, w.H, w.N, w.d, w.dv, True, "elu1", False, w.dtype) == "tcgen05"
-    assert la.la_forward_path(1, 1, 100, 64, 64, False, "elu1", False, torch.bfloat16) == "simt"
-    assert la.la_forward_path(1, 1, 100, 64, 64, True, "none", True, torch.bfloat16) == "simt"
+    w = synth.WORKLOADS["retnet_n8192_d128_bf16"]
+    assert la.la_forward_path(w.B, w.H, w.N, w.d, w.dv, True, "none", True,
+                              w.dtype) == "tcgen05_chunked"
+    assert la.la_forward_path(1, 1, 100, 64, 64, False, "elu1", False,
+                              torch.bfloat16) == "tcgen05_chunked"
+    assert la.la_forward_path(1, 1, 100, 64, 64, True, "none", True,
+                              torch.bfloat16) == "tcgen05_chunked"
+    assert la.la_forward_path(1, 1, 100, 64, 64, True, "elu1", False, torch.float32) == "simt"
 
 
 @pytest.mark.parametrize("fm", ["elu1", "identity_norm", "none"])
