@@ -60,6 +60,7 @@ using namespace tcc;
 
 constexpr int kC = 128;        // tokens per chunk
 constexpr int kT = 64;         // value channels per output tile
+constexpr int kPrefetch = 4;   // chunks the L2 prefetch runs ahead of the loads
 constexpr uint64_t kWaitNs = 2000000000ull;  // any single wait gives up after 2 s
 
 // Rows of the [S^T; z] operand image of one value tile: 64 value channels,
@@ -152,6 +153,22 @@ __device__ __forceinline__ void init_const_blocks(unsigned char* z, unsigned cha
     *reinterpret_cast<uint4*>(e + r * 128 + c * 16) = w;
 }
 
+// Optional per-chunk event timestamps (SM clock) of the output kernel's
+// roles, for pipeline analysis; only in builds with LA_TG_TRACE defined,
+// never in the library as shipped.
+#ifdef LA_TG_TRACE
+__device__ unsigned long long* g_tg_trace;
+#define TG_TRACE(u, ev)                                                                       \
+    do {                                                                                      \
+        if (g_tg_trace && (u) < 64)                                                           \
+            g_tg_trace[(static_cast<size_t>(blockIdx.x) * 64 + (u)) * 32 + (ev)] = clock64(); \
+    } while (0)
+#else
+#define TG_TRACE(u, ev) \
+    do {                \
+    } while (0)
+#endif
+
 // Rows of a chunk that hold tokens (the last chunk of a sequence is short).
 __device__ __forceinline__ int chunk_valid(int64_t N, int c)
 {
@@ -187,9 +204,9 @@ struct StLayout {
     // Z, E above the stages, then the barriers: offsets from the end of the stages
     static constexpr uint32_t TAIL = 2048 + 2048 + 1024;
     static constexpr uint32_t SMEM_MAX = OFF_ST + kStStageBudget + TAIL + 1024;
-    // tensor memory: per value tile 64 columns of [dS^T]; for D = 128 the
-    // normaliser increments in 64 more columns
-    static constexpr uint32_t COLS_USED = VB * 64 + (D == 128 ? 64 : 0);
+    // tensor memory: [dS^T] in D columns (lanes = value channels); with
+    // DV = 128 the normaliser increments in D more columns (lane 0)
+    static constexpr uint32_t COLS_USED = D + (VB == 2 ? D : 0);
     static constexpr uint32_t TMEM_COLS = COLS_USED <= 32 ? 32 : COLS_USED <= 64 ? 64
                                         : COLS_USED <= 128 ? 128 : COLS_USED <= 256 ? 256 : 512;
     static_assert(SMEM_MAX <= 232448, "shared memory");
@@ -297,11 +314,32 @@ __global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StP
             int u = 0;
             int last_ph[4] = {-1, -1, -1, -1};
             bool ok = true;
+            // L2 prefetch kPrefetch chunks ahead of the loads (walks the same
+            // items and chunks)
+            int pf_it = blockIdx.x, pf_k = 0;
+            auto prefetch_next = [&]() {
+                if (pf_it >= items)
+                    return;
+                const int s = pf_it / p.nseg, g = pf_it % p.nseg;
+                const int c0 = g * p.L, n = min(p.L, p.nchunk - c0);
+                const int row = (c0 + pf_k) * kC;
+                for (int kb = 0; kb < KB; ++kb)
+                    tma_prefetch_l2_3d(&p.mk, 64 * kb, row, s);
+                for (int vb = 0; vb < VB; ++vb)
+                    tma_prefetch_l2_3d(&p.mv, 64 * vb, row, s);
+                if (++pf_k == n) {
+                    pf_k = 0;
+                    pf_it += gridDim.x;
+                }
+            };
+            for (int i = 0; i < kPrefetch; ++i)
+                prefetch_next();
             for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
                 const int s = it / p.nseg, g = it % p.nseg;
                 const int c0 = g * p.L, n = min(p.L, p.nchunk - c0);
                 for (int k = 0; k < n; ++k, ++u) {
                     const int st = u % NST;
+                    prefetch_next();
                     if (u >= NST && !tg_wait(&m->free_[st], ((u / NST) & 1) ^ 1, abort)) {
                         ok = false;
                         break;
@@ -325,9 +363,12 @@ __global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StP
     } else if (warp == 1) {
         // ------------------------------------------ MMA issuer -----------
         if ((tid & 31) == 0) {
-            const uint32_t id64 = idesc_bf16_f32(128, 64, true, true);
-            const uint32_t zb = smem_addr(sm + LY::OFF_ZB), eb = smem_addr(sm + LY::OFF_EB);
+            // one MMA per K step covers every value channel (M) and every
+            // feature (N = D): [dS^T] lanes = channels, columns = features
+            const uint32_t idD = idesc_bf16_f32(128, D, true, true);
+            const uint32_t eb = smem_addr(sm + LY::OFF_EB);
             const uint32_t zt = smem_addr(sm + OFF_ZT), et = smem_addr(sm + OFF_ET);
+            const uint32_t klbo = D == 128 ? 16384u : 16u;  // feature blocks of phi(K)
             const int nk = p.elu ? 2 : 1, nv = p.decay ? 2 : 1;
             const bool dz_mma = p.zsum && !p.decay;  // else the CUDA cores sum dz
             int u = 0, j = 0;
@@ -348,49 +389,31 @@ __global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StP
                     }
                     tc_fence_after();
                     const uint32_t b = smem_addr(stage(st));
-                    // [dS^T] += [V' | x]^T phi(K) over the hi/lo parts of V'
-                    // (decay) and of phi(K) (elu); accumulate from the item's
-                    // first MMA on
-                    for (int h = 0; h < VB; ++h) {
-                        const uint32_t d = tm + (uint32_t)h * 64u;
-                        for (int pv = 0; pv < nv; ++pv)
-                            for (int pk = 0; pk < nk; ++pk) {
-                                const uint32_t vsrc = b + (pv ? p.off_vlo : p.off_v) + h * 16384u;
-                                const uint32_t ksrc = b + (pk ? p.off_klo : 0u);
-                                const bool acc0 = k > 0 || pv > 0 || pk > 0;
-                                if (D == 64) {
-                                    // lanes 0..63: dS^T; lane 64: dz (E) or nothing (Z)
-                                    const uint32_t x = dz_mma && h == 0 && pv == 0 ? et : zt;
-                                    for (int kk = 0; kk < 8; ++kk)
-                                        mma_bf16_ss(d, mndesc(vsrc, false, x, true, kk),
-                                                    sdesc_sw128(ksrc + kk * 2048, 16, 1024), id64,
-                                                    acc0 || kk > 0);
-                                } else {
-                                    // feature block 0 -> lanes 0..63, block 1 -> 64..127
-                                    for (int kk = 0; kk < 8; ++kk)
-                                        mma_bf16_ss(d, mndesc(vsrc, false, zt, true, kk),
-                                                    sdesc_sw128(ksrc + kk * 2048, 16, 1024), id64,
-                                                    acc0 || kk > 0);
-                                    for (int kk = 0; kk < 8; ++kk)
-                                        mma_bf16_ss(d, mndesc(zb, true, vsrc, false, kk),
-                                                    sdesc_sw128(ksrc + 16384 + kk * 2048, 16, 1024),
-                                                    id64, 1);
-                                }
+                    // [dS^T] += [V']^T phi(K) over the hi/lo parts of V' (decay)
+                    // and of phi(K) (elu); accumulate from the item's first MMA
+                    for (int pv = 0; pv < nv; ++pv)
+                        for (int pk = 0; pk < nk; ++pk) {
+                            const uint32_t vsrc = b + (pv ? p.off_vlo : p.off_v);
+                            const uint32_t ksrc = b + (pk ? p.off_klo : 0u);
+                            const bool acc0 = k > 0 || pv > 0 || pk > 0;
+                            // DV = 64: lanes 64.. read the E block (lane 64 = dz) or Z
+                            const uint32_t x = dz_mma && pv == 0 ? et : zt;
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint64_t ad = VB == 2
+                                                        ? mndesc(vsrc, false, vsrc + 16384u, false, kk)
+                                                        : mndesc(vsrc, false, x, true, kk);
+                                mma_bf16_ss(tm, ad, sdesc_sw128(ksrc + kk * 2048, klbo, 1024), idD,
+                                            acc0 || kk > 0);
                             }
-                    }
-                    if (D == 128 && dz_mma) {
-                        // dz: lane 0 <- features 0..63, lane 64 <- features 64..127
-                        const uint32_t d = tm + (uint32_t)VB * 64u;
+                        }
+                    if (VB == 2 && dz_mma) {
+                        // dz in lane 0 of the next D columns
                         for (int pk = 0; pk < nk; ++pk) {
                             const uint32_t ksrc = b + (pk ? p.off_klo : 0u);
                             for (int kk = 0; kk < 8; ++kk)
-                                mma_bf16_ss(d, mndesc(eb, true, zt, true, kk),
-                                            sdesc_sw128(ksrc + kk * 2048, 16, 1024), id64,
+                                mma_bf16_ss(tm + D, mndesc(eb, true, zt, true, kk),
+                                            sdesc_sw128(ksrc + kk * 2048, klbo, 1024), idD,
                                             k > 0 || pk > 0 || kk > 0);
-                            for (int kk = 0; kk < 8; ++kk)
-                                mma_bf16_ss(d, mndesc(zb, true, et, true, kk),
-                                            sdesc_sw128(ksrc + 16384 + kk * 2048, 16, 1024),
-                                            id64, 1);
                         }
                     }
                     mma_commit(&m->free_[st]);
@@ -476,50 +499,49 @@ __global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StP
             float* dst = p.U + ((size_t)s * p.nseg + g) * (size_t)(DV * D + D);
             if (p.decay && p.zsum && t < D)
                 dst[(size_t)DV * D + t] = zdec;
-            for (int h = 0; h < VB; ++h) {
+            // lane t: value channel t (DV = 128), or t < 64 and lane 64 = dz (DV = 64)
+            float* row = nullptr;
+            if (t < DV)
+                row = dst + (size_t)t * D;
+            else if (DV == 64 && t == 64 && p.zsum && !p.decay)
+                row = dst + (size_t)DV * D;
+            for (int cb = 0; cb < D / 64; ++cb) {
                 uint32_t r[4][16];
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    tmem_ld16(tm + lane_off + (uint32_t)(h * 64 + 16 * q), r[q]);
+                    tmem_ld16(tm + lane_off + (uint32_t)(cb * 64 + 16 * q), r[q]);
                 tmem_ld_wait();
-                float* row = nullptr;
-                if (D == 64) {
-                    if (t < 64)
-                        row = dst + (size_t)(h * 64 + t) * D;
-                    else if (t == 64 && h == 0 && p.zsum && !p.decay)
-                        row = dst + (size_t)DV * D;
-                } else {
-                    row = dst + (size_t)(h * 64 + (t & 63)) * D + (t >> 6) * 64;
-                }
                 if (row) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            *reinterpret_cast<float4*>(row + 16 * q + 4 * e) =
+                            *reinterpret_cast<float4*>(row + cb * 64 + 16 * q + 4 * e) =
                                 make_float4(__uint_as_float(r[q][4 * e]),
                                             __uint_as_float(r[q][4 * e + 1]),
                                             __uint_as_float(r[q][4 * e + 2]),
                                             __uint_as_float(r[q][4 * e + 3]));
                 }
             }
-            if (D == 128 && p.zsum && !p.decay && (wq == 0 || wq == 2)) {
-                uint32_t r[4][16];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    tmem_ld16(tm + lane_off + (uint32_t)(VB * 64 + 16 * q), r[q]);
-                tmem_ld_wait();
-                if ((t & 63) == 0) {
-                    float* row = dst + (size_t)DV * D + (t >> 6) * 64;
+            if (VB == 2 && p.zsum && !p.decay && wq == 0) {
+                for (int cb = 0; cb < D / 64; ++cb) {
+                    uint32_t r[4][16];
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
+                        tmem_ld16(tm + lane_off + (uint32_t)(D + cb * 64 + 16 * q), r[q]);
+                    tmem_ld_wait();
+                    if (t == 0) {
+                        float* zr = dst + (size_t)DV * D + cb * 64;
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            *reinterpret_cast<float4*>(row + 16 * q + 4 * e) =
-                                make_float4(__uint_as_float(r[q][4 * e]),
-                                            __uint_as_float(r[q][4 * e + 1]),
-                                            __uint_as_float(r[q][4 * e + 2]),
-                                            __uint_as_float(r[q][4 * e + 3]));
+                        for (int q = 0; q < 4; ++q)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                *reinterpret_cast<float4*>(zr + 16 * q + 4 * e) =
+                                    make_float4(__uint_as_float(r[q][4 * e]),
+                                                __uint_as_float(r[q][4 * e + 1]),
+                                                __uint_as_float(r[q][4 * e + 2]),
+                                                __uint_as_float(r[q][4 * e + 3]));
+                    }
                 }
             }
             tc_fence_before();
@@ -555,22 +577,22 @@ struct ScanParams {
     GammaTable g;
 };
 
-// One thread per (sequence, value tile h, row r, 8 features); rows 0..63 are
+// One thread per (sequence, value tile h, row r, 4 features); rows 0..63 are
 // value channels (S^T), row 64 the normaliser, rows 65..79 of a normalised
 // image zero.  The normaliser row of tiles h > 0 repeats tile 0's (each
 // output tile divides by it).
 __global__ void __launch_bounds__(128) k_tg_scan(const __grid_constant__ ScanParams p)
 {
-    const int ntile = p.DV / kT, IR = img_rows(p.norm), F8 = p.D / 8;
+    const int ntile = p.DV / kT, IR = img_rows(p.norm), F4 = p.D / 4;
     const int RR = p.norm ? IR : (p.zsum ? 65 : 64);  // rows carried by threads
-    const int per_seq = ntile * RR * F8;
+    const int per_seq = ntile * RR * F4;
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (gid >= (int64_t)p.BH * per_seq)
         return;
     const int s = (int)(gid / per_seq);
     int rem = (int)(gid % per_seq);
-    const int f8 = rem % F8;
-    rem /= F8;
+    const int f4 = rem % F4;
+    rem /= F4;
     const int r = rem % RR, h = rem / RR;
     const int head = s % p.H;
     const bool zrow = p.zsum && r == 64;
@@ -578,55 +600,77 @@ __global__ void __launch_bounds__(128) k_tg_scan(const __grid_constant__ ScanPar
     const bool data = r < 64 || zrow;
     const int c = h * kT + r;  // value channel (r < 64)
     const size_t E = (size_t)p.DV * p.D + p.D;
-    const size_t src_off = zrow ? (size_t)p.DV * p.D + f8 * 8 : (size_t)c * p.D + f8 * 8;
+    const size_t src_off = zrow ? (size_t)p.DV * p.D + f4 * 4 : (size_t)c * p.D + f4 * 4;
 
-    float acc[8];
+    float acc[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
+    for (int e = 0; e < 4; ++e)
         acc[e] = 0.f;
     if (data && p.S0) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int f = f8 * 8 + e;
+        for (int e = 0; e < 4; ++e) {
+            const int f = f4 * 4 + e;
             acc[e] = zrow ? p.z0[(size_t)s * p.D + f] : p.S0[((size_t)s * p.D + f) * p.DV + c];
         }
     }
+    // normalised maps: a hi image then a lo image, each of D/64 blocks of IR
+    // rows; the unnormalised map: per block the 64 hi rows then the 64 lo
+    // rows (one N = 128 operand)
     const size_t part = (size_t)(p.D / 64) * IR * 128;
-    const uint32_t off = (uint32_t)(f8 >> 3) * (uint32_t)IR * 128u + sw128_off(r, f8 & 7);
+    const int f8 = f4 >> 1;  // 16-byte chunk; this thread writes its half (f4 & 1)
+    const uint32_t off = (p.norm ? (uint32_t)(f8 >> 3) * (uint32_t)IR * 128u
+                                 : (uint32_t)(f8 >> 3) * 16384u) +
+                         sw128_off(r, f8 & 7) + 8u * (uint32_t)(f4 & 1);
+    const size_t lo_delta = p.norm ? part : 8192;
     auto write_img = [&](size_t index) {
         if (!in_img)
             return;
         unsigned char* base = p.img + (index * 2) * part;
-        uint4 hi = make_uint4(0, 0, 0, 0), lo = hi;
-        if (data)
-            split8(acc, hi, lo);
-        *reinterpret_cast<uint4*>(base + off) = hi;
-        *reinterpret_cast<uint4*>(base + part + off) = lo;
+        uint2 hi = make_uint2(0, 0), lo = hi;
+        if (data) {
+            split2(acc[0], acc[1], hi.x, lo.x);
+            split2(acc[2], acc[3], hi.y, lo.y);
+        }
+        *reinterpret_cast<uint2*>(base + off) = hi;
+        *reinterpret_cast<uint2*>(base + lo_delta + off) = lo;
     };
     const float* u = p.U ? p.U + (size_t)s * p.nseg * E + src_off : nullptr;
-    for (int g = 0; g < p.nseg; ++g) {
-        if (p.img && p.img_per_seg)
-            write_img(((size_t)s * p.nseg + g) * ntile + h);
-        if (data && p.U) {
-            const float4 a = *reinterpret_cast<const float4*>(u + (size_t)g * E);
-            const float4 b = *reinterpret_cast<const float4*>(u + (size_t)g * E + 4);
-            float dec = 1.0f;
-            if (p.decay) {
-                const int64_t len = min((int64_t)p.L * kC, p.N - (int64_t)g * p.L * kC);
-                dec = exp2f((float)len * p.g.log2g[head]);
+    const bool add = data && p.U;
+    const float l2g = p.decay ? p.g.log2g[head] : 0.f;
+    constexpr int kAhead = 8;  // segments whose aggregates are in flight at once
+    float4 buf[kAhead];
+#pragma unroll
+    for (int i = 0; i < kAhead; ++i)
+        if (add && i < p.nseg)
+            buf[i] = __ldcg(reinterpret_cast<const float4*>(u + (size_t)i * E));
+    for (int g0 = 0; g0 < p.nseg; g0 += kAhead) {
+#pragma unroll
+        for (int i = 0; i < kAhead; ++i) {
+            const int g = g0 + i;
+            if (g >= p.nseg)
+                break;
+            if (p.img && p.img_per_seg)
+                write_img(((size_t)s * p.nseg + g) * ntile + h);
+            if (add) {
+                const float4 a = buf[i];
+                if (g + kAhead < p.nseg)
+                    buf[i] = __ldcg(reinterpret_cast<const float4*>(u + (size_t)(g + kAhead) * E));
+                float dec = 1.0f;
+                if (p.decay) {
+                    const int64_t len = min((int64_t)p.L * kC, p.N - (int64_t)g * p.L * kC);
+                    dec = exp2f((float)len * l2g);
+                }
+                acc[0] = fmaf(dec, acc[0], a.x), acc[1] = fmaf(dec, acc[1], a.y);
+                acc[2] = fmaf(dec, acc[2], a.z), acc[3] = fmaf(dec, acc[3], a.w);
             }
-            acc[0] = fmaf(dec, acc[0], a.x), acc[1] = fmaf(dec, acc[1], a.y);
-            acc[2] = fmaf(dec, acc[2], a.z), acc[3] = fmaf(dec, acc[3], a.w);
-            acc[4] = fmaf(dec, acc[4], b.x), acc[5] = fmaf(dec, acc[5], b.y);
-            acc[6] = fmaf(dec, acc[6], b.z), acc[7] = fmaf(dec, acc[7], b.w);
         }
     }
     if (p.img && !p.img_per_seg)
         write_img((size_t)s * ntile + h);
     if (data && p.S_out) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int f = f8 * 8 + e;
+        for (int e = 0; e < 4; ++e) {
+            const int f = f4 * 4 + e;
             if (zrow) {
                 if (p.z_out)
                     p.z_out[(size_t)s * p.D + f] = acc[e];
@@ -655,18 +699,19 @@ struct OutParams {
 template <int D>
 struct OutLayout {
     static constexpr int KB = D / 64;
-    static constexpr int NQ = 2;
+    static constexpr int NQ = D == 64 ? 2 : 1;  // Q stages (Q is reloaded from L2 after a prefetch)
     static constexpr int NKV = D == 64 ? 3 : 2;
     static constexpr uint32_t OFF_ZB = 0, OFF_EB = 2048;       // Z, E below every tile
-    static constexpr uint32_t OFF_Q = 4096;                    // NQ x KB x 16 KiB
+    static constexpr uint32_t OFF_Q = 4096;                     // NQ x KB x 16 KiB
     static constexpr uint32_t OFF_K = OFF_Q + NQ * KB * 16384;  // NKV x KB x 16 KiB
     static constexpr uint32_t OFF_V = OFF_K + NKV * KB * 16384; // NKV x 16 KiB (one value tile)
-    static constexpr uint32_t OFF_VLO = OFF_V + NKV * 16384;   // lo part of the decayed values
-    static constexpr uint32_t OFF_S = OFF_VLO + 16384;         // [S^T; z] hi then lo
+    static constexpr uint32_t OFF_VH = OFF_V + NKV * 16384;    // decayed values, hi
+    static constexpr uint32_t OFF_VL = OFF_VH + 16384;         // decayed values, lo
+    static constexpr uint32_t OFF_S = OFF_VL + 16384;          // [S^T; z] hi then lo
     static constexpr uint32_t SPART_MAX = KB * 80 * 128;
     static constexpr uint32_t OFF_ZT = OFF_S + 2 * SPART_MAX;  // Z, E above every tile
     static constexpr uint32_t OFF_ET = OFF_ZT + 2048;
-    static constexpr uint32_t OFF_PW = OFF_ET + 2048;          // gamma^n, n = 0..127
+    static constexpr uint32_t OFF_PW = OFF_ET + 2048;          // gamma^-(j+1), j = 0..127
     static constexpr uint32_t OFF_MISC = OFF_PW + 512;
     static constexpr uint32_t SMEM = OFF_MISC + 1024 + 1024;
     static_assert(SMEM <= 232448, "shared memory");
@@ -675,14 +720,15 @@ struct OutLayout {
 struct OutMisc {
     uint64_t qfull[2], qfree[2], phid[2];
     uint64_t kvfull[3], kvfree[3];
-    uint64_t sdone[2], pdone[2], accfull[2], accfree[2], pvd[2], prepd[2], dsd[2], pfree[2];
-    uint64_t simg, sfree, drain;
+    uint64_t sdone[2], pdone[2], pvd[2], ind[2], accfull[2], accfree[2];
+    uint64_t prepd[2], dsd[2], upd[2];
+    uint64_t simg, sfree, drain_o, drain_s;
     uint32_t tmem;
     int abort;
 };
 
-// tensor memory: P[b] (scores, then P hi/lo, then the chunk's state
-// increment) at 128 b; the output accumulators at 256 + 128 b
+// tensor memory: P[b] (scores, then P hi/lo) at 128 b; the output
+// accumulators at 256 + ACCW a; the chunk's state increment after them
 constexpr uint32_t TM_P = 0, TM_ACC = 256;
 
 // Walks the work items of this CTA (item = blockIdx.x + j * gridDim.x) and
@@ -726,11 +772,45 @@ struct Iter {
     __device__ __forceinline__ bool last() const { return k == n - 1; }
 };
 
+// A 128-token row t of a 64-channel value block scaled by w and split into
+// bf16 hi and lo parts in two other blocks (same swizzled positions).
+__device__ __forceinline__ void decay_row(const unsigned char* v, unsigned char* vhi,
+                                          unsigned char* vlo, int t, float w)
+{
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint32_t off = sw128_off(t, c);
+        float x[8];
+        unpack8(*reinterpret_cast<const uint4*>(v + off), x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            x[e] *= w;
+        uint4 hi, lo;
+        split8(x, hi, lo);
+        *reinterpret_cast<uint4*>(vhi + off) = hi;
+        *reinterpret_cast<uint4*>(vlo + off) = lo;
+    }
+}
+
+// The CTA is warp-specialised; work flows through shared-memory stages and
+// tensor-memory buffers, synchronised by mbarriers:
+//   warp 0      producer (one thread): the state image of each item, Q, K, V
+//               of each chunk, and an L2 prefetch a few chunks ahead
+//   warp 1      output MMAs (one thread): scores, P [V | 1]
+//   warp 2      state MMAs (one thread): phi(Q) [S^T; z], the state increment
+//   warp 3      decayed values V' = gamma^(C-1-t) V as bf16 hi/lo (decay only)
+//   warps 4-7   feature map in place, then P from the scores
+//   warps 8-11  epilogue
+//   warps 12-15 the state update S <- gamma^C S + dS in the operand image
+// The output chain (scores -> P -> P [V | 1] -> epilogue) and the state
+// chain (state increment -> update -> phi(Q) [S^T; z] of the next chunk) meet
+// only in the shared accumulator: P [V | 1] of a chunk waits until
+// phi(Q) [S^T; z] of that chunk is complete.
 template <int D>
 __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutParams p)
 {
     using LY = OutLayout<D>;
-    constexpr int KB = LY::KB, NKV = LY::NKV;
+    constexpr int KB = LY::KB, NQ = LY::NQ, NKV = LY::NKV;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -740,12 +820,28 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
     const int IR = img_rows(p.norm);
     const uint32_t spart = (uint32_t)KB * (uint32_t)IR * 128u;
     const bool causal = p.causal != 0;
+    // accumulator columns per buffer, buffers, and the state-increment region
+    const int ACCW = p.norm ? 80 : 64;
+    // the state increment: D = 64: lanes 0..63 value channels, lane 64 dz,
+    // 64 columns; D = 128: features 0..63 in lanes 0..63 and 64..127 in lanes
+    // 64..127 (so that four warps share the update), 64 columns, and for
+    // normalised maps dz in lanes 0 and 64 of 64 more columns
+    // (with decay, D = 128: lanes 0..63 the V'_hi part and 64..127 the V'_lo
+    // part of all 128 features, 128 columns)
+    const int DSW = D == 64 ? 64 : (p.norm || p.decay ? 128 : 64);
+    const int NACC = 256 + 2 * ACCW + DSW <= 512 ? 2 : 1;
+    const uint32_t TM_DS = TM_ACC + (uint32_t)(NACC * ACCW);
 
     if (tid == 0) {
         uint64_t* bars = reinterpret_cast<uint64_t*>(m);
         const int nbars = (int)(offsetof(OutMisc, tmem) / sizeof(uint64_t));
         for (int i = 0; i < nbars; ++i)
             mbar_init(&bars[i], 1);
+        // stages read by both MMA threads are released by both
+        for (int i = 0; i < 2; ++i)
+            mbar_init(&m->qfree[i], causal ? 2 : 1);
+        for (int i = 0; i < 3; ++i)
+            mbar_init(&m->kvfree[i], 2);
         m->abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&p.mq);
@@ -765,7 +861,7 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = m->tmem;
-    auto qst = [&](int u) { return sm + LY::OFF_Q + (uint32_t)(u & 1) * KB * 16384u; };
+    auto qst = [&](int u) { return sm + LY::OFF_Q + (uint32_t)(u % NQ) * KB * 16384u; };
     auto kst = [&](int u) { return sm + LY::OFF_K + (uint32_t)(u % NKV) * KB * 16384u; };
     auto vst = [&](int u) { return sm + LY::OFF_V + (uint32_t)(u % NKV) * 16384u; };
     unsigned char* s_hi = sm + LY::OFF_S;
@@ -773,16 +869,31 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
 
     if (warp == 0) {
         // ------------------------------------------------ producer --------
-        // Three load streams advanced as their slots free up: the state image
-        // of each item, Q of each chunk, K and V of each chunk.
         if (lane == 0) {
             const uint64_t stream = policy_evict_first();
             const uint64_t keep = policy_evict_last();
-            Iter iq, ikv;
+            Iter iq, ikv, ipf;
             iq.start(p);
             ikv.start(p);
+            ipf.start(p);
             if (!causal)
                 ikv.done = true;
+            // L2 prefetch of the chunk kPrefetch ahead of the Q stream: the
+            // tiled loads then wait on L2, not on HBM
+            auto prefetch = [&](const Iter& c) {
+                const int row = (c.c0 + c.k) * kC;
+                for (int kb = 0; kb < KB; ++kb)
+                    tma_prefetch_l2_3d(&p.mq, 64 * kb, row, c.s);
+                if (causal) {
+                    for (int kb = 0; kb < KB; ++kb)
+                        tma_prefetch_l2_3d(&p.mk, 64 * kb, row, c.s);
+                    tma_prefetch_l2_3d(&p.mv, kT * c.h, row, c.s);
+                }
+            };
+            for (int i = 0; i < kPrefetch && !ipf.done; ++i) {
+                prefetch(ipf);
+                ipf.advance(p);
+            }
             int jimg = 0;
             bool img_done = false;
             int q_ph[2] = {-1, -1}, kv_ph[3] = {-1, -1, -1}, img_ph = -1;
@@ -808,16 +919,21 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
                     }
                 }
                 if (!iq.done) {
-                    const int qs = iq.u & 1;
-                    if (iq.u < 2 || mbar_test_wait(&m->qfree[qs], ((iq.u >> 1) & 1) ^ 1)) {
+                    const int qs = iq.u % NQ;
+                    if (iq.u < NQ || mbar_test_wait(&m->qfree[qs], ((iq.u / NQ) & 1) ^ 1)) {
                         mbar_arrive_expect_tx(&m->qfull[qs], KB * 16384u);
                         unsigned char* dst = qst(iq.u);
                         const int row = (iq.c0 + iq.k) * kC;
                         for (int kb = 0; kb < KB; ++kb)
                             tma_load_3d(dst + kb * 16384, &p.mq, 64 * kb, row, iq.s, &m->qfull[qs],
                                         stream);
-                        q_ph[qs] = (iq.u >> 1) & 1;
+                        q_ph[qs] = (iq.u / NQ) & 1;
+                        TG_TRACE(iq.u, 0);
                         iq.advance(p);
+                        if (!ipf.done) {
+                            prefetch(ipf);
+                            ipf.advance(p);
+                        }
                         prog = true;
                     }
                 }
@@ -833,6 +949,7 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
                         tma_load_3d(vst(ikv.u), &p.mv, kT * ikv.h, row, ikv.s, &m->kvfull[ks],
                                     stream);
                         kv_ph[ks] = (ikv.u / NKV) & 1;
+                        TG_TRACE(ikv.u, 1);
                         ikv.advance(p);
                         prog = true;
                     }
@@ -853,7 +970,7 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
                 }
             }
             if (*abort) {  // every load this thread issued lands before exit
-                for (int i = 0; i < 2; ++i)
+                for (int i = 0; i < NQ; ++i)
                     if (q_ph[i] >= 0)
                         tg_drain(&m->qfull[i], q_ph[i]);
                 for (int i = 0; i < NKV; ++i)
@@ -864,153 +981,64 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer ------
-        // Four streams, each in chunk order, issued as their inputs are ready:
-        // SC scores, IN phi(Q) [S^T; z], PV P [V | 1], DS the state increment.
-        if (lane == 0) {
+        // ---------------------------------------------- output MMAs -------
+        // Two streams in chunk order, each issued as its inputs are ready:
+        // SC scores into P[b]; PV P [V | 1] into the accumulator once the
+        // chunk's phi(Q) [S^T; z] is complete.
+        if (lane == 0 && causal) {
             const uint32_t id_sc = idesc_bf16_f32(128, 128, false, false);
-            const uint32_t id_in = idesc_bf16_f32(128, IR, false, false);
             const uint32_t id_pv = idesc_bf16_f32(128, IR, false, true);
-            const uint32_t id64 = idesc_bf16_f32(128, 64, true, true);
-            const uint32_t zb = smem_addr(sm + LY::OFF_ZB), eb = smem_addr(sm + LY::OFF_EB);
-            const uint32_t zt = smem_addr(sm + LY::OFF_ZT), et = smem_addr(sm + LY::OFF_ET);
-            const uint32_t shi = smem_addr(s_hi), slo = smem_addr(s_lo);
-            const uint32_t vlo = smem_addr(sm + LY::OFF_VLO);
-            Iter sc, in, pv, ds;
+            const uint32_t et = smem_addr(sm + LY::OFF_ET);
+            Iter sc, pv;
             sc.start(p);
-            in.start(p);
             pv.start(p);
-            ds.start(p);
-            if (!causal)
-                sc.done = pv.done = ds.done = true;
             bool issued = false;
             uint64_t idle_since = 0;
-            while (!(sc.done && in.done && pv.done && ds.done)) {
+            while (!(sc.done && pv.done)) {
                 bool prog = false;
-                // ---- scores
                 if (!sc.done) {
                     const int u = sc.u, b = u & 1;
-                    if (mbar_test_wait(&m->qfull[u & 1], (u >> 1) & 1) &&
+                    if (mbar_test_wait(&m->qfull[u % NQ], (u / NQ) & 1) &&
                         mbar_test_wait(&m->kvfull[u % NKV], (u / NKV) & 1) &&
-                        (!p.elu || mbar_test_wait(&m->phid[u & 1], (u >> 1) & 1)) &&
-                        (u < 2 || mbar_test_wait(&m->pfree[b], ((u - 2) >> 1) & 1))) {
+                        (!p.elu || mbar_test_wait(&m->phid[u % NQ], (u / NQ) & 1)) &&
+                        (u < 2 || mbar_test_wait(&m->pvd[b], ((u - 2) >> 1) & 1))) {
+                        TG_TRACE(u, 15);
                         tc_fence_after();
                         const uint32_t qa = smem_addr(qst(u)), ka = smem_addr(kst(u));
                         for (int kk = 0; kk < D / 16; ++kk)
                             mma_bf16_ss(tm + TM_P + 128 * b, kdesc(qa, 128, kk), kdesc(ka, 128, kk),
                                         id_sc, kk > 0);
                         mma_commit(&m->sdone[b]);
-                        if (in.u > u)
-                            mma_commit(&m->qfree[u & 1]);
+                        mma_commit(&m->qfree[u % NQ]);
                         issued = true;
+                        TG_TRACE(u, 2);
                         sc.advance(p);
                         prog = true;
                     }
                 }
-                // ---- inter: phi(Q) [S^T; z] (hi, lo)
-                if (!in.done) {
-                    const int u = in.u, b = u & 1;
-                    const bool s_ready =
-                        in.first() ? mbar_test_wait(&m->simg, in.j & 1)
-                                   : mbar_test_wait(&m->pfree[(u - 1) & 1], ((u - 1) >> 1) & 1);
-                    if (mbar_test_wait(&m->qfull[u & 1], (u >> 1) & 1) &&
-                        (!p.elu || mbar_test_wait(&m->phid[u & 1], (u >> 1) & 1)) && s_ready &&
-                        (u < 2 || mbar_test_wait(&m->accfree[b], ((u - 2) >> 1) & 1))) {
-                        tc_fence_after();
-                        const uint32_t qa = smem_addr(qst(u));
-                        const uint32_t d = tm + TM_ACC + 128 * b;
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            mma_bf16_ss(d, kdesc(qa, 128, kk), kdesc(shi, IR, kk), id_in, kk > 0);
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            mma_bf16_ss(d, kdesc(qa, 128, kk), kdesc(slo, IR, kk), id_in, 1);
-                        if (!causal || sc.u > u)
-                            mma_commit(&m->qfree[u & 1]);
-                        if (!causal || pv.u > u)
-                            mma_commit(&m->accfull[b]);
-                        if (in.last())
-                            mma_commit(&m->sfree);
-                        issued = true;
-                        in.advance(p);
-                        prog = true;
-                    }
-                }
-                // ---- intra: P [V | 1] (P hi, lo from tensor memory)
                 if (!pv.done) {
-                    const int u = pv.u, b = u & 1;
-                    const bool acc_ok = p.decay ? (u < 2 || mbar_test_wait(&m->accfree[b],
-                                                                           ((u - 2) >> 1) & 1))
-                                                : in.u > u;
-                    if (acc_ok && mbar_test_wait(&m->pdone[b], (u >> 1) & 1) &&
+                    const int u = pv.u, b = u & 1, a = u % NACC;
+                    if (mbar_test_wait(&m->pdone[b], (u >> 1) & 1) &&
+                        mbar_test_wait(&m->ind[b], (u >> 1) & 1) &&
                         mbar_test_wait(&m->kvfull[u % NKV], (u / NKV) & 1)) {
+                        TG_TRACE(u, 17);
                         tc_fence_after();
                         const uint32_t va = smem_addr(vst(u));
-                        const uint32_t d = tm + TM_ACC + 128 * b + (p.decay ? 64 : 0);
+                        const uint32_t d = tm + TM_ACC + (uint32_t)(ACCW * a);
                         const uint32_t pa = tm + TM_P + 128 * b;
                         for (int ps = 0; ps < 2; ++ps)
                             for (int kk = 0; kk < 8; ++kk) {
                                 const uint64_t bd = p.norm ? mndesc(va, false, et, true, kk)
                                                            : sdesc_sw128(va + kk * 2048, 16, 1024);
                                 mma_bf16_ts(d, pa + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * ps, bd,
-                                            id_pv, p.decay ? (ps > 0 || kk > 0) : 1);
+                                            id_pv, 1);
                             }
                         mma_commit(&m->pvd[b]);
-                        if (in.u > u)
-                            mma_commit(&m->accfull[b]);
-                        if (pv.last()) {  // no state update after an item's last chunk
-                            mma_commit(&m->dsd[b]);
-                            mma_commit(&m->kvfree[u % NKV]);
-                        }
-                        issued = true;
-                        pv.advance(p);
-                        prog = true;
-                    }
-                }
-                // ---- the chunk's state increment [V' | 1]^T phi(K) into P[b]
-                if (!ds.done) {
-                    const int u = ds.u, b = u & 1;
-                    if (ds.last()) {
-                        if (pv.u > u) {
-                            ds.advance(p);
-                            prog = true;
-                        }
-                    } else if (pv.u > u && in.u > u &&
-                               mbar_test_wait(&m->pvd[b], (u >> 1) & 1) &&
-                               (!p.decay || mbar_test_wait(&m->prepd[b], (u >> 1) & 1))) {
-                        tc_fence_after();
-                        const uint32_t ka = smem_addr(kst(u)), va = smem_addr(vst(u));
-                        const uint32_t d = tm + TM_P + 128 * b;
-                        const int npass = p.decay ? 2 : 1;
-                        for (int ps = 0; ps < npass; ++ps) {
-                            const uint32_t vsrc = ps ? vlo : va;
-                            if (D == 64) {
-                                const uint32_t x = (p.norm && ps == 0) ? et : zt;
-                                for (int kk = 0; kk < 8; ++kk)
-                                    mma_bf16_ss(d, mndesc(vsrc, false, x, true, kk),
-                                                sdesc_sw128(ka + kk * 2048, 16, 1024), id64,
-                                                ps > 0 || kk > 0);
-                            } else {
-                                for (int kk = 0; kk < 8; ++kk)
-                                    mma_bf16_ss(d, mndesc(vsrc, false, zt, true, kk),
-                                                sdesc_sw128(ka + kk * 2048, 16, 1024), id64,
-                                                ps > 0 || kk > 0);
-                                for (int kk = 0; kk < 8; ++kk)
-                                    mma_bf16_ss(d, mndesc(zb, true, vsrc, false, kk),
-                                                sdesc_sw128(ka + 16384 + kk * 2048, 16, 1024),
-                                                id64, 1);
-                            }
-                        }
-                        if (D == 128 && p.norm) {
-                            for (int kk = 0; kk < 8; ++kk)
-                                mma_bf16_ss(d + 64, mndesc(eb, true, zt, true, kk),
-                                            sdesc_sw128(ka + kk * 2048, 16, 1024), id64, kk > 0);
-                            for (int kk = 0; kk < 8; ++kk)
-                                mma_bf16_ss(d + 64, mndesc(zb, true, et, true, kk),
-                                            sdesc_sw128(ka + 16384 + kk * 2048, 16, 1024), id64, 1);
-                        }
-                        mma_commit(&m->dsd[b]);
+                        mma_commit(&m->accfull[a]);
                         mma_commit(&m->kvfree[u % NKV]);
                         issued = true;
-                        ds.advance(p);
+                        TG_TRACE(u, 4);
+                        pv.advance(p);
                         prog = true;
                     }
                 }
@@ -1029,8 +1057,138 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
                 }
             }
             if (issued && *abort) {
-                mma_commit(&m->drain);
-                tg_drain(&m->drain, 0);
+                mma_commit(&m->drain_o);
+                tg_drain(&m->drain_o, 0);
+            }
+        }
+    } else if (warp == 2) {
+        // ----------------------------------------------- state MMAs -------
+        // Per chunk in order: IN phi(Q) [S^T; z] (hi, lo) into the
+        // accumulator, then DS the chunk's state increment [V' | x]^T phi(K)
+        // into its own region (lanes 0..63 = value channels, lane 64 = dz
+        // through E for normalised maps; columns = the D features).
+        if (lane == 0) {
+            const uint32_t id_in = idesc_bf16_f32(128, IR, false, false);
+            const uint32_t id64 = idesc_bf16_f32(128, 64, true, true);
+            const uint32_t id128 = idesc_bf16_f32(128, 128, true, true);
+            const uint32_t zb = smem_addr(sm + LY::OFF_ZB), eb = smem_addr(sm + LY::OFF_EB);
+            const uint32_t zt = smem_addr(sm + LY::OFF_ZT), et = smem_addr(sm + LY::OFF_ET);
+            const uint32_t shi = smem_addr(s_hi), slo = smem_addr(s_lo);
+            const uint32_t vhi = smem_addr(sm + LY::OFF_VH), vlo = smem_addr(sm + LY::OFF_VL);
+            Iter w;
+            w.start(p);
+            bool ok = true, issued = false;
+            while (ok && !w.done) {
+                const int u = w.u, b = u & 1, a = u % NACC;
+                // ---- IN
+                bool okw = tg_wait(&m->qfull[u % NQ], (u / NQ) & 1, abort);
+                if (okw && p.elu)
+                    okw = tg_wait(&m->phid[u % NQ], (u / NQ) & 1, abort);
+                // the state before the chunk: the item's image, or (causal) the
+                // previous chunk's update
+                if (okw && w.first())
+                    okw = tg_wait(&m->simg, w.j & 1, abort);
+                else if (okw && causal)
+                    okw = tg_wait(&m->upd[(u - 1) & 1], ((u - 1) >> 1) & 1, abort);
+                if (okw && u >= NACC)
+                    okw = tg_wait(&m->accfree[a], ((u / NACC) & 1) ^ 1, abort);
+                if (!okw) {
+                    ok = false;
+                    break;
+                }
+                TG_TRACE(u, 16);
+                tc_fence_after();
+                const uint32_t qa = smem_addr(qst(u));
+                const uint32_t d = tm + TM_ACC + (uint32_t)(ACCW * a);
+                if (p.norm) {
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_bf16_ss(d, kdesc(qa, 128, kk), kdesc(shi, IR, kk), id_in, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_bf16_ss(d, kdesc(qa, 128, kk), kdesc(slo, IR, kk), id_in, 1);
+                } else {  // per block: hi rows 0..63, lo rows 64..127
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_bf16_ss(d, kdesc(qa, 128, kk), kdesc(shi, 128, kk), id_in, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_bf16_ss(d, kdesc(qa, 128, kk), kdesc(shi + 8192u, 128, kk), id_in, 1);
+                }
+                mma_commit(&m->ind[b]);
+                mma_commit(&m->qfree[u % NQ]);
+                if (!causal)
+                    mma_commit(&m->accfull[a]);
+                if (w.last())
+                    mma_commit(&m->sfree);
+                issued = true;
+                TG_TRACE(u, 3);
+                // ---- DS
+                if (causal) {
+                    // the increment region holds no unread increment (this wait
+                    // also keeps dsd from running two phases ahead of the update
+                    // warps when items are one chunk long)
+                    okw = u < 1 || tg_wait(&m->upd[(u - 1) & 1], ((u - 1) >> 1) & 1, abort);
+                    if (!okw) {
+                        ok = false;
+                        break;
+                    }
+                    if (!w.last()) {
+                        okw = tg_wait(&m->kvfull[u % NKV], (u / NKV) & 1, abort);
+                        if (okw && p.decay)
+                            okw = tg_wait(&m->prepd[b], (u >> 1) & 1, abort);
+                        if (!okw) {
+                            ok = false;
+                            break;
+                        }
+                        TG_TRACE(u, 18);
+                        tc_fence_after();
+                        const uint32_t ka = smem_addr(kst(u)), va = smem_addr(vst(u));
+                        // D = 128 with decay: [V'_hi | V'_lo]^T phi(K), one N = 128 MMA
+                        // per K step (the halves are added by the update warps)
+                        const int npass = D == 128 && p.decay ? 0 : (p.decay ? 2 : 1);
+                        if (D == 128 && p.decay)
+                            for (int kk = 0; kk < 8; ++kk)
+                                mma_bf16_ss(tm + TM_DS, mndesc(vhi, false, vlo, false, kk),
+                                            sdesc_sw128(ka + kk * 2048, 16384, 1024), id128, kk > 0);
+                        for (int ps = 0; ps < npass; ++ps) {
+                            const uint32_t vsrc = p.decay ? (ps ? vlo : vhi) : va;
+                            if (D == 64) {
+                                const uint32_t x = (p.norm && ps == 0) ? et : zt;
+                                for (int kk = 0; kk < 8; ++kk)
+                                    mma_bf16_ss(tm + TM_DS, mndesc(vsrc, false, x, true, kk),
+                                                sdesc_sw128(ka + kk * 2048, 16, 1024), id64,
+                                                ps > 0 || kk > 0);
+                            } else {
+                                // feature block 0 -> lanes 0..63, block 1 -> 64..127
+                                for (int kk = 0; kk < 8; ++kk)
+                                    mma_bf16_ss(tm + TM_DS, mndesc(vsrc, false, zt, true, kk),
+                                                sdesc_sw128(ka + kk * 2048, 16, 1024), id64,
+                                                ps > 0 || kk > 0);
+                                for (int kk = 0; kk < 8; ++kk)
+                                    mma_bf16_ss(tm + TM_DS, mndesc(zb, true, vsrc, false, kk),
+                                                sdesc_sw128(ka + 16384 + kk * 2048, 16, 1024),
+                                                id64, 1);
+                            }
+                        }
+                        if (D == 128 && p.norm) {
+                            // dz: lane 0 <- features 0..63, lane 64 <- features 64..127
+                            for (int kk = 0; kk < 8; ++kk)
+                                mma_bf16_ss(tm + TM_DS + 64, mndesc(eb, true, zt, true, kk),
+                                            sdesc_sw128(ka + kk * 2048, 16, 1024), id64, kk > 0);
+                            for (int kk = 0; kk < 8; ++kk)
+                                mma_bf16_ss(tm + TM_DS + 64, mndesc(zb, true, et, true, kk),
+                                            sdesc_sw128(ka + 16384 + kk * 2048, 16, 1024), id64,
+                                            1);
+                        }
+                        TG_TRACE(u, 5);
+                    }
+                    // one completion per chunk on both: the update waits for it,
+                    // and the K, V stage is released by both MMA threads
+                    mma_commit(&m->dsd[b]);
+                    mma_commit(&m->kvfree[u % NKV]);
+                }
+                w.advance(p);
+            }
+            if (issued && *abort) {
+                mma_commit(&m->drain_s);
+                tg_drain(&m->drain_s, 0);
             }
         }
     } else if (warp >= 4 && warp < 8) {
@@ -1046,12 +1204,15 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
             const int u = w.u, b = u & 1;
             const int valid = chunk_valid(p.N, w.c0 + w.k);
             if (p.decay && w.first()) {
+                // gamma^(i-j) = gamma^(i+1) gamma^-(j+1): the column factor goes
+                // into P here, the row factor into the epilogue (gamma >= 2^-1/2
+                // keeps gamma^-128 within 2^64)
                 named_bar(1, 128);  // every thread is past the previous item's P pass
-                pw[t] = exp2f((float)t * p.g.log2g[w.s % p.H]);
+                pw[t] = exp2f(-(float)(t + 1) * p.g.log2g[w.s % p.H]);
                 named_bar(1, 128);
             }
             if (p.elu) {
-                bool okw = tg_wait(&m->qfull[u & 1], (u >> 1) & 1, abort);
+                bool okw = tg_wait(&m->qfull[u % NQ], (u / NQ) & 1, abort);
                 if (causal)
                     okw = okw && tg_wait(&m->kvfull[u % NKV], (u / NKV) & 1, abort);
                 if (!group_ok(okw, 1, 128)) {
@@ -1068,8 +1229,10 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
                 }
                 fence_proxy_async_smem();
                 named_bar(1, 128);
-                if (lead)
-                    mbar_arrive(&m->phid[u & 1]);
+                if (lead) {
+                    mbar_arrive(&m->phid[u % NQ]);
+                    TG_TRACE(u, 6);
+                }
             }
             if (causal) {
                 const bool okw = tg_wait(&m->sdone[b], (u >> 1) & 1, abort);
@@ -1077,8 +1240,10 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
                     ok = false;
                     break;
                 }
+                if (lead)
+                    TG_TRACE(u, 7);
                 tc_fence_after();
-                // P = tril(scores) o gamma^(i-j) as bf16 hi/lo, in place: keys
+                // P = tril(scores) (o gamma^-(j+1)) as bf16 hi/lo, in place: keys
                 // 32q..32q+31 of row t move to columns 32q..32q+15 (hi) and
                 // 32q+16..32q+31 (lo); blocks right of the diagonal become zero.
                 const uint32_t pb = tm + TM_P + 128 * b + lane_off;
@@ -1101,10 +1266,8 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
                     }
                     if (p.decay) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int dist = t - (32 * q + e);
-                            x[e] = dist >= 0 ? x[e] * pw[dist] : 0.f;
-                        }
+                        for (int e = 0; e < 32; ++e)
+                            x[e] *= pw[32 * q + e];
                     }
 #pragma unroll
                     for (int mm = 0; mm < 8; ++mm) {
@@ -1125,17 +1288,19 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
                 tmem_st_wait();
                 tc_fence_before();
                 named_bar(1, 128);
-                if (lead)
+                if (lead) {
                     mbar_arrive(&m->pdone[b]);
+                    TG_TRACE(u, 8);
+                }
             }
             w.advance(p);
         }
     } else if (warp >= 8 && warp < 12) {
         // ------------------------------------------------ epilogue --------
-        // o = (g inter + intra) / (g den_inter + den_intra) from registers.  A
-        // 16x256b tensor-memory load gives each quad of threads 8 consecutive
-        // columns of one row; neighbours swap one pair so that every store
-        // is 16 bytes and a quad fills whole 32-byte sectors.
+        // o = num / den (normalised) or gamma^(i+1) acc (unnormalised) from
+        // registers.  A 16x256b tensor-memory load gives each quad of threads
+        // 8 consecutive columns of one row; neighbours swap one pair so that
+        // every store is 16 bytes and a quad fills whole 32-byte sectors.
         const int t = tid - 256, wq = t >> 5;
         const bool lead = t == 0;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -1144,22 +1309,24 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
         w.start(p);
         bool ok = true;
         while (ok && !w.done) {
-            const int u = w.u, b = u & 1;
-            const bool okw = tg_wait(&m->accfull[b], (u >> 1) & 1, abort);
+            const int u = w.u, a = u % NACC;
+            const bool okw = tg_wait(&m->accfull[a], (u / NACC) & 1, abort);
             if (!group_ok(okw, 2, 128)) {
                 ok = false;
                 break;
             }
+            if (lead)
+                TG_TRACE(u, 9);
             tc_fence_after();
-            const uint32_t acc = tm + TM_ACC + 128 * b + lane_off;
-            float den_row = 1.0f, g_row = 1.0f;
+            const uint32_t acc = tm + TM_ACC + (uint32_t)(ACCW * a) + lane_off;
+            float scale_row = 1.0f;
             if (p.norm) {
-                den_row = __uint_as_float(tmem_ld1(acc + 64));
+                const float den = __uint_as_float(tmem_ld1(acc + 64));
                 tmem_ld_wait();
+                scale_row = 1.0f / fmaxf(den, FLT_MIN);
+            } else if (p.decay) {
+                scale_row = exp2f((float)(t + 1) * p.g.log2g[w.s % p.H]);
             }
-            if (p.decay)
-                g_row = exp2f((float)(t + 1) * p.g.log2g[w.s % p.H]);
-            const float inv_row = p.norm ? 1.0f / fmaxf(den_row, FLT_MIN) : 1.0f;
             const int valid = chunk_valid(p.N, w.c0 + w.k);
             float* obase = p.out + ((size_t)w.s * p.N + (size_t)(w.c0 + w.k) * kC) * p.DV +
                            kT * w.h;
@@ -1168,27 +1335,10 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
                 uint32_t rr[32];
                 tmem_ld16x256b_x8(acc + ((uint32_t)(16 * h2) << 16), rr);
                 tmem_ld_wait();
-                if (p.decay) {
-                    uint32_t ra[32];
-                    tmem_ld16x256b_x8(acc + 64 + ((uint32_t)(16 * h2) << 16), ra);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int hr = 0; hr < 2; ++hr) {
-                        const float gr = __shfl_sync(full, g_row, 16 * h2 + 8 * hr + (lane >> 2));
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const int r = 4 * i + 2 * hr + e;
-                                rr[r] = __float_as_uint(
-                                    fmaf(gr, __uint_as_float(rr[r]), __uint_as_float(ra[r])));
-                            }
-                    }
-                }
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
                     const int rw = 16 * h2 + 8 * hr + (lane >> 2);  // row within the warp
-                    const float inv = __shfl_sync(full, inv_row, rw);
+                    const float sc = __shfl_sync(full, scale_row, rw);
                     const int row = 32 * wq + rw;
                     const bool odd = lane & 1;
                     float* orow = obase + (size_t)row * p.DV + 2 * ((lane & 3) & ~1);
@@ -1196,11 +1346,11 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
                     for (int i = 0; i < 8; i += 2) {
                         const float2 g0 = mul2(make_float2(__uint_as_float(rr[4 * i + 2 * hr]),
                                                            __uint_as_float(rr[4 * i + 2 * hr + 1])),
-                                               make_float2(inv, inv));
+                                               make_float2(sc, sc));
                         const float2 g1 =
                             mul2(make_float2(__uint_as_float(rr[4 * (i + 1) + 2 * hr]),
                                              __uint_as_float(rr[4 * (i + 1) + 2 * hr + 1])),
-                                 make_float2(inv, inv));
+                                 make_float2(sc, sc));
                         const float2 give = odd ? g0 : g1;
                         const float2 got = make_float2(__shfl_xor_sync(full, give.x, 1),
                                                        __shfl_xor_sync(full, give.y, 1));
@@ -1214,12 +1364,18 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
             }
             tc_fence_before();
             named_bar(2, 128);
-            if (lead)
-                mbar_arrive(&m->accfree[b]);
+            if (lead) {
+                mbar_arrive(&m->accfree[a]);
+                TG_TRACE(u, 10);
+            }
             w.advance(p);
         }
     } else if (warp >= 12 && causal) {
-        // -------------------------- decayed values and the state update ---
+        // ------------------------- decayed values and the state update ----
+        // Per chunk but an item's last: V' = gamma^(C-1-t) V as bf16 hi/lo
+        // (decay only; thread t takes token row t) once V has landed, then,
+        // once the chunk's increment is in and phi(Q) [S^T; z] has read S,
+        // S <- gamma^C S + dS in the operand image.
         const int t = tid - 384, wq = t >> 5;
         const bool lead = t == 0;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -1228,8 +1384,8 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
         bool ok = true;
         while (ok && !w.done) {
             const int u = w.u, b = u & 1;
-            if (w.last()) {  // nothing to carry: P[b] is free once its MMAs are done
-                if (lead && p.decay)  // keep one arrival per chunk on every barrier
+            if (w.last()) {  // nothing to carry into the next item
+                if (lead && p.decay)  // one arrival per chunk on every barrier
                     mbar_arrive(&m->prepd[b]);
                 const bool okw = !lead || tg_wait(&m->dsd[b], (u >> 1) & 1, abort);
                 if (!group_ok(okw, 3, 128)) {
@@ -1237,37 +1393,49 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
                     break;
                 }
                 if (lead)
-                    mbar_arrive(&m->pfree[b]);
+                    mbar_arrive(&m->upd[b]);
                 w.advance(p);
                 continue;
             }
             const float l2g = p.decay ? p.g.log2g[w.s % p.H] : 0.f;
             if (p.decay) {
-                // V' = gamma^(C-1-t) V, hi in place and lo aside, once P [V | 1] is done
-                const bool okw = tg_wait(&m->pvd[b], (u >> 1) & 1, abort);
+                // the previous increment (chunk u-1) read the V' blocks before
+                // this group updated with it, so only V must have landed
+                const bool okw = tg_wait(&m->kvfull[u % NKV], (u / NKV) & 1, abort);
                 if (!group_ok(okw, 3, 128)) {
                     ok = false;
                     break;
                 }
-                decay_block(vst(u), sm + LY::OFF_VLO, t, exp2f((float)(kC - 1 - t) * l2g));
+                if (lead)
+                    TG_TRACE(u, 11);
+                decay_row(vst(u), sm + LY::OFF_VH, sm + LY::OFF_VL, t,
+                          exp2f((float)(kC - 1 - t) * l2g));
                 fence_proxy_async_smem();
                 named_bar(3, 128);
-                if (lead)
+                if (lead) {
                     mbar_arrive(&m->prepd[b]);
+                    TG_TRACE(u, 12);
+                }
             }
-            const bool okw = tg_wait(&m->dsd[b], (u >> 1) & 1, abort);
+            // the increment is in, and phi(Q) [S^T; z] of this chunk has read S
+            bool okw = tg_wait(&m->dsd[b], (u >> 1) & 1, abort);
+            okw = okw && tg_wait(&m->ind[b], (u >> 1) & 1, abort);
             if (!group_ok(okw, 3, 128)) {
                 ok = false;
                 break;
             }
+            if (lead)
+                TG_TRACE(u, 13);
             tc_fence_after();
             // S <- gamma^C S + dS in the operand image: row r (value channel,
             // or 64 for the normaliser), 64 features of block fb
             const float dec = p.decay ? exp2f((float)kC * l2g) : 1.0f;
-            const uint32_t pb = tm + TM_P + 128 * b + lane_off;
+            const uint32_t pb = tm + TM_DS + lane_off;
             auto update_row = [&](const uint32_t (&dsv)[4][16], int r, int fb) {
-                unsigned char* hrow = s_hi + (uint32_t)fb * (uint32_t)IR * 128u;
-                unsigned char* lrow = s_lo + (uint32_t)fb * (uint32_t)IR * 128u;
+                unsigned char* hrow = p.norm ? s_hi + (uint32_t)fb * (uint32_t)IR * 128u
+                                             : s_hi + (uint32_t)fb * 16384u;
+                unsigned char* lrow = p.norm ? s_lo + (uint32_t)fb * (uint32_t)IR * 128u
+                                             : hrow + 8192;
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
                     const uint32_t off = sw128_off(r, c8);
@@ -1293,6 +1461,67 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
                     if (t < 64 || (t == 64 && p.norm))
                         update_row(dsv, t, 0);
                 }
+            } else if (p.decay) {
+                // lane c < 64 holds V'_hi^T phi(K) of channel c, lane 64 + c the
+                // V'_lo part, each for all 128 features.  Thread c keeps
+                // features 0..63 and thread 64 + c features 64..127; each hands
+                // the other half to its partner through the (now free) V' blocks.
+                float* xch = reinterpret_cast<float*>(sm + LY::OFF_VH);  // 64 x 64 x 2 fp32
+                const int c = t & 63, mine = t >> 6;
+                {
+                    uint32_t give[4][16];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        tmem_ld16(pb + 64 * (1 - mine) + 16 * q, give[q]);
+                    tmem_ld_wait();
+                    // slot (part, channel, feature): part = the sender's half
+                    float4* dst = reinterpret_cast<float4*>(xch + ((size_t)mine * 64 + c) * 64);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            dst[((4 * q + e) + c) & 15] =
+                                make_float4(__uint_as_float(give[q][4 * e]),
+                                            __uint_as_float(give[q][4 * e + 1]),
+                                            __uint_as_float(give[q][4 * e + 2]),
+                                            __uint_as_float(give[q][4 * e + 3]));
+                }
+                named_bar(3, 128);
+                const float4* src =
+                    reinterpret_cast<const float4*>(xch + ((size_t)(1 - mine) * 64 + c) * 64);
+                unsigned char* hrow = s_hi + (uint32_t)mine * 16384u;
+                unsigned char* lrow = hrow + 8192;
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {  // 16 features at a time
+                    uint32_t kp[16];
+                    tmem_ld16(pb + 64 * mine + 16 * q, kp);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int c8 = 2 * q + hh;
+                        const float4 o0 = src[((2 * c8) + c) & 15];
+                        const float4 o1 = src[((2 * c8 + 1) + c) & 15];
+                        const float dsn[8] = {__uint_as_float(kp[8 * hh]) + o0.x,
+                                              __uint_as_float(kp[8 * hh + 1]) + o0.y,
+                                              __uint_as_float(kp[8 * hh + 2]) + o0.z,
+                                              __uint_as_float(kp[8 * hh + 3]) + o0.w,
+                                              __uint_as_float(kp[8 * hh + 4]) + o1.x,
+                                              __uint_as_float(kp[8 * hh + 5]) + o1.y,
+                                              __uint_as_float(kp[8 * hh + 6]) + o1.z,
+                                              __uint_as_float(kp[8 * hh + 7]) + o1.w};
+                        const uint32_t off = sw128_off(c, c8);
+                        float o[8], l[8];
+                        unpack8(*reinterpret_cast<const uint4*>(hrow + off), o);
+                        unpack8(*reinterpret_cast<const uint4*>(lrow + off), l);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            o[e] = fmaf(dec, o[e] + l[e], dsn[e]);
+                        uint4 hi, lo;
+                        split8(o, hi, lo);
+                        *reinterpret_cast<uint4*>(hrow + off) = hi;
+                        *reinterpret_cast<uint4*>(lrow + off) = lo;
+                    }
+                }
             } else {
                 {
                     uint32_t dsv[4][16];
@@ -1315,8 +1544,10 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar(3, 128);
-            if (lead)
-                mbar_arrive(&m->pfree[b]);
+            if (lead) {
+                mbar_arrive(&m->upd[b]);
+                TG_TRACE(u, 14);
+            }
             w.advance(p);
         }
     }
@@ -1412,12 +1643,25 @@ cudaError_t launch_out(const OutParams& op, int grid, cudaStream_t st)
 
 }  // namespace
 
+#ifdef LA_TG_TRACE
+extern "C" __attribute__((visibility("default"))) int la_debug_set_tg_trace(void* buf)
+{
+    return (int)cudaMemcpyToSymbol(g_tg_trace, &buf, sizeof(buf));
+}
+#endif
+
 bool tg_eligible(const FwdArgs& a)
 {
     const bool dims = (a.d == 64 || a.d == 128) && (a.dv == 64 || a.dv == 128);
     // decay is carried only with the unnormalised map, except for state-only
-    // calls (the aggregates take any map)
-    const bool decay_ok = !a.gamma->has_decay || a.fm == LA_FM_NONE || !a.out;
+    // calls (the aggregates take any map); the forward writes gamma^(i-j) as
+    // gamma^(i+1) gamma^-(j+1), which needs gamma >= 2^-1/2 (gamma^-128 <= 2^64)
+    bool decay_ok = !a.gamma->has_decay || !a.out;
+    if (a.gamma->has_decay && a.out && a.fm == LA_FM_NONE) {
+        decay_ok = true;
+        for (int h = 0; h < a.gamma->H; ++h)
+            decay_ok = decay_ok && a.gamma->log2g[h] >= -0.5f;
+    }
     return a.dtype == LA_BF16 && dims && decay_ok && a.N >= 1 &&
            a.N <= (int64_t)INT32_MAX - kC && a.B * a.H <= (int64_t)INT32_MAX / 4;
 }
@@ -1494,7 +1738,7 @@ cudaError_t tg_run(const FwdArgs& a)
         cp.z_out = a.z_out;
         cp.g = *a.gamma;
         const int RR = norm ? img_rows(true) : (cp.zsum ? 65 : 64);
-        const int64_t threads = BH * (a.dv / kT) * RR * (a.d / 8);
+        const int64_t threads = BH * (a.dv / kT) * RR * (a.d / 4);
         const int64_t grid = (threads + 127) / 128;
         k_tg_scan<<<(unsigned)grid, 128, 0, a.stream>>>(cp);
         count_launches(1);

@@ -87,6 +87,17 @@ def test_chunked_decay(orc, d, dv, N):
     assert err <= TOL[BF], err
 
 
+def test_fast_decay_takes_the_cuda_cores(orc):
+    """gamma < 2^-1/2 is served by the CUDA-core path (the tensor-core form
+    factors gamma^(i-j) into gamma^(i+1) gamma^-(j+1)), with the same results."""
+    q, k, v = _inputs(1, 2, 700, 128, 128, "none", seed=70, scale=1 / np.sqrt(128))
+    for g in ([0.5, 0.9], [0.7072, 0.75]):
+        g = torch.tensor(g, dtype=torch.float32)
+        out = la.la_forward(q, k, v, feature_map="none", gamma=g)
+        ref = orc.forward(to_np(q), to_np(k), to_np(v), fm="none", gamma=g.double().numpy())
+        assert rel_err_rows(out, ref) <= TOL[BF]
+
+
 @pytest.mark.parametrize("B,H,N", [(1, 1, 40000), (2, 3, 9000), (1, 16, 4096)])
 def test_chunked_many_segments(orc, B, H, N):
     """Long sequences: many segments per sequence, the scan carries the state
