@@ -233,6 +233,22 @@ LA_API la_status la_forward_noalloc(const void* q, const void* k, const void* v,
 LA_API uint64_t la_launch_count(void);
 
 /*
+ * TEST HOOK, not for production use: exercises the give-up path of the
+ * single-pass tensor-core forward, whose CTAs wait on one another's published
+ * segment states.  wait_ns (> 0) replaces the 2 s limit of any single wait in
+ * that kernel; withheld_segment (>= 0) is a segment ticket (the tickets of a
+ * launch are numbered segment-major over the B*H sequences) whose aggregate
+ * and exclusive prefix are computed but never published, so that the
+ * look-backs of its successors run out of time; -1 withholds nothing.  The
+ * setting applies to later launches on the current device until changed;
+ * la_debug_set_tc_faults(2000000000, -1) restores the library's behaviour.
+ * A launch whose waits ran out records LA_ERR_TIMEOUT (la_get_device_status),
+ * every CTA drains its own copies and MMAs, frees its tensor memory and
+ * exits; the context stays usable.
+ */
+LA_API la_status la_debug_set_tc_faults(uint64_t wait_ns, int withheld_segment);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's status
  * word: LA_OK, LA_ERR_TIMEOUT or LA_ERR_DEVICE_CHECK (or LA_ERR_CUDA if the
  * synchronisation itself failed).

@@ -59,6 +59,8 @@ _lib.la_forward_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i, _i
                                     _i, _vp]
 _lib.la_forward_path.restype = ctypes.c_char_p
 _lib.la_forward_path.argtypes = [_i64, _i64, _i64, _i, _i, _i, _i, _i, _i]
+_lib.la_debug_set_tc_faults.restype = _i
+_lib.la_debug_set_tc_faults.argtypes = [ctypes.c_uint64, _i]
 _lib.la_launch_count.restype = ctypes.c_uint64
 _lib.la_launch_count.argtypes = []
 _lib.la_get_device_status.restype = _i
@@ -245,6 +247,12 @@ def la_forward_path(B, H, N, d, dv, causal=True, feature_map="elu1", has_decay=F
                     dtype=torch.bfloat16) -> str:
     return _lib.la_forward_path(B, H, N, d, dv, int(bool(causal)), _fm(feature_map),
                                 int(bool(has_decay)), DTYPES[dtype]).decode()
+
+
+def la_debug_set_tc_faults(wait_ns: int, withheld_segment: int = -1) -> None:
+    """Test hook of the single-pass kernel's give-up path (see linattn.h)."""
+    _check(_lib.la_debug_set_tc_faults(int(wait_ns), int(withheld_segment)),
+           "la_debug_set_tc_faults")
 
 
 def la_launch_count() -> int:

@@ -171,10 +171,18 @@ __device__ unsigned long long* g_tc_trace;
     } while (0)
 #endif
 
+// Test hooks of the give-up path (la_debug_set_tc_faults): the limit of any
+// single wait, and one segment ticket whose aggregate and exclusive prefix are
+// never published, so that its successors' look-backs run out of time.  The
+// library sets neither: 2 s and no ticket.
+__device__ uint64_t g_tc_wait_ns = kWaitNs;
+__device__ int g_tc_withheld_ticket = -1;
+
 // Bounded wait that also gives up as soon as another role has aborted.  The
 // first test is inline; the sleeping loop is one shared out-of-line copy.
 __device__ __noinline__ bool bwait_slow(uint64_t* bar, uint32_t parity, volatile int* abort)
 {
+    const uint64_t limit = g_tc_wait_ns;
     uint64_t t0 = 0;
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait_sleep(bar, parity, 20000u))
@@ -185,7 +193,7 @@ __device__ __noinline__ bool bwait_slow(uint64_t* bar, uint32_t parity, volatile
             const uint64_t now = globaltimer();
             if (!t0)
                 t0 = now;
-            else if (now - t0 > kWaitNs) {
+            else if (now - t0 > limit) {
                 *abort = 1;
                 return false;
             }
@@ -201,9 +209,9 @@ __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile i
 // Bounded wait used only while draining (ignores the abort flag).
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity)
 {
-    const uint64_t t0 = globaltimer();
+    const uint64_t t0 = globaltimer(), limit = g_tc_wait_ns;
     while (!mbar_try_wait(bar, parity))
-        if (globaltimer() - t0 > kWaitNs)
+        if (globaltimer() - t0 > limit)
             return;
 }
 
@@ -317,6 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
     volatile int* abort = &m->abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool norm = p.fm != LA_FM_NONE;
+    const uint64_t wait_ns = g_tc_wait_ns;
+    const int withheld = g_tc_withheld_ticket;
     const bool elu = p.fm == LA_FM_ELU1;
     const unsigned full = 0xffffffffu;
 
@@ -501,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     const uint64_t now = globaltimer();
                     if (!idle_since) {
                         idle_since = now;
-                    } else if (now - idle_since > kWaitNs) {
+                    } else if (now - idle_since > wait_ns) {
                         set_status(p.status, LA_ERR_TIMEOUT);
                         *abort = 1;
                         break;
@@ -608,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                     const uint64_t now = globaltimer();
                     if (!start)
                         start = now;
-                    if (__any_sync(full, now - start > kWaitNs || *abort)) {
+                    if (__any_sync(full, now - start > wait_ns || *abort)) {
                         n = -1;
                         break;
                     }
@@ -683,7 +693,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
             named_bar(barLB, kLB);
             if (lead) {
                 TC_TRACE(j, 23);
-                st_release(flag_base + my, (static_cast<unsigned>(gi + 1) << 2) | 2u);
+                if (t != withheld)
+                    st_release(flag_base + my, (static_cast<unsigned>(gi + 1) << 2) | 2u);
                 mbar_arrive(&m->sin_ready[j % NSIN]);
                 TC_TRACE(j, 12);
             }
@@ -772,8 +783,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fwd_tc64(const __grid_constant_
                         break;
                     if (lead) {
                         __threadfence();
-                        st_release(p.flags + static_cast<size_t>(r.gA.s) * p.R + gi % p.R,
-                                   (static_cast<unsigned>(gi + 1) << 2) | 1u);
+                        if (r.tA != withheld)
+                            st_release(p.flags + static_cast<size_t>(r.gA.s) * p.R + gi % p.R,
+                                       (static_cast<unsigned>(gi + 1) << 2) | 1u);
                         // the segment's phi(K) tiles are all in the scratch
                         bulk_wait<0>();
                         mbar_arrive(&m->phik_stored[j % NPH]);
@@ -1143,9 +1155,12 @@ TcGeom tc_geom(int64_t BH, int64_t N, int sms)
     if (G < 1)
         G = 1;
     g.G = G;
-    // segment tickets a CTA holds at once: the ring plus one being placed
-    const int64_t per_seq = ((NS + 1) * (int64_t)G + BH - 1) / BH + 2;
-    g.R = (int)std::min<int64_t>(per_seq, g.nseg);
+    // one slot per segment: a slot is written once per launch, so no reader
+    // can ever see it overwritten (a ring sized by the tickets in flight
+    // bounds the tickets held, not the span between a slow reader and the
+    // newest writer: a later segment can finish its look-back, and a yet
+    // later one publish, while an earlier one is still reading)
+    g.R = g.nseg;
     g.flags_off = 256;
     g.slots_off = (g.flags_off + sizeof(unsigned) * (size_t)BH * g.R + 255) & ~(size_t)255;
     g.sin_off = g.slots_off + sizeof(float) * (size_t)BH * g.R * kSlotFloats;
@@ -1159,8 +1174,13 @@ TcGeom tc_geom(int64_t BH, int64_t N, int sms)
 
 bool tc_forward_eligible(const FwdArgs& a)
 {
+    // the look-back list bounds this kernel to 20 CTAs per sequence; with
+    // fewer sequences than that needs to fill the GPU, the chunked path
+    // (which splits each sequence over the whole GPU) serves the call
+    const int64_t BH = a.B * a.H;
+    const int sms = sm_count() > 0 ? sm_count() : 148;
     return a.dtype == LA_BF16 && a.d == 64 && a.dv == 64 && a.causal == 1 && !a.gamma->has_decay &&
-           a.N >= 1 && a.N <= (int64_t)INT32_MAX - kC;
+           a.N >= 1 && a.N <= (int64_t)INT32_MAX - kC && BH * 20 >= sms;
 }
 
 size_t tc_forward_workspace(int64_t BH, int64_t N)
@@ -1209,6 +1229,18 @@ cudaError_t tc_forward(const FwdArgs& a)
     k_fwd_tc64<<<g.G, kThreads, SMEM_BYTES, a.stream>>>(p);
     count_launches(1);
     return cudaGetLastError();
+}
+
+// Test hook of the give-up path (declared in linattn.h).
+extern "C" __attribute__((visibility("default"))) la_status la_debug_set_tc_faults(
+    uint64_t wait_ns, int withheld_segment)
+{
+    if (wait_ns == 0)
+        return LA_ERR_INVALID_ARG;
+    if (cudaMemcpyToSymbol(g_tc_wait_ns, &wait_ns, sizeof wait_ns) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_tc_withheld_ticket, &withheld_segment, sizeof(int)) != cudaSuccess)
+        return LA_ERR_CUDA;
+    return LA_OK;
 }
 
 bool tma_map_bf16_3d(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t depth)

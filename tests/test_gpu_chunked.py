@@ -49,7 +49,8 @@ def test_paths_reported():
     assert la.la_forward_path(4, 8, 8192, 128, 128, True, "none", True, BF) == "tcgen05_chunked"
     assert la.la_forward_path(4, 8, 2048, 64, 64, False, "elu1", False, BF) == "tcgen05_chunked"
     assert la.la_forward_path(1, 1, 100, 128, 64, True, "elu1", False, BF) == "tcgen05_chunked"
-    assert la.la_forward_path(1, 1, 100, 64, 64, True, "elu1", False, BF) == "tcgen05"
+    assert la.la_forward_path(4, 8, 100, 64, 64, True, "elu1", False, BF) == "tcgen05"
+    assert la.la_forward_path(1, 1, 100, 64, 64, True, "elu1", False, BF) == "tcgen05_chunked"
     # decay with a normalised map and the d = 32 shapes stay on the CUDA cores
     assert la.la_forward_path(1, 1, 100, 64, 64, True, "elu1", True, BF) == "simt"
     assert la.la_forward_path(1, 1, 100, 32, 64, True, "elu1", False, BF) == "simt"

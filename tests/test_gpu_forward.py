@@ -180,6 +180,9 @@ def test_tensor_core_path_is_taken():
     assert la.la_forward_path(1, 1, 100, 64, 64, True, "none", True,
                               torch.bfloat16) == "tcgen05_chunked"
     assert la.la_forward_path(1, 1, 100, 64, 64, True, "elu1", False, torch.float32) == "simt"
+    # one long sequence: the chunked path uses the whole GPU
+    assert la.la_forward_path(1, 1, 1 << 20, 64, 64, True, "elu1", False,
+                              torch.bfloat16) == "tcgen05_chunked"
 
 
 @pytest.mark.parametrize("fm", ["elu1", "identity_norm", "none"])
@@ -196,9 +199,13 @@ def test_tensor_core_feature_maps(orc, fm):
     assert err <= TOL[torch.bfloat16]
 
 
-@pytest.mark.parametrize("B,H,N", [(1, 1, 40000), (3, 1, 5000), (1, 7, 3000)])
+@pytest.mark.parametrize("B,H,N", [(1, 1, 40000), (3, 1, 5000), (1, 7, 3000), (1, 8, 60000),
+                                   (2, 5, 20000)])
 def test_tensor_core_few_sequences_long(orc, B, H, N):
-    """Few sequences: many chunks of one sequence in flight at once, deep look-back."""
+    """Few sequences: with fewer than a GPU's worth the chunked path splits
+    each sequence over every SM; from eight sequences on the single-pass
+    kernel runs them, with many chunks of one sequence in flight at once and
+    deep look-backs."""
     w = synth.Workload("few", B, H, N, 64, 64, torch.bfloat16, seed_id=45)
     out, ref = _run_workload(orc, w)
     assert rel_err_rows(out, ref) <= TOL[torch.bfloat16]
