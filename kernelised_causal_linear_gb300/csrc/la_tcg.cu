@@ -577,105 +577,159 @@ struct ScanParams {
     GammaTable g;
 };
 
-// One thread per (sequence, value tile h, row r, 4 features); rows 0..63 are
+// One element = (sequence, value tile h, row r, 4 features); rows 0..63 are
 // value channels (S^T), row 64 the normaliser, rows 65..79 of a normalised
 // image zero.  The normaliser row of tiles h > 0 repeats tile 0's (each
 // output tile divides by it).
-__global__ void __launch_bounds__(128) k_tg_scan(const __grid_constant__ ScanParams p)
+//
+// The segments of a sequence are split into NP parts scanned in parallel: a
+// CTA holds kScanElems elements x NP parts, one thread each.  Each thread
+// sums its part (A = the part's aggregate, starting from 0), the parts
+// exchange (A, gamma^len) through shared memory, and each thread then walks
+// its part again from the prefix of the parts before it, writing the state
+// before every segment.  The additions within a part stay in segment order.
+constexpr int kScanThreads = 256;
+
+__global__ void __launch_bounds__(kScanThreads) k_tg_scan(const __grid_constant__ ScanParams p,
+                                                          int NP)
 {
+    __shared__ float4 part_acc[kScanThreads];
+    __shared__ float part_dec[kScanThreads];
+    const int EPC = kScanThreads / NP;  // elements per CTA
     const int ntile = p.DV / kT, IR = img_rows(p.norm), F4 = p.D / 4;
     const int RR = p.norm ? IR : (p.zsum ? 65 : 64);  // rows carried by threads
     const int per_seq = ntile * RR * F4;
-    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (gid >= (int64_t)p.BH * per_seq)
-        return;
-    const int s = (int)(gid / per_seq);
-    int rem = (int)(gid % per_seq);
+    const int el = threadIdx.x % EPC, part = threadIdx.x / EPC;
+    const int64_t gid = (int64_t)blockIdx.x * EPC + el;
+    const bool live = gid < (int64_t)p.BH * per_seq;
+    const int s = live ? (int)(gid / per_seq) : 0;
+    int rem = live ? (int)(gid % per_seq) : 0;
     const int f4 = rem % F4;
     rem /= F4;
     const int r = rem % RR, h = rem / RR;
     const int head = s % p.H;
     const bool zrow = p.zsum && r == 64;
-    const bool in_img = r < IR;
-    const bool data = r < 64 || zrow;
+    const bool data = live && (r < 64 || zrow);
+    const bool in_img = live && r < IR;
     const int c = h * kT + r;  // value channel (r < 64)
     const size_t E = (size_t)p.DV * p.D + p.D;
     const size_t src_off = zrow ? (size_t)p.DV * p.D + f4 * 4 : (size_t)c * p.D + f4 * 4;
+    const float* u = p.U && data ? p.U + (size_t)s * p.nseg * E + src_off : nullptr;
+    const float l2g = p.decay ? p.g.log2g[head] : 0.f;
+    const int SP = (p.nseg + NP - 1) / NP;  // segments per part
+    const int g0 = min(p.nseg, part * SP), g1 = min(p.nseg, g0 + SP);
+    auto seg_len = [&](int g) { return min((int64_t)p.L * kC, p.N - (int64_t)g * p.L * kC); };
+    auto seg_dec = [&](int g) { return p.decay ? exp2f((float)seg_len(g) * l2g) : 1.0f; };
+    constexpr int kAhead = 8;  // aggregates in flight per thread
 
-    float acc[4];
+    // ---- 1. this part's aggregate, from zero
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (u) {
+        for (int gb = g0; gb < g1; gb += kAhead) {
+            float4 buf[kAhead];
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-        acc[e] = 0.f;
+            for (int i = 0; i < kAhead; ++i)
+                if (gb + i < g1)
+                    buf[i] = __ldcg(reinterpret_cast<const float4*>(u + (size_t)(gb + i) * E));
+#pragma unroll
+            for (int i = 0; i < kAhead; ++i)
+                if (gb + i < g1) {
+                    const float d = seg_dec(gb + i);
+                    a.x = fmaf(d, a.x, buf[i].x), a.y = fmaf(d, a.y, buf[i].y);
+                    a.z = fmaf(d, a.z, buf[i].z), a.w = fmaf(d, a.w, buf[i].w);
+                }
+        }
+    }
+    float dpart = 1.0f;  // gamma^(tokens of the part)
+    if (p.decay && g1 > g0) {
+        int64_t toks = 0;
+        for (int g = g0; g < g1; ++g)
+            toks += seg_len(g);
+        dpart = exp2f((float)toks * l2g);
+    }
+    part_acc[threadIdx.x] = a;
+    part_dec[threadIdx.x] = dpart;
+    __syncthreads();
+    // ---- 2. the state before this part: S_0, then the earlier parts in order
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (data && p.S0) {
+        float v[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int f = f4 * 4 + e;
-            acc[e] = zrow ? p.z0[(size_t)s * p.D + f] : p.S0[((size_t)s * p.D + f) * p.DV + c];
+            v[e] = zrow ? p.z0[(size_t)s * p.D + f] : p.S0[((size_t)s * p.D + f) * p.DV + c];
         }
+        acc = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    const bool img_per_seg = p.img && p.img_per_seg;
+    const int upto = img_per_seg ? part : (part == NP - 1 ? NP : 0);
+    for (int q = 0; q < upto; ++q) {
+        const float4 b = part_acc[q * EPC + el];
+        const float d = part_dec[q * EPC + el];
+        acc.x = fmaf(d, acc.x, b.x), acc.y = fmaf(d, acc.y, b.y);
+        acc.z = fmaf(d, acc.z, b.z), acc.w = fmaf(d, acc.w, b.w);
     }
     // normalised maps: a hi image then a lo image, each of D/64 blocks of IR
     // rows; the unnormalised map: per block the 64 hi rows then the 64 lo
     // rows (one N = 128 operand)
-    const size_t part = (size_t)(p.D / 64) * IR * 128;
+    const size_t part_bytes = (size_t)(p.D / 64) * IR * 128;
     const int f8 = f4 >> 1;  // 16-byte chunk; this thread writes its half (f4 & 1)
     const uint32_t off = (p.norm ? (uint32_t)(f8 >> 3) * (uint32_t)IR * 128u
                                  : (uint32_t)(f8 >> 3) * 16384u) +
                          sw128_off(r, f8 & 7) + 8u * (uint32_t)(f4 & 1);
-    const size_t lo_delta = p.norm ? part : 8192;
+    const size_t lo_delta = p.norm ? part_bytes : 8192;
     auto write_img = [&](size_t index) {
         if (!in_img)
             return;
-        unsigned char* base = p.img + (index * 2) * part;
+        unsigned char* base = p.img + (index * 2) * part_bytes;
         uint2 hi = make_uint2(0, 0), lo = hi;
         if (data) {
-            split2(acc[0], acc[1], hi.x, lo.x);
-            split2(acc[2], acc[3], hi.y, lo.y);
+            split2(acc.x, acc.y, hi.x, lo.x);
+            split2(acc.z, acc.w, hi.y, lo.y);
         }
         *reinterpret_cast<uint2*>(base + off) = hi;
         *reinterpret_cast<uint2*>(base + lo_delta + off) = lo;
     };
-    const float* u = p.U ? p.U + (size_t)s * p.nseg * E + src_off : nullptr;
-    const bool add = data && p.U;
-    const float l2g = p.decay ? p.g.log2g[head] : 0.f;
-    constexpr int kAhead = 8;  // segments whose aggregates are in flight at once
-    float4 buf[kAhead];
+    // ---- 3. walk the part again, writing the state before each segment
+    if (img_per_seg) {
+        for (int gb = g0; gb < g1; gb += kAhead) {
+            float4 buf[kAhead];
+            if (u) {
 #pragma unroll
-    for (int i = 0; i < kAhead; ++i)
-        if (add && i < p.nseg)
-            buf[i] = __ldcg(reinterpret_cast<const float4*>(u + (size_t)i * E));
-    for (int g0 = 0; g0 < p.nseg; g0 += kAhead) {
+                for (int i = 0; i < kAhead; ++i)
+                    if (gb + i < g1)
+                        buf[i] = __ldcg(reinterpret_cast<const float4*>(u + (size_t)(gb + i) * E));
+            }
 #pragma unroll
-        for (int i = 0; i < kAhead; ++i) {
-            const int g = g0 + i;
-            if (g >= p.nseg)
-                break;
-            if (p.img && p.img_per_seg)
+            for (int i = 0; i < kAhead; ++i) {
+                const int g = gb + i;
+                if (g >= g1)
+                    break;
                 write_img(((size_t)s * p.nseg + g) * ntile + h);
-            if (add) {
-                const float4 a = buf[i];
-                if (g + kAhead < p.nseg)
-                    buf[i] = __ldcg(reinterpret_cast<const float4*>(u + (size_t)(g + kAhead) * E));
-                float dec = 1.0f;
-                if (p.decay) {
-                    const int64_t len = min((int64_t)p.L * kC, p.N - (int64_t)g * p.L * kC);
-                    dec = exp2f((float)len * l2g);
+                if (u) {
+                    const float d = seg_dec(g);
+                    acc.x = fmaf(d, acc.x, buf[i].x), acc.y = fmaf(d, acc.y, buf[i].y);
+                    acc.z = fmaf(d, acc.z, buf[i].z), acc.w = fmaf(d, acc.w, buf[i].w);
                 }
-                acc[0] = fmaf(dec, acc[0], a.x), acc[1] = fmaf(dec, acc[1], a.y);
-                acc[2] = fmaf(dec, acc[2], a.z), acc[3] = fmaf(dec, acc[3], a.w);
             }
         }
     }
+    // the total: the last part has walked to the end (causal), or has
+    // combined every part (non-causal)
+    if (part != NP - 1)
+        return;
     if (p.img && !p.img_per_seg)
         write_img((size_t)s * ntile + h);
     if (data && p.S_out) {
+        const float v[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int f = f4 * 4 + e;
             if (zrow) {
                 if (p.z_out)
-                    p.z_out[(size_t)s * p.D + f] = acc[e];
+                    p.z_out[(size_t)s * p.D + f] = v[e];
             } else {
-                p.S_out[((size_t)s * p.D + f) * p.DV + c] = acc[e];
+                p.S_out[((size_t)s * p.D + f) * p.DV + c] = v[e];
             }
         }
     }
@@ -1738,9 +1792,13 @@ cudaError_t tg_run(const FwdArgs& a)
         cp.z_out = a.z_out;
         cp.g = *a.gamma;
         const int RR = norm ? img_rows(true) : (cp.zsum ? 65 : 64);
-        const int64_t threads = BH * (a.dv / kT) * RR * (a.d / 4);
-        const int64_t grid = (threads + 127) / 128;
-        k_tg_scan<<<(unsigned)grid, 128, 0, a.stream>>>(cp);
+        const int64_t elems = BH * (a.dv / kT) * RR * (a.d / 4);
+        // parts: enough CTAs to fill the GPU, each part at least 4 segments
+        int NP = 1;
+        while (NP < 16 && g.nseg >= 8 * NP && elems * NP < (int64_t)sms * kScanThreads * 4)
+            NP *= 2;
+        const int64_t grid = (elems + kScanThreads / NP - 1) / (kScanThreads / NP);
+        k_tg_scan<<<(unsigned)grid, kScanThreads, 0, a.stream>>>(cp, NP);
         count_launches(1);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
