@@ -77,6 +77,10 @@ def job_throughput(units_per_step: int, world: int, steps: int, ms_total: float)
     return units_per_step * world * steps / (ms_total / 1e3)
 
 
+# summary file name under profiles/ for the kernels of a path
+PROFILE_NAME = {"k_tg_state+k_tg_scan+k_tg_out": "k_tg"}
+
+
 def profiled_traffic(kernel: str, workload: str):
     """DRAM bytes per launch (read + write) of `kernel` on `workload`, from the
     ncu summary under profiles/, or None when there is none or the kernel's
@@ -243,12 +247,17 @@ def main():
         from kernelised_causal_linear_gb300 import prefill
 
         S, z = prefill.prefill_decode_state(w)
-        tok = synth.decode_tokens(w, 1, device="cuda")
-        q, k, v = (t[0] for t in tok)
+        # a fresh token for every step (cycled after n_tok distinct ones)
+        n_tok = min(256, steps + warmup)
+        tq, tk, tv = synth.decode_tokens(w, n_tok, device="cuda")
+        q, k, v = tq[0], tk[0], tv[0]
         out = torch.empty((w.B, w.H, w.dv), dtype=torch.float32, device="cuda")
+        tok_i = [0]
 
         def step():
-            la.la_decode_step(S, z, q, k, v, out, feature_map=w.feature_map)
+            i = tok_i[0] % n_tok
+            tok_i[0] += 1
+            la.la_decode_step(S, z, tq[i], tk[i], tv[i], out, feature_map=w.feature_map)
 
         units_per_step = w.BH
         bytes_per_launch = decode_bytes(w)
@@ -310,10 +319,21 @@ def main():
                    "sample": f"{desc}; {dt:.1f} s wall"}
 
     achieved = bytes_per_launch / (ms_step / 1e3) / 1e9
-    kernel = ("k_fwd_tc64" if la_path_dtype(w) == "bf16" else "la_forward") if not decode \
-        else "k_decode_step"
+    path = "decode" if decode else la.la_forward_path(w.B, w.H, w.N, w.d, w.dv, w.causal,
+                                                      w.feature_map, w.decay, w.dtype)
+    # the kernel(s) one step launches; for the multi-kernel paths the roofline
+    # is that of the whole call (every launch of the step inside the time)
+    kernel = {"tcgen05": "k_fwd_tc64", "tcgen05_chunked": "k_tg_state+k_tg_scan+k_tg_out",
+              "simt": "k_chunk_state+k_block_scan+k_block_out",
+              "decode": "k_decode_step"}[path]
+    if decode:
+        metric = "batched decode step token*heads/s, d=dv=128"
+    elif w.name == "causal_n32768_d64_bf16":
+        metric = METRIC
+    else:
+        metric = f"linear-attn fwd token*heads/s on {w.name}"
     line = {
-        "metric": METRIC if not decode else "batched decode step token*heads/s, d=dv=128",
+        "metric": metric,
         "value": value,
         "unit": UNIT,
         "n_gpus": world,
@@ -339,8 +359,9 @@ def main():
             "peak": peaks["hbm_gbs"],
             "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"],
-            "traffic": profiled_traffic(kernel, w.name),
+            "traffic": profiled_traffic(PROFILE_NAME.get(kernel, kernel), w.name),
             "kernel": kernel,
+            "path": path,
             "peak_source": f"{peak_src} HBM copy bandwidth",
             "algorithmic_bytes_per_launch": bytes_per_launch,
         },
@@ -365,7 +386,7 @@ def la_path_dtype(w) -> str:
 
     path = la.la_forward_path(w.B, w.H, w.N, w.d, w.dv, w.causal, w.feature_map, w.decay,
                               w.dtype)
-    return "bf16" if path == "tcgen05" else "f32"
+    return "bf16" if path.startswith("tcgen05") else "f32"
 
 
 def run_e2e(la, w, decode, steps, stream, world, out, env):

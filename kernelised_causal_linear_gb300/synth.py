@@ -63,6 +63,10 @@ WORKLOADS = {
     # mid-size bf16, q and k scaled by 1/sqrt(d); run causal and non-causal
     "causal_n2048_d64_bf16": Workload("causal_n2048_d64_bf16", 4, 8, 2048, 64, 64, torch.bfloat16,
                                       q_scale=1 / 8, k_scale=1 / 8, seed_id=2),
+    # the same shape, non-causal (every query reads the whole sequence's state)
+    "noncausal_n2048_d64_bf16": Workload("noncausal_n2048_d64_bf16", 4, 8, 2048, 64, 64,
+                                         torch.bfloat16, q_scale=1 / 8, k_scale=1 / 8,
+                                         causal=False, seed_id=2),
     # long-context causal forward: the headline throughput workload
     "causal_n32768_d64_bf16": Workload("causal_n32768_d64_bf16", 2, 16, 32768, 64, 64,
                                        torch.bfloat16, seed_id=3),
