@@ -201,6 +201,11 @@ def oracle_forward_sample(w, q, k, v, cores):
                   for t in (q, k, v))
     gamma = w.gamma()
     t0 = time.perf_counter()
+    if w.extra.get("favor_r"):  # the features are part of the method here
+        from kernelised_causal_linear_gb300 import synth
+
+        W = synth.gaussian_rows(w.extra["favor_r"], w.d, seed=w.seed(30)).double().numpy()
+        qf, kf = orc.favor(qf, W), orc.favor(kf, W)
     orc.forward(qf.reshape(ns, 1, w.N, -1), kf.reshape(ns, 1, w.N, -1),
                 vf.reshape(ns, 1, w.N, -1), causal=w.causal, fm=w.feature_map,
                 gamma=None if gamma is None else gamma[:1].double().numpy(), nthreads=cores)
@@ -261,6 +266,30 @@ def main():
 
         units_per_step = w.BH
         bytes_per_launch = decode_bytes(w)
+    elif w.extra.get("favor_r"):
+        # Performer: positive random features of q and k, then the
+        # identity-normalised forward over them (feature dimension r)
+        r = w.extra["favor_r"]
+        q, k, v = synth.qkv(w, device="cuda")
+        W = synth.gaussian_rows(r, w.d, seed=w.seed(30), device="cuda")
+        fq = torch.empty((w.B, w.H, w.N, r), dtype=w.dtype, device="cuda")
+        fk = torch.empty_like(fq)
+        out = torch.empty((w.B, w.H, w.N, w.dv), dtype=torch.float32, device="cuda")
+        ws = torch.empty(max(16, la.la_forward_workspace_size(w.B, w.H, w.N, r, w.dv, w.causal,
+                                                               w.dtype)),
+                         dtype=torch.uint8, device="cuda")
+
+        def call(q_, k_, v_, o_):
+            la.la_favor_features(q_, W, fq)
+            la.la_favor_features(k_, W, fk)
+            la.la_forward(fq, fk, v_, o_, causal=w.causal, feature_map="identity_norm",
+                          workspace=ws)
+
+        def step():
+            call(q, k, v, out)
+
+        units_per_step = w.BH * w.N
+        bytes_per_launch = algorithmic_bytes(w)
     else:
         q, k, v = synth.qkv(w, device="cuda")
         out = torch.empty((w.B, w.H, w.N, w.dv), dtype=torch.float32, device="cuda")
@@ -269,9 +298,12 @@ def main():
                          dtype=torch.uint8, device="cuda")
         gamma = w.gamma()
 
+        def call(q_, k_, v_, o_):
+            la.la_forward(q_, k_, v_, o_, causal=w.causal, feature_map=w.feature_map,
+                          gamma=gamma, workspace=ws)
+
         def step():
-            la.la_forward(q, k, v, out, causal=w.causal, feature_map=w.feature_map, gamma=gamma,
-                          workspace=ws)
+            call(q, k, v, out)
 
         units_per_step = w.BH * w.N
         bytes_per_launch = algorithmic_bytes(w)
@@ -319,13 +351,16 @@ def main():
                    "sample": f"{desc}; {dt:.1f} s wall"}
 
     achieved = bytes_per_launch / (ms_step / 1e3) / 1e9
-    path = "decode" if decode else la.la_forward_path(w.B, w.H, w.N, w.d, w.dv, w.causal,
+    fdim = w.extra.get("favor_r", w.d)
+    path = "decode" if decode else la.la_forward_path(w.B, w.H, w.N, fdim, w.dv, w.causal,
                                                       w.feature_map, w.decay, w.dtype)
     # the kernel(s) one step launches; for the multi-kernel paths the roofline
     # is that of the whole call (every launch of the step inside the time)
     kernel = {"tcgen05": "k_fwd_tc64", "tcgen05_chunked": "k_tg_state+k_tg_scan+k_tg_out",
               "simt": "k_chunk_state+k_block_scan+k_block_out",
               "decode": "k_decode_step"}[path]
+    if w.extra.get("favor_r"):
+        kernel = "k_favor+" + kernel
     if decode:
         metric = "batched decode step token*heads/s, d=dv=128"
     elif w.name == "causal_n32768_d64_bf16":
@@ -444,7 +479,7 @@ def run_e2e(la, w, decode, steps, stream, world, out, env):
             torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
             ms = float(t.item())
     else:
-        q, k, v, ws = env["q"], env["k"], env["v"], env["ws"]
+        q, k, v = env["q"], env["k"], env["v"]
         hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
         hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         gamma = w.gamma()
@@ -469,8 +504,7 @@ def run_e2e(la, w, decode, steps, stream, world, out, env):
                 ready.record(s_in)
             stream.wait_event(ready)
             with torch.cuda.stream(stream):
-                la.la_forward(dq, dk, dv, do, causal=w.causal, feature_map=w.feature_map,
-                              gamma=gamma, workspace=ws)
+                env["call"](dq, dk, dv, do)
                 done = torch.cuda.Event()
                 done.record(stream)
             with torch.cuda.stream(s_out):
@@ -560,8 +594,12 @@ def run_reference(args, w, steps, warmup, world):
         q, k, v = synth.qkv(w, device="cpu", B=1, H=ns, N=n_tok)
         qf, kf, vf = (t.double().numpy() for t in (q, k, v))
 
+        W = (synth.gaussian_rows(w.extra["favor_r"], w.d, seed=w.seed(30)).double().numpy()
+             if w.extra.get("favor_r") else None)
+
         def step():
-            orc.forward(qf, kf, vf, causal=w.causal, fm=w.feature_map,
+            a, b = (orc.favor(qf, W), orc.favor(kf, W)) if W is not None else (qf, kf)
+            orc.forward(a, b, vf, causal=w.causal, fm=w.feature_map,
                         gamma=None if gamma is None else np.full(ns, float(gamma[0])),
                         nthreads=cores)
 

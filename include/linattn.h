@@ -197,6 +197,39 @@ LA_API la_status la_decode_step(float* S, float* z, const void* q, const void* k
                          const float* gamma, int dtype, la_stream_t stream);
 
 /*
+ * The state before part `upto` of a sequence split into `nparts` consecutive
+ * parts (sequence parallelism, "Linear Attention and SSM", LASP-2 section):
+ * given each part's own final state from a zero start, U_p = (S_parts[p],
+ * z_parts[p]) as la_state returns it, and the parts' token counts
+ * part_len[p] (HOST array), computes
+ *     P_0 = 0,   P_{p+1} = gamma^(part_len[p]) P_p + U_p,   out = P_upto
+ * into S_out [B,H,d,dv] and z_out [B,H,d] (fp32).  S_parts is
+ * [nparts][B,H,d,dv] and z_parts [nparts][B,H,d] (fp32, device), e.g. the
+ * result of an all-gather of every rank's U_p.  la_forward_with_state from
+ * (S_out, z_out) then gives the rank's outputs.  nparts <= 256; gamma as for
+ * la_forward (host, H floats, or NULL).
+ */
+LA_API la_status la_state_prefix(const float* S_parts, const float* z_parts, int nparts,
+                                 const int64_t* part_len, int upto, float* S_out, float* z_out,
+                                 int64_t B, int64_t H, int d, int dv, const float* gamma,
+                                 la_stream_t stream);
+
+/*
+ * Positive random features (Performer, FAVOR+): for each of `rows` rows u of
+ * x [rows, d] (in_dtype) and the r rows w_j of w [r, d] (fp32, Gaussian,
+ * drawn by the caller -- i.i.d. or in orthogonal blocks),
+ *     x' = u / d^(1/4),   out[row, j] = exp(w_j . x' - |x'|^2 / 2) / sqrt(r)
+ * written to out [rows, r] in out_dtype.  phi(q) . phi(k) is then an unbiased
+ * estimate of exp(q . k / sqrt(d)) ["Efficient Attention Variants", section 6
+ * Performer]; passing the features of q and k to la_forward with
+ * LA_FM_IDENTITY_NORM (feature dimension r, r in {32, 64, 128}) gives
+ * linear attention with that kernel.  d <= 128, r <= 256; all pointers are
+ * device pointers, 16-byte aligned.
+ */
+LA_API la_status la_favor_features(const void* x, const float* w, void* out, int64_t rows, int d,
+                                   int r, int in_dtype, int out_dtype, la_stream_t stream);
+
+/*
  * la_forward without a workspace argument, for callers that cannot allocate
  * device memory (the pages have no counterpart: this is a deployment
  * convenience).  Typical such callers are a plugin running inside a host

@@ -54,6 +54,11 @@ _lib.la_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _i
 _lib.la_forward_with_state.restype = _i
 _lib.la_forward_with_state.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
                                        _i, _i, _i, _fp, _i, _vp, _sz, _vp]
+_lib.la_state_prefix.restype = _i
+_lib.la_state_prefix.argtypes = [_vp, _vp, _i, ctypes.POINTER(ctypes.c_int64), _i, _vp, _vp, _i64,
+                                 _i64, _i, _i, _fp, _vp]
+_lib.la_favor_features.restype = _i
+_lib.la_favor_features.argtypes = [_vp, _vp, _vp, _i64, _i, _i, _i, _i, _vp]
 _lib.la_forward_noalloc.restype = _i
 _lib.la_forward_noalloc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _i, _i, _fp,
                                     _i, _vp]
@@ -240,6 +245,42 @@ def la_decode_step(S: torch.Tensor, z: torch.Tensor, q: torch.Tensor, k: torch.T
                                _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(out, "out"), B, H, d,
                                dv, _fm(feature_map), gp, _dtype(q), _stream_handle(stream))
     _check(code, "la_decode_step")
+    return out
+
+
+def la_state_prefix(S_parts: torch.Tensor, z_parts: torch.Tensor, part_len, upto: int,
+                    S_out: torch.Tensor | None = None, z_out: torch.Tensor | None = None, *,
+                    gamma=None, stream=None):
+    """State before part `upto` from every part's own state: S_parts
+    [P,B,H,d,dv], z_parts [P,B,H,d], part_len P token counts -> (S, z)."""
+    P, B, H, d, dv = S_parts.shape
+    if S_out is None:
+        S_out = torch.empty((B, H, d, dv), dtype=torch.float32, device=S_parts.device)
+    if z_out is None:
+        z_out = torch.empty((B, H, d), dtype=torch.float32, device=S_parts.device)
+    lens = (ctypes.c_int64 * P)(*[int(x) for x in part_len])
+    gp, _keep = _gamma_arg(gamma, H)
+    code = _lib.la_state_prefix(_dev_ptr(S_parts, "S_parts"), _dev_ptr(z_parts, "z_parts"), P,
+                                lens, int(upto), _dev_ptr(S_out, "S_out"), _dev_ptr(z_out, "z_out"),
+                                B, H, d, dv, gp, _stream_handle(stream))
+    _check(code, "la_state_prefix")
+    return S_out, z_out
+
+
+def la_favor_features(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None, *,
+                      out_dtype=torch.float32, stream=None) -> torch.Tensor:
+    """Positive random features of x [..., d] with Gaussian rows w [r, d]
+    (fp32): exp(w . x' - |x'|^2 / 2) / sqrt(r), x' = x / d^(1/4) -> [..., r]."""
+    d = x.shape[-1]
+    r = w.shape[0]
+    if w.dtype != torch.float32 or tuple(w.shape) != (r, d):
+        raise ValueError("w must be a float32 [r, d] tensor")
+    if out is None:
+        out = torch.empty(x.shape[:-1] + (r,), dtype=out_dtype, device=x.device)
+    code = _lib.la_favor_features(_dev_ptr(x, "x"), _dev_ptr(w, "w"), _dev_ptr(out, "out"),
+                                  x.numel() // d, d, r, _dtype(x), DTYPES[out.dtype],
+                                  _stream_handle(stream))
+    _check(code, "la_favor_features")
     return out
 
 

@@ -349,6 +349,44 @@ la_status la_decode_step(float* S, float* z, const void* q, const void* k, const
     return from_cuda(decode_step(a));
 }
 
+la_status la_state_prefix(const float* S_parts, const float* z_parts, int nparts,
+                          const int64_t* part_len, int upto, float* S_out, float* z_out,
+                          int64_t B, int64_t H, int d, int dv, const float* gamma,
+                          la_stream_t stream)
+{
+    la_status st = check_sizes(B, H, 1, d, dv, LA_FM_ELU1, LA_FP32);
+    if (st != LA_OK)
+        return st;
+    GammaTable gt;
+    if ((st = make_gamma(gamma, H, &gt)) != LA_OK)
+        return st;
+    if (nparts < 1 || nparts > state_prefix_max_parts() || upto < 0 || upto > nparts || !part_len)
+        return LA_ERR_INVALID_ARG;
+    for (int q = 0; q < nparts; ++q)
+        if (part_len[q] < 0)
+            return LA_ERR_INVALID_ARG;
+    if (!S_parts || !z_parts || !S_out || !z_out || !aligned16(S_parts) || !aligned16(z_parts) ||
+        !aligned16(S_out) || !aligned16(z_out))
+        return LA_ERR_INVALID_ARG;
+    return from_cuda(state_prefix(S_parts, z_parts, nparts, part_len, upto, S_out, z_out, B * H,
+                                  (int)H, d, dv, gt, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+la_status la_favor_features(const void* x, const float* w, void* out, int64_t rows, int d, int r,
+                            int in_dtype, int out_dtype, la_stream_t stream)
+{
+    if (rows < 0 || !favor_shape_ok(d, r))
+        return rows < 0 || d < 1 || r < 1 ? LA_ERR_INVALID_ARG : LA_ERR_UNSUPPORTED;
+    if ((in_dtype != LA_BF16 && in_dtype != LA_FP32) || (out_dtype != LA_BF16 && out_dtype != LA_FP32))
+        return LA_ERR_INVALID_ARG;
+    if (rows == 0)
+        return LA_OK;
+    if (!x || !w || !out || !aligned16(x) || !aligned16(w) || !aligned16(out))
+        return LA_ERR_INVALID_ARG;
+    return from_cuda(favor_features(x, w, out, rows, d, r, in_dtype, out_dtype,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
 uint64_t la_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 la_status la_get_device_status(la_stream_t stream)

@@ -113,6 +113,17 @@ bool tma_map_bf16_3d(CUtensorMap* m, const void* base, int64_t cols, int64_t row
 // Streaming multiprocessors of the current device (0 if unknown).
 int device_sm_count();
 
+// exclusive prefix of per-part states for a split sequence (la_state_prefix)
+int state_prefix_max_parts();
+cudaError_t state_prefix(const float* S, const float* z, int nparts, const int64_t* len, int upto,
+                         float* S_out, float* z_out, int64_t BH, int H, int d, int dv,
+                         const GammaTable& g, cudaStream_t st);
+
+// positive random features (la_favor_features)
+bool favor_shape_ok(int d, int r);
+cudaError_t favor_features(const void* x, const float* w, void* out, int64_t rows, int d, int r,
+                           int in_dtype, int out_dtype, cudaStream_t st);
+
 struct DecodeArgs {
     float* S;
     float* z;

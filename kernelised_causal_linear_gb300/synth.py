@@ -75,6 +75,10 @@ WORKLOADS = {
                                        torch.bfloat16, q_scale=1 / math.sqrt(128),
                                        k_scale=1 / math.sqrt(128), v_scale=1 / math.sqrt(128),
                                        feature_map="none", decay=True, seed_id=4),
+    # positive random features (Performer): d = 64 inputs, r = 128 features
+    "favor_n4096_d64_r128_bf16": Workload("favor_n4096_d64_r128_bf16", 2, 8, 4096, 64, 64,
+                                          torch.bfloat16, feature_map="identity_norm",
+                                          seed_id=6, extra={"favor_r": 128}),
     # batched decode: 256 sequences x 32 heads, state from a 4096-token prefix
     "decode_b256_h32_d128_bf16": Workload("decode_b256_h32_d128_bf16", 256, 32, 1, 128, 128,
                                           torch.bfloat16, seed_id=5, prefix=4096, steps=1000),
@@ -90,6 +94,27 @@ def normal(shape, *, seed: int, scale: float = 1.0, dtype=torch.bfloat16, device
     if scale != 1.0:
         x.mul_(scale)
     return x.to(dtype)
+
+
+def gaussian_rows(r: int, d: int, *, seed: int, orthogonal: bool = True, device="cpu"):
+    """r random rows of length d for positive random features, fp32.
+
+    orthogonal=True draws them in blocks of d mutually orthogonal rows (the QR
+    factor of a Gaussian block), each row rescaled to the norm of an
+    independent Gaussian vector, so every row is still marginally N(0, I);
+    otherwise i.i.d. N(0, 1).  These are the random numbers the feature map
+    consumes; the map itself is la_favor_features."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(int(seed))
+    if not orthogonal:
+        return torch.randn(r, d, generator=gen, dtype=torch.float64).float().to(device)
+    blocks = []
+    for _ in range((r + d - 1) // d):
+        g = torch.randn(d, d, generator=gen, dtype=torch.float64)
+        qm, _ = torch.linalg.qr(g)
+        norms = torch.randn(d, d, generator=gen, dtype=torch.float64).norm(dim=1)
+        blocks.append(qm.T * norms[:, None])
+    return torch.cat(blocks)[:r].float().contiguous().to(device)
 
 
 def qkv(w: Workload, device="cpu", N: int | None = None, B: int | None = None,
