@@ -201,6 +201,13 @@ def oracle_forward_sample(w, q, k, v, cores):
                   for t in (q, k, v))
     gamma = w.gamma()
     t0 = time.perf_counter()
+    alpha = None
+    if w.extra.get("gla_gates"):
+        from kernelised_causal_linear_gb300 import synth
+
+        lo, hi = w.extra["gla_gates"]
+        alpha = synth.gates((w.B, w.H, w.N, w.d), seed=w.seed(31), lo=lo, hi=hi)
+        alpha = alpha.reshape(w.BH, 1, w.N, w.d)[:ns].double().numpy()
     if w.extra.get("favor_r"):  # the features are part of the method here
         from kernelised_causal_linear_gb300 import synth
 
@@ -208,7 +215,8 @@ def oracle_forward_sample(w, q, k, v, cores):
         qf, kf = orc.favor(qf, W), orc.favor(kf, W)
     orc.forward(qf.reshape(ns, 1, w.N, -1), kf.reshape(ns, 1, w.N, -1),
                 vf.reshape(ns, 1, w.N, -1), causal=w.causal, fm=w.feature_map,
-                gamma=None if gamma is None else gamma[:1].double().numpy(), nthreads=cores)
+                gamma=None if gamma is None else gamma[:1].double().numpy(), alpha=alpha,
+                nthreads=cores)
     dt = time.perf_counter() - t0
     return ns * w.N / dt, f"{ns} of {w.BH} sequences x {w.N} tokens (fp64 oracle)", min(ns, cores), dt
 
@@ -266,6 +274,23 @@ def main():
 
         units_per_step = w.BH
         bytes_per_launch = decode_bytes(w)
+    elif w.extra.get("gla_gates"):
+        # per-key-channel decay: the gates are an input of the method
+        q, k, v = synth.qkv(w, device="cuda")
+        lo, hi = w.extra["gla_gates"]
+        alpha = synth.gates((w.B, w.H, w.N, w.d), seed=w.seed(31), lo=lo, hi=hi, device="cuda")
+        out = torch.empty((w.B, w.H, w.N, w.dv), dtype=torch.float32, device="cuda")
+        ws = torch.empty(max(16, la.la_gla_workspace_size(w.B, w.H, w.N, w.d, w.dv)),
+                         dtype=torch.uint8, device="cuda")
+
+        def call(q_, k_, v_, o_):
+            la.la_forward_gla(q_, k_, v_, alpha, o_, feature_map=w.feature_map, workspace=ws)
+
+        def step():
+            call(q, k, v, out)
+
+        units_per_step = w.BH * w.N
+        bytes_per_launch = algorithmic_bytes(w) + w.BH * w.N * w.d * 4  # + the fp32 gates
     elif w.extra.get("favor_r"):
         # Performer: positive random features of q and k, then the
         # identity-normalised forward over them (feature dimension r)
@@ -361,6 +386,8 @@ def main():
               "decode": "k_decode_step"}[path]
     if w.extra.get("favor_r"):
         kernel = "k_favor+" + kernel
+    if w.extra.get("gla_gates"):
+        path, kernel = "gla_simt", "k_gla_state+k_gla_scan+k_gla_out"
     if decode:
         metric = "batched decode step token*heads/s, d=dv=128"
     elif w.name == "causal_n32768_d64_bf16":
@@ -415,12 +442,12 @@ def main():
 def la_path_dtype(w) -> str:
     """Arithmetic type of the path that runs: bf16 tensor-core operands with
     fp32 accumulation on the tcgen05 kernel, fp32 on the CUDA-core paths."""
-    if w.steps > 0:
+    if w.steps > 0 or w.extra.get("gla_gates"):
         return "f32"
     import kernelised_causal_linear_gb300 as la
 
-    path = la.la_forward_path(w.B, w.H, w.N, w.d, w.dv, w.causal, w.feature_map, w.decay,
-                              w.dtype)
+    path = la.la_forward_path(w.B, w.H, w.N, w.extra.get("favor_r", w.d), w.dv, w.causal,
+                              w.feature_map, w.decay, w.dtype)
     return "bf16" if path.startswith("tcgen05") else "f32"
 
 
@@ -596,12 +623,16 @@ def run_reference(args, w, steps, warmup, world):
 
         W = (synth.gaussian_rows(w.extra["favor_r"], w.d, seed=w.seed(30)).double().numpy()
              if w.extra.get("favor_r") else None)
+        alpha = None
+        if w.extra.get("gla_gates"):
+            lo, hi = w.extra["gla_gates"]
+            alpha = synth.gates((1, ns, n_tok, w.d), seed=w.seed(31), lo=lo, hi=hi).double().numpy()
 
         def step():
             a, b = (orc.favor(qf, W), orc.favor(kf, W)) if W is not None else (qf, kf)
             orc.forward(a, b, vf, causal=w.causal, fm=w.feature_map,
                         gamma=None if gamma is None else np.full(ns, float(gamma[0])),
-                        nthreads=cores)
+                        alpha=alpha, nthreads=cores)
 
         units = ns * n_tok
         desc = f"{ns} of {w.BH} sequences x first {n_tok} of {w.N} tokens (fp64 oracle)"

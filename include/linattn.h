@@ -197,6 +197,33 @@ LA_API la_status la_decode_step(float* S, float* z, const void* q, const void* k
                          const float* gamma, int dtype, la_stream_t stream);
 
 /*
+ * Causal forward with a per-key-channel decay (GLA):
+ *     S_t = diag(alpha_t) S_{t-1} + phi(k_t) v_t^T,  z_t = alpha_t o z_{t-1} + phi(k_t),
+ *     o_t = phi(q_t)^T S_t / phi(q_t)^T z_t   (o_t = phi(q_t)^T S_t for LA_FM_NONE)
+ * ["Efficient Attention Variants", section 7.2 GLA: alpha_t scales row i of
+ * the state and is broadcast along the values].  alpha [B,H,N,d] is fp32
+ * device memory with every entry in (0, 1] (data-dependent gates computed by
+ * the caller; an exact 0 is not supported).  Runs on the CUDA cores in fp32;
+ * workspace: la_gla_workspace_size() bytes, 256-byte aligned.  Other
+ * arguments as for la_forward.
+ */
+LA_API size_t la_gla_workspace_size(int64_t B, int64_t H, int64_t N, int d, int dv);
+LA_API la_status la_forward_gla(const void* q, const void* k, const void* v, const float* alpha,
+                                float* out, int64_t B, int64_t H, int64_t N, int d, int dv,
+                                int feature_map, int dtype, void* workspace,
+                                size_t workspace_bytes, la_stream_t stream);
+
+/*
+ * One decode step with a per-key-channel decay alpha [B,H,d] (fp32, in
+ * (0, 1]): S <- diag(alpha) S + phi(k) v^T, z <- alpha o z + phi(k), then the
+ * read, as la_decode_step.
+ */
+LA_API la_status la_decode_step_gla(float* S, float* z, const void* q, const void* k,
+                                    const void* v, const float* alpha, float* out, int64_t B,
+                                    int64_t H, int d, int dv, int feature_map, int dtype,
+                                    la_stream_t stream);
+
+/*
  * The state before part `upto` of a sequence split into `nparts` consecutive
  * parts (sequence parallelism, "Linear Attention and SSM", LASP-2 section):
  * given each part's own final state from a zero start, U_p = (S_parts[p],

@@ -13,7 +13,7 @@ library raises ImportError -- there is no CPU fallback.
 from __future__ import annotations
 
 _EXPORTS = {
-    "la_forward", "la_forward_noalloc", "la_forward_with_state", "la_favor_features", "la_state_prefix", "la_state", "la_decode_step", "la_get_device_status", "la_status_string",
+    "la_forward", "la_forward_noalloc", "la_forward_with_state", "la_favor_features", "la_state_prefix", "la_forward_gla", "la_gla_workspace_size", "la_decode_step_gla", "la_state", "la_decode_step", "la_get_device_status", "la_status_string",
     "la_version", "la_launch_count", "la_debug_set_tc_faults", "la_forward_path", "la_forward_workspace_size", "la_state_workspace_size", "LinAttnError",
 }
 

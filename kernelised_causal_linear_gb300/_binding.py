@@ -54,6 +54,14 @@ _lib.la_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _i
 _lib.la_forward_with_state.restype = _i
 _lib.la_forward_with_state.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
                                        _i, _i, _i, _fp, _i, _vp, _sz, _vp]
+_lib.la_gla_workspace_size.restype = _sz
+_lib.la_gla_workspace_size.argtypes = [_i64, _i64, _i64, _i, _i]
+_lib.la_forward_gla.restype = _i
+_lib.la_forward_gla.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i, _i, _i, _i, _vp,
+                                _sz, _vp]
+_lib.la_decode_step_gla.restype = _i
+_lib.la_decode_step_gla.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i, _i, _i, _i,
+                                    _vp]
 _lib.la_state_prefix.restype = _i
 _lib.la_state_prefix.argtypes = [_vp, _vp, _i, ctypes.POINTER(ctypes.c_int64), _i, _vp, _vp, _i64,
                                  _i64, _i, _i, _fp, _vp]
@@ -245,6 +253,46 @@ def la_decode_step(S: torch.Tensor, z: torch.Tensor, q: torch.Tensor, k: torch.T
                                _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(out, "out"), B, H, d,
                                dv, _fm(feature_map), gp, _dtype(q), _stream_handle(stream))
     _check(code, "la_decode_step")
+    return out
+
+
+def la_gla_workspace_size(B, H, N, d, dv) -> int:
+    return int(_lib.la_gla_workspace_size(B, H, N, d, dv))
+
+
+def la_forward_gla(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Tensor,
+                   out: torch.Tensor | None = None, *, feature_map="elu1",
+                   workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Causal forward with per-key-channel decay alpha [B,H,N,d] (fp32, in (0, 1])."""
+    B, H, N, d = q.shape
+    dv = v.shape[-1]
+    if alpha.dtype != torch.float32:
+        raise TypeError("alpha must be float32")
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=torch.float32, device=q.device)
+    need = int(_lib.la_gla_workspace_size(B, H, N, d, dv))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    code = _lib.la_forward_gla(_dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                               _dev_ptr(alpha, "alpha"), _dev_ptr(out, "out"), B, H, N, d, dv,
+                               _fm(feature_map), _dtype(q), _dev_ptr(workspace, "workspace"),
+                               workspace.numel() * workspace.element_size(),
+                               _stream_handle(stream))
+    _check(code, "la_forward_gla")
+    return out
+
+
+def la_decode_step_gla(S, z, q, k, v, alpha, out=None, *, feature_map="elu1", stream=None):
+    """One token per sequence with per-key-channel decay alpha [B,H,d] (fp32)."""
+    B, H, d = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=torch.float32, device=q.device)
+    code = _lib.la_decode_step_gla(_dev_ptr(S, "S"), _dev_ptr(z, "z"), _dev_ptr(q, "q"),
+                                   _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(alpha, "alpha"),
+                                   _dev_ptr(out, "out"), B, H, d, dv, _fm(feature_map), _dtype(q),
+                                   _stream_handle(stream))
+    _check(code, "la_decode_step_gla")
     return out
 
 

@@ -349,6 +349,60 @@ la_status la_decode_step(float* S, float* z, const void* q, const void* k, const
     return from_cuda(decode_step(a));
 }
 
+size_t la_gla_workspace_size(int64_t B, int64_t H, int64_t N, int d, int dv)
+{
+    if (check_sizes(B, H, N, d, dv, LA_FM_ELU1, LA_FP32) != LA_OK)
+        return 0;
+    return gla_workspace(B * H, N, d, dv);
+}
+
+la_status la_forward_gla(const void* q, const void* k, const void* v, const float* alpha,
+                         float* out, int64_t B, int64_t H, int64_t N, int d, int dv,
+                         int feature_map, int dtype, void* workspace, size_t workspace_bytes,
+                         la_stream_t stream)
+{
+    la_status st = check_sizes(B, H, N, d, dv, feature_map, dtype);
+    if (st != LA_OK)
+        return st;
+    if (N == 0)
+        return LA_OK;
+    if (!q || !k || !v || !alpha || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+        !aligned16(alpha) || !aligned16(out))
+        return LA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < gla_workspace(B * H, N, d, dv) || !aligned256(workspace))
+        return LA_ERR_WORKSPACE;
+    GlaArgs a{};
+    a.q = q, a.k = k, a.v = v, a.alpha = alpha, a.out = out;
+    a.B = B, a.H = H, a.N = N, a.d = d, a.dv = dv, a.fm = feature_map, a.dtype = dtype;
+    a.ws = workspace, a.ws_bytes = workspace_bytes;
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    return from_cuda(gla_forward(a));
+}
+
+la_status la_decode_step_gla(float* S, float* z, const void* q, const void* k, const void* v,
+                             const float* alpha, float* out, int64_t B, int64_t H, int d, int dv,
+                             int feature_map, int dtype, la_stream_t stream)
+{
+    if (!alpha || !aligned16(alpha))
+        return LA_ERR_INVALID_ARG;
+    la_status st = check_sizes(B, H, 1, d, dv, feature_map, dtype);
+    if (st != LA_OK)
+        return st;
+    if (!S || !z || !q || !k || !v || !out)
+        return LA_ERR_INVALID_ARG;
+    if (!aligned16(S) || !aligned16(z) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+        !aligned16(out))
+        return LA_ERR_INVALID_ARG;
+    GammaTable gt;
+    make_gamma(nullptr, H, &gt);
+    DecodeArgs a{};
+    a.S = S, a.z = z, a.q = q, a.k = k, a.v = v, a.alpha = alpha, a.out = out;
+    a.BH = B * H, a.H = H, a.d = d, a.dv = dv, a.fm = feature_map, a.dtype = dtype;
+    a.gamma = &gt;
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    return from_cuda(decode_step(a));
+}
+
 la_status la_state_prefix(const float* S_parts, const float* z_parts, int nparts,
                           const int64_t* part_len, int upto, float* S_out, float* z_out,
                           int64_t B, int64_t H, int d, int dv, const float* gamma,

@@ -8,6 +8,9 @@
 //   S <- gamma S + phi(k) v^T,  z <- gamma z + phi(k),
 //   o  = phi(q)^T S / max(phi(q)^T z, FLT_MIN)      (o = phi(q)^T S unnormalised)
 //
+// or, with a per-key-channel decay alpha (GLA, "Efficient Attention Variants"
+// section 7.2), row i of S and entry i of z decay by alpha_i instead of gamma.
+//
 // The step is pure streaming: every state element is read once and written
 // once (8 bytes per element), so the kernel is bound by HBM bandwidth.  One
 // CTA owns one sequence's d x dv state; each thread keeps its RI rows of one
@@ -34,12 +37,14 @@ struct DecodeTile {
 template <int D, int DV, typename T>
 __global__ void __launch_bounds__(kThreads)
     k_decode_step(float* __restrict__ S, float* __restrict__ z, const T* __restrict__ q,
-                  const T* __restrict__ k, const T* __restrict__ v, float* __restrict__ out,
-                  int H, int fm, GammaTable g)
+                  const T* __restrict__ k, const T* __restrict__ v,
+                  const float* __restrict__ alpha, float* __restrict__ out, int H, int fm,
+                  GammaTable g)
 {
     using TL = DecodeTile<D, DV>;
     __shared__ float sfq[D];
     __shared__ float sfk[D];
+    __shared__ float sal[D];  // per-row decay of this step
     __shared__ __align__(16) float sv[DV];
     __shared__ __align__(16) float4 red[kThreads];
     __shared__ float sden[D / 32];
@@ -60,6 +65,7 @@ __global__ void __launch_bounds__(kThreads)
     if (tid < D) {
         sfq[tid] = phi_f32(to_f32<T>(q[seq * D + tid]), fm);
         sfk[tid] = phi_f32(to_f32<T>(k[seq * D + tid]), fm);
+        sal[tid] = alpha ? alpha[seq * D + tid] : gm;
     }
     if (tid < DV)
         sv[tid] = to_f32<T>(v[seq * DV + tid]);
@@ -68,7 +74,7 @@ __global__ void __launch_bounds__(kThreads)
     // z update and phi(q).z on the first D threads (whole warps)
     if (tid < D) {
         float* zp = z + seq * D + tid;
-        const float zn = fmaf(gm, *zp, sfk[tid]);
+        const float zn = fmaf(sal[tid], *zp, sfk[tid]);
         *zp = zn;
         float part = sfq[tid] * zn;
 #pragma unroll
@@ -83,12 +89,12 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int a = 0; a < TL::RI; ++a) {
         const int i = ti + a * TL::TI;
-        const float f = sfk[i];
+        const float f = sfk[i], ga = sal[i];
         float4 x = s[a];
-        x.x = fmaf(gm, x.x, f * vv.x);
-        x.y = fmaf(gm, x.y, f * vv.y);
-        x.z = fmaf(gm, x.z, f * vv.z);
-        x.w = fmaf(gm, x.w, f * vv.w);
+        x.x = fmaf(ga, x.x, f * vv.x);
+        x.y = fmaf(ga, x.y, f * vv.y);
+        x.z = fmaf(ga, x.z, f * vv.z);
+        x.w = fmaf(ga, x.w, f * vv.w);
         __stcs(reinterpret_cast<float4*>(Sb + i * DV + tj * 4), x);
         const float fq = sfq[i];
         acc.x = fmaf(fq, x.x, acc.x);
@@ -121,7 +127,7 @@ cudaError_t run_decode(const DecodeArgs& a)
 {
     k_decode_step<D, DV, T><<<(unsigned)a.BH, kThreads, 0, a.stream>>>(
         a.S, a.z, static_cast<const T*>(a.q), static_cast<const T*>(a.k),
-        static_cast<const T*>(a.v), a.out, (int)a.H, a.fm, *a.gamma);
+        static_cast<const T*>(a.v), a.alpha, a.out, (int)a.H, a.fm, *a.gamma);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -113,6 +113,22 @@ bool tma_map_bf16_3d(CUtensorMap* m, const void* base, int64_t cols, int64_t row
 // Streaming multiprocessors of the current device (0 if unknown).
 int device_sm_count();
 
+// per-key-channel decay (GLA): CUDA-core chunked forward
+struct GlaArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* alpha;  // [B,H,N,d] fp32 in (0, 1]
+    float* out;
+    int64_t B, H, N;
+    int d, dv, fm, dtype;
+    void* ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+};
+size_t gla_workspace(int64_t BH, int64_t N, int d, int dv);
+cudaError_t gla_forward(const GlaArgs& a);
+
 // exclusive prefix of per-part states for a split sequence (la_state_prefix)
 int state_prefix_max_parts();
 cudaError_t state_prefix(const float* S, const float* z, int nparts, const int64_t* len, int upto,
@@ -130,6 +146,7 @@ struct DecodeArgs {
     const void* q;
     const void* k;
     const void* v;
+    const float* alpha;  // [B,H,d] per-key-channel decay of this step, or NULL
     float* out;
     int64_t BH, H;
     int d, dv, fm, dtype;

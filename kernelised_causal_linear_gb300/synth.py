@@ -75,6 +75,11 @@ WORKLOADS = {
                                        torch.bfloat16, q_scale=1 / math.sqrt(128),
                                        k_scale=1 / math.sqrt(128), v_scale=1 / math.sqrt(128),
                                        feature_map="none", decay=True, seed_id=4),
+    # per-key-channel decay (GLA), gates uniform in [0.95, 1), no feature map
+    "gla_n8192_d128_bf16": Workload("gla_n8192_d128_bf16", 4, 8, 8192, 128, 128, torch.bfloat16,
+                                    q_scale=1 / math.sqrt(128), k_scale=1 / math.sqrt(128),
+                                    v_scale=1 / math.sqrt(128), feature_map="none", seed_id=7,
+                                    extra={"gla_gates": (0.95, 1.0)}),
     # positive random features (Performer): d = 64 inputs, r = 128 features
     "favor_n4096_d64_r128_bf16": Workload("favor_n4096_d64_r128_bf16", 2, 8, 4096, 64, 64,
                                           torch.bfloat16, feature_map="identity_norm",
@@ -94,6 +99,16 @@ def normal(shape, *, seed: int, scale: float = 1.0, dtype=torch.bfloat16, device
     if scale != 1.0:
         x.mul_(scale)
     return x.to(dtype)
+
+
+def gates(shape, *, seed: int, lo: float = 0.9, hi: float = 1.0, device="cpu"):
+    """Per-key-channel decay gates, i.i.d. uniform in [lo, hi) (lo > 0), fp32:
+    the data-dependent alpha_t of a gated recurrence, here drawn instead of
+    computed from the tokens."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(int(seed))
+    u = torch.rand(tuple(shape), generator=gen, dtype=torch.float64)
+    return (lo + (hi - lo) * u).float().to(device)
 
 
 def gaussian_rows(r: int, d: int, *, seed: int, orthogonal: bool = True, device="cpu"):
