@@ -37,8 +37,9 @@
 //
 // Every fp32 quantity that enters a bf16 MMA (P, the state, the decayed
 // values) is split into a bf16 hi/lo pair (two MMAs, ~2^-17 relative); phi(Q)
-// and phi(K) are rounded once to bf16; accumulators, states and denominators
-// are fp32.  The ones column of [V | 1] gives the row sums of P and the
+// and phi(K) are rounded once to bf16, except in the aggregates of a call that
+// returns its state (1e-5), where phi(K) is a hi/lo pair too.  Accumulators,
+// states and denominators are fp32.  The ones column of [V | 1] gives the row sums of P and the
 // normaliser increments on the same MMAs.
 //
 // Decay together with a normalised feature map is not taken by this path
@@ -184,6 +185,7 @@ struct StParams {
     int BH, H;
     int nchunk, L, nseg;
     int elu, zsum, decay;  // zsum: also the normaliser increments
+    int klo;               // phi(K) as a bf16 hi/lo pair (states returned to the caller)
     // stage layout (bytes from the stage start): phi(K) hi blocks at 0, phi(K)
     // lo blocks at off_klo (elu), V blocks at off_v, decayed-V lo blocks at
     // off_vlo (decay); nst stages of `stage` bytes
@@ -205,23 +207,29 @@ struct StLayout {
     static constexpr uint32_t TAIL = 2048 + 2048 + 1024;
     static constexpr uint32_t SMEM_MAX = OFF_ST + kStStageBudget + TAIL + 1024;
     // tensor memory: [dS^T] in D columns (lanes = value channels); with
-    // DV = 128 the normaliser increments in D more columns (lane 0)
+    // DV = 128 the normaliser increments in D more columns (lane 0).  Two
+    // such accumulators: item j + 1 accumulates while item j is read out.
     static constexpr uint32_t COLS_USED = D + (VB == 2 ? D : 0);
-    static constexpr uint32_t TMEM_COLS = COLS_USED <= 32 ? 32 : COLS_USED <= 64 ? 64
-                                        : COLS_USED <= 128 ? 128 : COLS_USED <= 256 ? 256 : 512;
+    static constexpr uint32_t TMEM_COLS = 2 * COLS_USED <= 64 ? 64
+                                        : 2 * COLS_USED <= 128 ? 128 : 2 * COLS_USED <= 256 ? 256 : 512;
     static_assert(SMEM_MAX <= 232448, "shared memory");
 };
 
+// Threads of the state kernel's feature-map warpgroups (two groups of 128).
+constexpr int kStMapThreads = 256;
+constexpr int kStThreads = 128 + kStMapThreads;
+
 // elu(x)+1 of a 128 x 64 bf16 block in fp32, split into bf16 hi (in place)
-// and lo parts; rows >= valid become zero.  128 threads: thread t takes
-// 16-byte chunk t & 7 of rows t/8 + 16 m.
+// and lo parts (lo == nullptr: rounded once to bf16, in place); rows >= valid
+// become zero.  kStMapThreads threads: thread t takes 16-byte chunk t & 7 of
+// rows t/8 + 32 m.
 __device__ __forceinline__ void phi_split_block(unsigned char* hi, unsigned char* lo, int t,
                                                 int valid)
 {
     const int cc = t & 7, r0 = t >> 3;
 #pragma unroll 2
-    for (int mm = 0; mm < 8; ++mm) {
-        const int r = r0 + 16 * mm;
+    for (int mm = 0; mm < 128 / (kStMapThreads / 8); ++mm) {
+        const int r = r0 + (kStMapThreads / 8) * mm;
         const uint32_t off = sw128_off(r, cc);
         uint4 h = make_uint4(0, 0, 0, 0), l = h;
         if (r < valid) {
@@ -233,24 +241,25 @@ __device__ __forceinline__ void phi_split_block(unsigned char* hi, unsigned char
             split8(x, h, l);
         }
         *reinterpret_cast<uint4*>(hi + off) = h;
-        *reinterpret_cast<uint4*>(lo + off) = l;
+        if (lo)
+            *reinterpret_cast<uint4*>(lo + off) = l;
     }
 }
 
 struct StMisc {
-    uint64_t full[4], prep[4], free_[4], accd, accfree, drain;  // at most 4 stages
+    uint64_t full[4], prep[4], free_[4], accd[2], accfree[2], drain;  // at most 4 stages
     uint32_t tmem;
     int abort;
 };
 
-// Decayed copy of a 128 x 64 value block for the state MMA: row t is scaled
-// by w_t and split into bf16 hi (written back in place) and lo parts.  Thread
-// t owns row t.
+// Decayed copy of a 128 x 64 value block for the state MMA: row t & 127 is
+// scaled by w and split into bf16 hi (written back in place) and lo parts.
+// Thread t owns the 16-byte chunks 4 (t >> 7) .. 4 (t >> 7) + 3 of its row.
 __device__ __forceinline__ void decay_block(unsigned char* v, unsigned char* vlo, int t, float w)
 {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const uint32_t off = sw128_off(t, c);
+    for (int c = 4 * (t >> 7); c < 4 * (t >> 7) + 4; ++c) {
+        const uint32_t off = sw128_off(t & 127, c);
         float x[8];
         unpack8(*reinterpret_cast<const uint4*>(v + off), x);
 #pragma unroll
@@ -259,12 +268,13 @@ __device__ __forceinline__ void decay_block(unsigned char* v, unsigned char* vlo
         uint4 hi, lo;
         split8(x, hi, lo);
         *reinterpret_cast<uint4*>(v + off) = hi;
-        *reinterpret_cast<uint4*>(vlo + off) = lo;
+        if (vlo)
+            *reinterpret_cast<uint4*>(vlo + off) = lo;
     }
 }
 
 template <int D, int DV>
-__global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StParams p)
+__global__ void __launch_bounds__(kStThreads, 1) k_tg_state(const __grid_constant__ StParams p)
 {
     using LY = StLayout<D, DV>;
     constexpr int KB = LY::KB, VB = LY::VB;
@@ -284,8 +294,10 @@ __global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StP
             mbar_init(&m->prep[i], 1);
             mbar_init(&m->free_[i], 1);
         }
-        mbar_init(&m->accd, 1);
-        mbar_init(&m->accfree, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&m->accd[i], 1);
+            mbar_init(&m->accfree[i], 1);
+        }
         mbar_init(&m->drain, 1);
         m->abort = 0;
         fence_mbar_init();
@@ -369,18 +381,19 @@ __global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StP
             const uint32_t eb = smem_addr(sm + LY::OFF_EB);
             const uint32_t zt = smem_addr(sm + OFF_ZT), et = smem_addr(sm + OFF_ET);
             const uint32_t klbo = D == 128 ? 16384u : 16u;  // feature blocks of phi(K)
-            const int nk = p.elu ? 2 : 1, nv = p.decay ? 2 : 1;
+            const int nk = p.elu && p.klo ? 2 : 1, nv = p.decay ? 2 : 1;
             const bool dz_mma = p.zsum && !p.decay;  // else the CUDA cores sum dz
             int u = 0, j = 0;
             bool ok = true, issued = false;
             for (int it = blockIdx.x; ok && it < items; it += gridDim.x, ++j) {
                 const int g = it % p.nseg;
                 const int n = min(p.L, p.nchunk - g * p.L);
-                // the previous item's aggregate has been read out
-                if (j > 0 && !tg_wait(&m->accfree, (j - 1) & 1, abort)) {
+                // the aggregate of item j - 2 (same accumulator) has been read out
+                if (j > 1 && !tg_wait(&m->accfree[j & 1], ((j - 2) >> 1) & 1, abort)) {
                     ok = false;
                     break;
                 }
+                const uint32_t ta = tm + (uint32_t)(j & 1) * LY::COLS_USED;
                 for (int k = 0; k < n; ++k, ++u) {
                     const int st = u % NST;
                     if (!tg_wait(&m->prep[st], (u / NST) & 1, abort)) {
@@ -402,7 +415,7 @@ __global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StP
                                 const uint64_t ad = VB == 2
                                                         ? mndesc(vsrc, false, vsrc + 16384u, false, kk)
                                                         : mndesc(vsrc, false, x, true, kk);
-                                mma_bf16_ss(tm, ad, sdesc_sw128(ksrc + kk * 2048, klbo, 1024), idD,
+                                mma_bf16_ss(ta, ad, sdesc_sw128(ksrc + kk * 2048, klbo, 1024), idD,
                                             acc0 || kk > 0);
                             }
                         }
@@ -411,7 +424,7 @@ __global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StP
                         for (int pk = 0; pk < nk; ++pk) {
                             const uint32_t ksrc = b + (pk ? p.off_klo : 0u);
                             for (int kk = 0; kk < 8; ++kk)
-                                mma_bf16_ss(tm + D, mndesc(eb, true, zt, true, kk),
+                                mma_bf16_ss(ta + D, mndesc(eb, true, zt, true, kk),
                                             sdesc_sw128(ksrc + kk * 2048, klbo, 1024), idD,
                                             k > 0 || pk > 0 || kk > 0);
                         }
@@ -419,7 +432,7 @@ __global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StP
                     mma_commit(&m->free_[st]);
                     issued = true;
                     if (k == n - 1)
-                        mma_commit(&m->accd);
+                        mma_commit(&m->accd[j & 1]);
                 }
             }
             if (issued && *abort) {
@@ -429,7 +442,8 @@ __global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StP
         }
     } else if (warp >= 4) {
         // ------------------- feature map, decayed values, read-out --------
-        const int t = tid - 128, wq = t >> 5;
+        // two warpgroups: thread t and t + 128 share tensor-memory lane t
+        const int t = tid - 128, wq = (t >> 5) & 3, half = t >> 7, tl = t & 127;
         const bool lead = t == 0;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         int u = 0, j = 0;
@@ -444,7 +458,7 @@ __global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StP
             for (int k = 0; k < n; ++k, ++u) {
                 const int st = u % NST;
                 const bool okw = tg_wait(&m->full[st], (u / NST) & 1, abort);
-                if (!group_ok(okw, 1, 128)) {
+                if (!group_ok(okw, 1, kStMapThreads)) {
                     ok = false;
                     break;
                 }
@@ -452,13 +466,14 @@ __global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StP
                 const int valid = chunk_valid(p.N, c0 + k);
                 if (p.elu)
                     for (int kb = 0; kb < KB; ++kb)
-                        phi_split_block(b + kb * 16384, b + p.off_klo + kb * 16384, t, valid);
+                        phi_split_block(b + kb * 16384,
+                                        p.klo ? b + p.off_klo + kb * 16384 : nullptr, t, valid);
                 if (p.decay) {
                     // V' = gamma^(T1-1-t) V: weights relative to the segment's end
                     // (rows past the sequence hold zeros and get weight 0)
-                    const int tl = k * kC + t;
+                    const int ts = k * kC + tl;
                     const float l2g = p.g.log2g[head];
-                    const float w = tl < seg_len ? exp2f((float)(seg_len - 1 - tl) * l2g) : 0.f;
+                    const float w = ts < seg_len ? exp2f((float)(seg_len - 1 - ts) * l2g) : 0.f;
                     for (int vb = 0; vb < VB; ++vb)
                         decay_block(b + p.off_v + vb * 16384, b + p.off_vlo + vb * 16384, t, w);
                     if (p.zsum && t < D) {
@@ -474,7 +489,7 @@ __global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StP
                             const uint32_t off = sw128_off(row, f >> 3) + (f & 7) * 2;
                             float x = __uint_as_float(
                                 (uint32_t)*reinterpret_cast<const uint16_t*>(kt + off) << 16);
-                            if (p.elu)
+                            if (p.elu && p.klo)
                                 x += __uint_as_float(
                                     (uint32_t)*reinterpret_cast<const uint16_t*>(kl + off) << 16);
                             acc = fmaf(wr, x, acc);
@@ -483,15 +498,15 @@ __global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StP
                     }
                 }
                 fence_proxy_async_smem();
-                named_bar(1, 128);
+                named_bar(1, kStMapThreads);
                 if (lead)
                     mbar_arrive(&m->prep[st]);
             }
             if (!ok)
                 break;
             // the aggregate: S^T rows and the normaliser, fp32
-            const bool okd = tg_wait(&m->accd, j & 1, abort);
-            if (!group_ok(okd, 1, 128)) {
+            const bool okd = tg_wait(&m->accd[j & 1], (j >> 1) & 1, abort);
+            if (!group_ok(okd, 1, kStMapThreads)) {
                 ok = false;
                 break;
             }
@@ -499,24 +514,27 @@ __global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StP
             float* dst = p.U + ((size_t)s * p.nseg + g) * (size_t)(DV * D + D);
             if (p.decay && p.zsum && t < D)
                 dst[(size_t)DV * D + t] = zdec;
-            // lane t: value channel t (DV = 128), or t < 64 and lane 64 = dz (DV = 64)
+            // lane tl: value channel tl (DV = 128), or tl < 64 and lane 64 = dz
+            // (DV = 64); warpgroup `half` reads columns 32 half .. 32 half + 31
+            // of every 64-column block
+            const uint32_t ta = tm + (uint32_t)(j & 1) * LY::COLS_USED;
             float* row = nullptr;
-            if (t < DV)
-                row = dst + (size_t)t * D;
-            else if (DV == 64 && t == 64 && p.zsum && !p.decay)
+            if (tl < DV)
+                row = dst + (size_t)tl * D;
+            else if (DV == 64 && tl == 64 && p.zsum && !p.decay)
                 row = dst + (size_t)DV * D;
             for (int cb = 0; cb < D / 64; ++cb) {
-                uint32_t r[4][16];
+                uint32_t r[2][16];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    tmem_ld16(tm + lane_off + (uint32_t)(cb * 64 + 16 * q), r[q]);
+                for (int q = 0; q < 2; ++q)
+                    tmem_ld16(ta + lane_off + (uint32_t)(cb * 64 + 32 * half + 16 * q), r[q]);
                 tmem_ld_wait();
                 if (row) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
+                    for (int q = 0; q < 2; ++q)
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            *reinterpret_cast<float4*>(row + cb * 64 + 16 * q + 4 * e) =
+                            *reinterpret_cast<float4*>(row + cb * 64 + 32 * half + 16 * q + 4 * e) =
                                 make_float4(__uint_as_float(r[q][4 * e]),
                                             __uint_as_float(r[q][4 * e + 1]),
                                             __uint_as_float(r[q][4 * e + 2]),
@@ -525,15 +543,16 @@ __global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StP
             }
             if (VB == 2 && p.zsum && !p.decay && wq == 0) {
                 for (int cb = 0; cb < D / 64; ++cb) {
-                    uint32_t r[4][16];
+                    uint32_t r[2][16];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        tmem_ld16(tm + lane_off + (uint32_t)(D + cb * 64 + 16 * q), r[q]);
+                    for (int q = 0; q < 2; ++q)
+                        tmem_ld16(ta + lane_off + (uint32_t)(D + cb * 64 + 32 * half + 16 * q),
+                                  r[q]);
                     tmem_ld_wait();
-                    if (t == 0) {
-                        float* zr = dst + (size_t)DV * D + cb * 64;
+                    if (tl == 0) {
+                        float* zr = dst + (size_t)DV * D + cb * 64 + 32 * half;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
+                        for (int q = 0; q < 2; ++q)
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
                                 *reinterpret_cast<float4*>(zr + 16 * q + 4 * e) =
@@ -545,9 +564,9 @@ __global__ void __launch_bounds__(256, 1) k_tg_state(const __grid_constant__ StP
                 }
             }
             tc_fence_before();
-            named_bar(1, 128);
+            named_bar(1, kStMapThreads);
             if (lead)
-                mbar_arrive(&m->accfree);
+                mbar_arrive(&m->accfree[j & 1]);
         }
     }
 
@@ -1657,7 +1676,7 @@ cudaError_t launch_state(StParams sp, int grid, cudaStream_t st)
 {
     using LY = StLayout<D, DV>;
     sp.off_klo = (uint32_t)LY::KB * 16384u;
-    sp.off_v = sp.off_klo * (sp.elu ? 2u : 1u);
+    sp.off_v = sp.off_klo * (sp.elu && sp.klo ? 2u : 1u);
     sp.off_vlo = sp.off_v + (uint32_t)LY::VB * 16384u;
     sp.stage = sp.off_vlo + (sp.decay ? (uint32_t)LY::VB * 16384u : 0u);
     sp.nst = (int)std::min<uint32_t>(4, kStStageBudget / sp.stage);
@@ -1667,7 +1686,7 @@ cudaError_t launch_state(StParams sp, int grid, cudaStream_t st)
     cudaError_t e = set_smem(k_tg_state<D, DV>, LY::SMEM_MAX);
     if (e != cudaSuccess)
         return e;
-    k_tg_state<D, DV><<<grid, 256, smem, st>>>(sp);
+    k_tg_state<D, DV><<<grid, kStThreads, smem, st>>>(sp);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -1760,6 +1779,12 @@ cudaError_t tg_run(const FwdArgs& a)
         sp.elu = a.fm == LA_FM_ELU1;
         sp.zsum = zsum;
         sp.decay = a.gamma->has_decay;
+        // the aggregates meet 1e-5 for returned states; for the outputs alone
+        // phi(K) rounded once to bf16 keeps the normalised read inside 2e-3
+        // (its denominator is a sum of positive terms); the decayed values of
+        // the RetNet form keep their lo part (their sums cancel, so a bf16
+        // rounding of V' would show at ~1e-3 of the output)
+        sp.klo = a.S_out != nullptr || a.z_out != nullptr;
         sp.U = U;
         sp.g = *a.gamma;
         sp.status = a.status;
