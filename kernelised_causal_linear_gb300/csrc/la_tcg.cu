@@ -596,6 +596,56 @@ struct ScanParams {
     GammaTable g;
 };
 
+// State-only calls over many sequences: one thread per (sequence, row of
+// [S^T; z]) adds the segments' aggregates in order, 32 features at a time,
+// and stores the total with the value channel fastest across a warp (S_out
+// is [D][DV] per sequence).  Few threads carry a lot of work each, which
+// suits many short scans; the element-parallel kernel below serves the rest.
+__global__ void __launch_bounds__(256) k_tg_total(const __grid_constant__ ScanParams p)
+{
+    const int rows = p.DV + (p.zsum ? 1 : 0);
+    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gid >= (int64_t)p.BH * rows)
+        return;
+    const int s = (int)(gid / rows), c = (int)(gid - (int64_t)s * rows);
+    const bool zr = c == p.DV;
+    if (zr && !p.z_out)
+        return;
+    const size_t E = (size_t)p.DV * p.D + p.D;
+    const float* u = p.U + (size_t)s * p.nseg * E + (zr ? (size_t)p.DV * p.D : (size_t)c * p.D);
+    const float l2g = p.decay ? p.g.log2g[s % p.H] : 0.f;
+    for (int f0 = 0; f0 < p.D; f0 += 32) {
+        float acc[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const size_t f = (size_t)s * p.D + f0 + e;
+            acc[e] = !p.S0 ? 0.f : zr ? p.z0[f] : p.S0[f * p.DV + c];
+        }
+        for (int g = 0; g < p.nseg; ++g) {
+            const float d =
+                p.decay ? exp2f((float)min((int64_t)p.L * kC, p.N - (int64_t)g * p.L * kC) * l2g)
+                        : 1.0f;
+            const float4* src = reinterpret_cast<const float4*>(u + (size_t)g * E + f0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 x = __ldg(src + q);
+                acc[4 * q] = fmaf(d, acc[4 * q], x.x);
+                acc[4 * q + 1] = fmaf(d, acc[4 * q + 1], x.y);
+                acc[4 * q + 2] = fmaf(d, acc[4 * q + 2], x.z);
+                acc[4 * q + 3] = fmaf(d, acc[4 * q + 3], x.w);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const size_t f = (size_t)s * p.D + f0 + e;
+            if (zr)
+                p.z_out[f] = acc[e];
+            else
+                p.S_out[f * p.DV + c] = acc[e];
+        }
+    }
+}
+
 // One element = (sequence, value tile h, row r, 4 features); rows 0..63 are
 // value channels (S^T), row 64 the normaliser, rows 65..79 of a normalised
 // image zero.  The normaliser row of tiles h > 0 repeats tile 0's (each
@@ -609,7 +659,7 @@ struct ScanParams {
 // before every segment.  The additions within a part stay in segment order.
 constexpr int kScanThreads = 256;
 
-__global__ void __launch_bounds__(kScanThreads) k_tg_scan(const __grid_constant__ ScanParams p,
+__global__ void __launch_bounds__(kScanThreads, 3) k_tg_scan(const __grid_constant__ ScanParams p,
                                                           int NP)
 {
     __shared__ float4 part_acc[kScanThreads];
@@ -620,12 +670,24 @@ __global__ void __launch_bounds__(kScanThreads) k_tg_scan(const __grid_constant_
     const int per_seq = ntile * RR * F4;
     const int el = threadIdx.x % EPC, part = threadIdx.x / EPC;
     const int64_t gid = (int64_t)blockIdx.x * EPC + el;
-    const bool live = gid < (int64_t)p.BH * per_seq;
-    const int s = live ? (int)(gid / per_seq) : 0;
-    int rem = live ? (int)(gid % per_seq) : 0;
-    const int f4 = rem % F4;
-    rem /= F4;
-    const int r = rem % RR, h = rem / RR;
+    const int64_t nel = (int64_t)p.BH * per_seq;
+    const bool live = gid < nel;
+    // element -> (sequence, tile, row, 4 features); 32-bit division where
+    // the element count allows (the kernel is bound by instruction issue)
+    int s = 0, rem = 0;
+    if (live) {
+        if (nel <= (int64_t)UINT32_MAX) {
+            const uint32_t g32 = (uint32_t)gid;
+            s = (int)(g32 / (uint32_t)per_seq);
+            rem = (int)(g32 - (uint32_t)s * (uint32_t)per_seq);
+        } else {
+            s = (int)(gid / per_seq);
+            rem = (int)(gid - (int64_t)s * per_seq);
+        }
+    }
+    const int f4 = rem & (F4 - 1);  // F4 = D / 4, a power of two
+    rem = (int)((uint32_t)rem / (uint32_t)F4);
+    const int r = (int)((uint32_t)rem % (uint32_t)RR), h = (int)((uint32_t)rem / (uint32_t)RR);
     const int head = s % p.H;
     const bool zrow = p.zsum && r == 64;
     const bool data = live && (r < 64 || zrow);
@@ -1818,6 +1880,12 @@ cudaError_t tg_run(const FwdArgs& a)
         cp.g = *a.gamma;
         const int RR = norm ? img_rows(true) : (cp.zsum ? 65 : 64);
         const int64_t elems = BH * (a.dv / kT) * RR * (a.d / 4);
+        const int64_t total_rows = BH * (a.dv + (cp.zsum ? 1 : 0));
+        if (!cp.img && cp.U && cp.S_out && g.nseg <= 64 && total_rows >= (int64_t)sms * 128) {
+            k_tg_total<<<(unsigned)((total_rows + 255) / 256), 256, 0, a.stream>>>(cp);
+            count_launches(1);
+            return cudaGetLastError();
+        }
         // parts: enough CTAs to fill the GPU, each part at least 4 segments
         int NP = 1;
         while (NP < 16 && g.nseg >= 8 * NP && elems * NP < (int64_t)sms * kScanThreads * 4)

@@ -127,6 +127,27 @@ def test_chunked_state(orc, fm, decay, d, dv):
     assert rel_err_rows(z, zr) <= 1e-5
 
 
+@pytest.mark.parametrize("fm,decay,d,dv", [("elu1", False, 64, 64), ("none", True, 128, 128),
+                                           ("elu1", True, 128, 64), ("identity_norm", False, 64, 128)])
+def test_state_many_sequences(orc, fm, decay, d, dv):
+    """la_state over hundreds of sequences (the prefill before decode), with
+    and without an initial state: the totals are summed one row per thread."""
+    B, H, N = 40, 8, 700
+    q, k, v = _inputs(B, H, N, d, dv, fm, seed=71)
+    g = _gamma(H) if decay else None
+    gd = None if g is None else g.double().numpy()
+    S, z = la.la_state(k, v, feature_map=fm, gamma=g)
+    Sr, zr = orc.state(to_np(k), to_np(v), fm=fm, gamma=gd)
+    assert rel_err_rows(S, Sr) <= 1e-5 and rel_err_rows(z, zr) <= 1e-5
+    # continued from a state: the second half from the first half's state
+    P = 300
+    _, S1, z1 = la.la_forward_with_state(None, k[:, :, :P].contiguous(), v[:, :, :P].contiguous(),
+                                         feature_map=fm, gamma=g)
+    _, S2, z2 = la.la_forward_with_state(None, k[:, :, P:].contiguous(), v[:, :, P:].contiguous(),
+                                         S0=S1, z0=z1, feature_map=fm, gamma=g)
+    assert rel_err_rows(S2, Sr) <= 1e-5 and rel_err_rows(z2, zr) <= 1e-5
+
+
 @pytest.mark.parametrize("fm,decay,d", [("elu1", False, 64), ("none", True, 128),
                                         ("elu1", False, 128), ("identity_norm", False, 64)])
 def test_forward_with_state_continues(orc, fm, decay, d):
