@@ -42,19 +42,49 @@ __device__ __forceinline__ float ldf(const T* p)
 }
 
 // ------------------------------------------------------------- step 1 ----
-// Thread (ti, tj) owns RI rows (channels) x 4 value columns of the D x DV
-// block state.  The running log-sum of each channel is kept by thread i < D.
+// Thread (ti, tj) owns RI consecutive rows (channels) x RJ consecutive value
+// columns of the D x DV block state: per token, RI + RJ shared loads (16-byte
+// where they line up) feed RI x RJ FMAs.  The running log-sum of each channel
+// is kept by thread i < D.
+template <int D, int DV>
+struct StateTile {
+    static constexpr int RJ = (D * DV / kThreads >= 8) ? 8 : 4;
+    static constexpr int TJ = DV / RJ;
+    static constexpr int TI = kThreads / TJ;
+    static constexpr int RI = D / TI;
+    static_assert(RI >= 1 && TI * TJ == kThreads && RI * TI == D, "state tile");
+};
+
+template <int N>
+__device__ __forceinline__ void lds_row(const float* p, float (&x)[N])
+{
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < N / 4; ++q) {
+            const float4 v = reinterpret_cast<const float4*>(p)[q];
+            x[4 * q] = v.x, x[4 * q + 1] = v.y, x[4 * q + 2] = v.z, x[4 * q + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < N; ++q)
+            x[q] = p[q];
+    }
+}
+
 template <int D, int DV, typename T>
 __global__ void __launch_bounds__(kThreads)
     k_gla_state(const T* __restrict__ kp, const T* __restrict__ vp, const float* __restrict__ ap,
                 float* __restrict__ ws, float* __restrict__ dec, int64_t N, int nblk, int fm)
 {
-    constexpr int TJ = (DV / 4) < 32 ? (DV / 4) : 32;
-    constexpr int TI = kThreads / TJ;
-    constexpr int RI = D / TI;
-    __shared__ __align__(16) float sk[kSub][D];  // phi(k) o exp(L_end - L_t)
-    __shared__ __align__(16) float sv[kSub][DV];
-    __shared__ float slog[D];                    // L_end of the block per channel
+    using TL = StateTile<D, DV>;
+    constexpr int TJ = TL::TJ, RI = TL::RI, RJ = TL::RJ;
+    // dynamic shared memory (more than the 48 KiB of static arrays with
+    // D = DV = 128): phi(k) o exp(L_end - L_t), v, log alpha, L_end
+    extern __shared__ __align__(16) float st_smem[];
+    float(*sk)[D] = reinterpret_cast<float(*)[D]>(st_smem);
+    float(*sv)[DV] = reinterpret_cast<float(*)[DV]>(st_smem + kSub * D);
+    float(*sl)[D] = reinterpret_cast<float(*)[D]>(st_smem + kSub * (D + DV));
+    float* slog = st_smem + kSub * (2 * D + DV);
     const int64_t gb = blockIdx.x;
     const int64_t seq = gb / nblk;
     const int blk = (int)(gb % nblk);
@@ -65,47 +95,54 @@ __global__ void __launch_bounds__(kThreads)
     const float* ab = ap + (seq * N + t0) * D;
     const int tid = threadIdx.x, tj = tid % TJ, ti = tid / TJ;
 
-    // total log decay of the block per channel
+    // total log decay of the block per channel, summed in token order like
+    // the running sums below (so that the last weight is exactly 1); the
+    // loads do not depend on the sum and stay in flight
     if (tid < D) {
         float l = 0.f;
+#pragma unroll 8
         for (int t = 0; t < len; ++t)
             l += logf(ab[(int64_t)t * D + tid]);
         slog[tid] = l;
     }
     float run = 0.f;  // L_t of channel tid (tid < D), running
     __syncthreads();
-    float acc[RI][4];
+    float acc[RI][RJ];
 #pragma unroll
     for (int a = 0; a < RI; ++a)
-        acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
+#pragma unroll
+        for (int b = 0; b < RJ; ++b)
+            acc[a][b] = 0.f;
     float zacc = 0.f;
     for (int s0 = 0; s0 < len; s0 += kSub) {
         const int n = min(kSub, len - s0);
-        if (tid < D) {
-            for (int t = 0; t < kSub; ++t) {
-                float x = 0.f;
-                if (t < n) {
-                    run += logf(ab[(int64_t)(s0 + t) * D + tid]);
-                    x = phi_f32(ldf(kb + (int64_t)(s0 + t) * D + tid), fm) * expf(slog[tid] - run);
-                }
-                sk[t][tid] = x;
-            }
+        for (int e = tid; e < kSub * D; e += kThreads) {
+            const int t = e / D, i = e % D;
+            const bool in = t < n;
+            sl[t][i] = in ? logf(ab[(int64_t)(s0 + t) * D + i]) : 0.f;
+            sk[t][i] = in ? phi_f32(ldf(kb + (int64_t)(s0 + t) * D + i), fm) : 0.f;
         }
+        __syncthreads();
+        if (tid < D)  // the running log-sum, and the weight exp(L_end - L_t)
+            for (int t = 0; t < n; ++t) {
+                run += sl[t][tid];
+                sk[t][tid] *= expf(slog[tid] - run);
+            }
         for (int e = tid; e < kSub * DV; e += kThreads) {
             const int t = e / DV, c = e % DV;
             sv[t][c] = t < n ? ldf(vb + (int64_t)(s0 + t) * DV + c) : 0.f;
         }
         __syncthreads();
+#pragma unroll 4
         for (int t = 0; t < kSub; ++t) {
-            const float4 vv = *reinterpret_cast<const float4*>(&sv[t][tj * 4]);
+            float kr[RI], vr[RJ];
+            lds_row(&sk[t][ti * RI], kr);
+            lds_row(&sv[t][tj * RJ], vr);
 #pragma unroll
-            for (int a = 0; a < RI; ++a) {
-                const float f = sk[t][ti + a * TI];
-                acc[a][0] = fmaf(f, vv.x, acc[a][0]);
-                acc[a][1] = fmaf(f, vv.y, acc[a][1]);
-                acc[a][2] = fmaf(f, vv.z, acc[a][2]);
-                acc[a][3] = fmaf(f, vv.w, acc[a][3]);
-            }
+            for (int a = 0; a < RI; ++a)
+#pragma unroll
+                for (int b = 0; b < RJ; ++b)
+                    acc[a][b] = fmaf(kr[a], vr[b], acc[a][b]);
             if (tid < D)
                 zacc += sk[t][tid];
         }
@@ -114,9 +151,11 @@ __global__ void __launch_bounds__(kThreads)
     float* dst = ws + gb * (int64_t)(D * DV + D);
 #pragma unroll
     for (int a = 0; a < RI; ++a) {
-        const int i = ti + a * TI;
-        *reinterpret_cast<float4*>(dst + i * DV + tj * 4) =
-            make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+        const int i = ti * RI + a;
+#pragma unroll
+        for (int q = 0; q < RJ / 4; ++q)
+            *reinterpret_cast<float4*>(dst + i * DV + tj * RJ + 4 * q) =
+                make_float4(acc[a][4 * q], acc[a][4 * q + 1], acc[a][4 * q + 2], acc[a][4 * q + 3]);
     }
     if (tid < D) {
         dst[D * DV + tid] = zacc;
@@ -140,22 +179,42 @@ __global__ void __launch_bounds__(kThreads)
     const int row = e < D * DV ? e / DV : e - D * DV;
     float* base = ws + seq * (int64_t)nblk * E + e;
     const float* db = dec + seq * (int64_t)nblk * D + row;
+    // kAhead blocks' values and decays in flight at a time
+    constexpr int kAhead = 8;
     float acc = 0.f;
-    for (int b = 0; b < nblk; ++b) {
-        const float x = base[(int64_t)b * E];
-        base[(int64_t)b * E] = acc;
-        acc = fmaf(acc, db[(int64_t)b * D], x);
+    for (int b0 = 0; b0 < nblk; b0 += kAhead) {
+        float x[kAhead], dd[kAhead];
+#pragma unroll
+        for (int i = 0; i < kAhead; ++i)
+            if (b0 + i < nblk) {
+                x[i] = __ldcg(base + (int64_t)(b0 + i) * E);
+                dd[i] = __ldg(db + (int64_t)(b0 + i) * D);
+            }
+#pragma unroll
+        for (int i = 0; i < kAhead; ++i)
+            if (b0 + i < nblk) {
+                base[(int64_t)(b0 + i) * E] = acc;
+                acc = fmaf(acc, dd[i], x[i]);
+            }
     }
 }
 
 // ------------------------------------------------------------- step 3 ----
+// Shared memory of the output kernel (floats): the running state S [D][DV]
+// and z [D]; phi(q), phi(k) and the running log-sums L of the sub-chunk,
+// transposed ([D][LDT], token fastest); v [kSub][DV]; the intra weights
+// transposed (AT[j][t]); the denominators.
 template <int D, int DV>
-struct GlaSmem {
-    static constexpr size_t floats = (size_t)D * DV + D      // S, z
-                                     + 3 * (size_t)kSub * D  // phi(q), phi(k), L (running log)
-                                     + (size_t)kSub * DV     // v
-                                     + (size_t)kSub * (kSub + 1) + kSub;  // A, den
+struct GlaOut {
+    static constexpr int LDT = kSub + 4;
+    static constexpr size_t oZ = (size_t)D * DV, oQ = oZ + D, oK = oQ + (size_t)D * LDT,
+                            oL = oK + (size_t)D * LDT, oV = oL + (size_t)D * LDT,
+                            oA = oV + (size_t)kSub * DV, oDen = oA + (size_t)kSub * LDT,
+                            floats = oDen + kSub;
     static constexpr size_t bytes = floats * sizeof(float);
+    // output tile of a thread: ORI tokens x 4 value columns
+    static constexpr int OJ = DV / 4, OI = kThreads / OJ, ORI = kSub / OI;
+    static_assert(OI * OJ == kThreads && ORI * OI == kSub, "output tile");
 };
 
 template <int D, int DV, typename T>
@@ -164,28 +223,25 @@ __global__ void __launch_bounds__(kThreads)
               const float* __restrict__ ap, float* __restrict__ out, const float* __restrict__ ws,
               int64_t N, int nblk, int fm)
 {
+    using G = GlaOut<D, DV>;
+    using TL = StateTile<D, DV>;
+    constexpr int LDT = G::LDT, E = D * DV + D;
     extern __shared__ __align__(16) float smem[];
     float* sS = smem;
-    float* sz = sS + D * DV;
-    float* sq = sz + D;
-    float* sk = sq + kSub * D;
-    float* sL = sk + kSub * D;
-    float* sv = sL + kSub * D;
-    float* sA = sv + kSub * DV;
-    float* sden = sA + kSub * (kSub + 1);
-    constexpr int LDA = kSub + 1;
-    constexpr int E = D * DV + D;
-    constexpr int TJo = (DV / 4) < 32 ? (DV / 4) : 32;
-    constexpr int TIo = kThreads / TJo;
-    constexpr int RIo = (kSub + TIo - 1) / TIo;
-    constexpr int TJ = TJo, TI = TIo, RI = D / TI;
+    float* sz = smem + G::oZ;
+    float* qT = smem + G::oQ;  // qT[i * LDT + t]
+    float* kT = smem + G::oK;
+    float* LT = smem + G::oL;
+    float* sv = smem + G::oV;  // sv[t * DV + c]
+    float* AT = smem + G::oA;  // AT[j * LDT + t]
+    float* sden = smem + G::oDen;
 
     const int64_t gb = blockIdx.x;
     const int64_t seq = gb / nblk;
     const int blk = (int)(gb % nblk);
     const int64_t t0 = (int64_t)blk * kBlockL;
     const int len = (int)min((int64_t)kBlockL, N - t0);
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const bool norm = fm_normalised(fm);
     for (int e = tid; e < E; e += kThreads)
         sS[e] = ws[gb * E + e];  // sz follows sS
@@ -198,129 +254,200 @@ __global__ void __launch_bounds__(kThreads)
     for (int s0 = 0; s0 < len; s0 += kSub) {
         const int n = min(kSub, len - s0);
         __syncthreads();  // the previous sub-chunk is consumed
-        if (tid < D) {    // running log decay of channel tid from the sub-chunk's start
-            float run = 0.f;
-            for (int t = 0; t < kSub; ++t) {
-                if (t < n)
-                    run += logf(ab[(int64_t)(s0 + t) * D + tid]);
-                sL[t * D + tid] = run;
-            }
-        }
+        // log alpha, phi(q), phi(k) of the sub-chunk (coalesced, every thread),
+        // then channel tid < D turns its log alphas into the running sum L
         for (int e = tid; e < kSub * D; e += kThreads) {
             const int t = e / D, i = e % D;
-            const bool in = t < n;
-            sq[e] = in ? phi_f32(ldf(qb + (int64_t)(s0 + t) * D + i), fm) : 0.f;
-            sk[e] = in ? phi_f32(ldf(kb + (int64_t)(s0 + t) * D + i), fm) : 0.f;
+            float la = 0.f, fq = 0.f, fk = 0.f;
+            if (t < n) {
+                const int64_t o = (int64_t)(s0 + t) * D + i;
+                la = logf(ab[o]);
+                fq = phi_f32(ldf(qb + o), fm);
+                fk = phi_f32(ldf(kb + o), fm);
+            }
+            LT[i * LDT + t] = la;
+            qT[i * LDT + t] = fq;
+            kT[i * LDT + t] = fk;
         }
         for (int e = tid; e < kSub * DV; e += kThreads) {
             const int t = e / DV, c = e % DV;
             sv[e] = t < n ? ldf(vb + (int64_t)(s0 + t) * DV + c) : 0.f;
         }
-        // When the sub-chunk's decay stays above e^-60 in every channel (thread
-        // tid < D tests its own channel, written above by itself),
+        __syncthreads();
+        if (tid < D) {
+            float run = 0.f;
+            for (int t = 0; t < kSub; ++t) {
+                run += LT[tid * LDT + t];
+                LT[tid * LDT + t] = run;
+            }
+        }
+        // When the sub-chunk's decay stays above e^-60 in every channel,
         // exp(L_t - L_j) = exp(L_t) exp(-L_j) with both factors in fp32 range:
-        // phi(q) and phi(k) are rescaled once and the scores are plain dot
-        // products; otherwise every factor is taken as exp of a difference.
+        // phi(q) and phi(k) are rescaled once and every product below is a
+        // plain sum of products; otherwise each factor is taken as exp of a
+        // difference.  (Thread tid < D tests its own channel, written above
+        // by itself.)
         const bool split =
-            __syncthreads_and(tid >= D || sL[(n - 1) * D + tid] >= -60.0f) != 0;
+            __syncthreads_and(tid >= D || LT[tid * LDT + n - 1] >= -60.0f) != 0;
         if (split) {
-            for (int e = tid; e < kSub * D; e += kThreads) {
-                sq[e] *= expf(sL[e]);
-                sk[e] *= expf(-sL[e]);
+            if (tid < D)
+                for (int t = 0; t < kSub; ++t) {
+                    const float l = LT[tid * LDT + t];
+                    qT[tid * LDT + t] *= expf(l);
+                    kT[tid * LDT + t] *= expf(-l);
+                }
+            __syncthreads();
+        }
+        // intra weights A_tj = sum_i q_ti k_ji exp(L_ti - L_ji), j <= t:
+        // thread (ty, tx) takes tokens 4 ty .. 4 ty + 3 and key token tx
+        {
+            const int ty = tid >> 5, tx = lane;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            if (split) {
+#pragma unroll 8
+                for (int i = 0; i < D; ++i) {
+                    const float4 q4 = *reinterpret_cast<const float4*>(qT + i * LDT + 4 * ty);
+                    const float kk = kT[i * LDT + tx];
+                    acc[0] = fmaf(q4.x, kk, acc[0]), acc[1] = fmaf(q4.y, kk, acc[1]);
+                    acc[2] = fmaf(q4.z, kk, acc[2]), acc[3] = fmaf(q4.w, kk, acc[3]);
+                }
+            } else {
+                for (int i = 0; i < D; ++i) {
+                    const float kk = kT[i * LDT + tx], lj = LT[i * LDT + tx];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        acc[r] = fmaf(qT[i * LDT + 4 * ty + r] * kk,
+                                      __expf(LT[i * LDT + 4 * ty + r] - lj), acc[r]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                if (tx > 4 * ty + r)
+                    acc[r] = 0.f;
+            *reinterpret_cast<float4*>(AT + tx * LDT + 4 * ty) =
+                make_float4(acc[0], acc[1], acc[2], acc[3]);
+        }
+        __syncthreads();
+        // denominators: (phi(q_t) o exp(L_t)) . z + sum_j A_tj, one warp per
+        // four tokens
+        if (norm) {
+            for (int t = 4 * warp; t < 4 * warp + 4; ++t) {
+                float part = lane <= t ? AT[lane * LDT + t] : 0.f;
+                for (int i = lane; i < D; i += 32) {
+                    const float qi = split ? qT[i * LDT + t] : qT[i * LDT + t] * expf(LT[i * LDT + t]);
+                    part = fmaf(qi, sz[i], part);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    part += __shfl_xor_sync(0xffffffffu, part, o);
+                if (lane == 0)
+                    sden[t] = part;
             }
             __syncthreads();
         }
-        // intra scores with the per-channel decay between the two tokens
-        for (int e = tid; e < kSub * kSub; e += kThreads) {
-            const int t = e / kSub, j = e % kSub;
-            float a = 0.f;
-            if (j <= t) {
-                const float* x = sq + t * D;
-                const float* y = sk + j * D;
-                const float* lt = sL + t * D;
-                const float* lj = sL + j * D;
-                if (split)
-                    for (int i = 0; i < D; ++i)
-                        a = fmaf(x[i], y[i], a);
-                else
-                    for (int i = 0; i < D; ++i)
-                        a = fmaf(x[i] * y[i], __expf(lt[i] - lj[i]), a);
-            }
-            sA[t * LDA + j] = a;
-        }
-        __syncthreads();
-        // denominators: (phi(q_t) o exp(L_t)) . z + sum_j A_tj
-        if (tid < kSub) {
-            const int t = tid;
-            float den = 0.f;
-            for (int i = 0; i < D; ++i)
-                den = fmaf(split ? sq[t * D + i] : sq[t * D + i] * __expf(sL[t * D + i]), sz[i],
-                           den);
-            for (int j = 0; j <= t; ++j)
-                den += sA[t * LDA + j];
-            sden[t] = den;
-        }
-        __syncthreads();
+        // outputs: thread (oi, oj) takes ORI tokens x 4 columns
         {
-            const int tj = tid % TJo, ti = tid / TJo;
-            for (int a = 0; a < RIo; ++a) {
-                const int t = ti + a * TIo;
-                if (t >= kSub)
-                    break;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int i = 0; i < D; ++i) {
-                    const float f = split ? sq[t * D + i] : sq[t * D + i] * __expf(sL[t * D + i]);
-                    const float4 s = *reinterpret_cast<const float4*>(sS + i * DV + tj * 4);
-                    acc.x = fmaf(f, s.x, acc.x);
-                    acc.y = fmaf(f, s.y, acc.y);
-                    acc.z = fmaf(f, s.z, acc.z);
-                    acc.w = fmaf(f, s.w, acc.w);
+            constexpr int ORI = G::ORI;
+            const int oj = tid % G::OJ, oi = tid / G::OJ;
+            const int tb = oi * ORI, c0 = 4 * oj;
+            float acc[ORI][4];
+#pragma unroll
+            for (int r = 0; r < ORI; ++r)
+                acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.f;
+#pragma unroll 4
+            for (int i = 0; i < D; ++i) {
+                float qv[ORI];
+                lds_row(qT + i * LDT + tb, qv);
+                if (!split)
+#pragma unroll
+                    for (int r = 0; r < ORI; ++r)
+                        qv[r] *= expf(LT[i * LDT + tb + r]);
+                const float4 s4 = *reinterpret_cast<const float4*>(sS + i * DV + c0);
+#pragma unroll
+                for (int r = 0; r < ORI; ++r) {
+                    acc[r][0] = fmaf(qv[r], s4.x, acc[r][0]);
+                    acc[r][1] = fmaf(qv[r], s4.y, acc[r][1]);
+                    acc[r][2] = fmaf(qv[r], s4.z, acc[r][2]);
+                    acc[r][3] = fmaf(qv[r], s4.w, acc[r][3]);
                 }
-                for (int j = 0; j <= t; ++j) {
-                    const float wgt = sA[t * LDA + j];
-                    const float4 vv = *reinterpret_cast<const float4*>(sv + j * DV + tj * 4);
-                    acc.x = fmaf(wgt, vv.x, acc.x);
-                    acc.y = fmaf(wgt, vv.y, acc.y);
-                    acc.z = fmaf(wgt, vv.z, acc.z);
-                    acc.w = fmaf(wgt, vv.w, acc.w);
+            }
+#pragma unroll 4
+            for (int j = 0; j < kSub; ++j) {
+                float av[ORI];
+                lds_row(AT + j * LDT + tb, av);
+                const float4 v4 = *reinterpret_cast<const float4*>(sv + j * DV + c0);
+#pragma unroll
+                for (int r = 0; r < ORI; ++r) {
+                    acc[r][0] = fmaf(av[r], v4.x, acc[r][0]);
+                    acc[r][1] = fmaf(av[r], v4.y, acc[r][1]);
+                    acc[r][2] = fmaf(av[r], v4.z, acc[r][2]);
+                    acc[r][3] = fmaf(av[r], v4.w, acc[r][3]);
                 }
+            }
+#pragma unroll
+            for (int r = 0; r < ORI; ++r) {
+                const int t = tb + r;
                 if (t < n) {
+                    float4 o = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
                     if (norm) {
                         const float inv = 1.0f / fmaxf(sden[t], FLT_MIN);
-                        acc.x *= inv, acc.y *= inv, acc.z *= inv, acc.w *= inv;
+                        o.x *= inv, o.y *= inv, o.z *= inv, o.w *= inv;
                     }
-                    *reinterpret_cast<float4*>(ob + (int64_t)(s0 + t) * DV + tj * 4) = acc;
+                    *reinterpret_cast<float4*>(ob + (int64_t)(s0 + t) * DV + c0) = o;
                 }
             }
         }
         __syncthreads();  // every read of S, z for this sub-chunk is done
         // S <- diag(exp(L_end)) S + sum_j (phi(k_j) o exp(L_end - L_j)) v_j^T ; z alike
         {
-            const int tj = tid % TJ, ti = tid / TJ;
+            constexpr int RI = TL::RI, RJ = TL::RJ;
+            const int tj = tid % TL::TJ, ti = tid / TL::TJ;
+            float g[RI], acc[RI][RJ];
+#pragma unroll
             for (int a = 0; a < RI; ++a) {
-                const int i = ti + a * TI;
-                const float lend = sL[(n - 1) * D + i];
-                const float gi = expf(lend);
-                float4 s = *reinterpret_cast<float4*>(sS + i * DV + tj * 4);
-                s.x *= gi, s.y *= gi, s.z *= gi, s.w *= gi;
-                for (int j = 0; j < n; ++j) {
-                    const float f = split ? sk[j * D + i] * gi
-                                          : sk[j * D + i] * __expf(lend - sL[j * D + i]);
-                    const float4 vv = *reinterpret_cast<const float4*>(sv + j * DV + tj * 4);
-                    s.x = fmaf(f, vv.x, s.x);
-                    s.y = fmaf(f, vv.y, s.y);
-                    s.z = fmaf(f, vv.z, s.z);
-                    s.w = fmaf(f, vv.w, s.w);
+                const int i = ti * RI + a;
+                g[a] = expf(LT[i * LDT + n - 1]);
+                float row[RJ];
+                lds_row(sS + i * DV + tj * RJ, row);
+#pragma unroll
+                for (int b = 0; b < RJ; ++b)
+                    acc[a][b] = split ? row[b] : g[a] * row[b];
+            }
+#pragma unroll 4
+            for (int j = 0; j < kSub; ++j) {
+                float kr[RI], vr[RJ];
+#pragma unroll
+                for (int a = 0; a < RI; ++a) {
+                    const int i = ti * RI + a;
+                    kr[a] = split ? kT[i * LDT + j]
+                                  : kT[i * LDT + j] * __expf(LT[i * LDT + n - 1] - LT[i * LDT + j]);
                 }
-                *reinterpret_cast<float4*>(sS + i * DV + tj * 4) = s;
+                lds_row(sv + j * DV + tj * RJ, vr);
+#pragma unroll
+                for (int a = 0; a < RI; ++a)
+#pragma unroll
+                    for (int b = 0; b < RJ; ++b)
+                        acc[a][b] = fmaf(kr[a], vr[b], acc[a][b]);
+            }
+#pragma unroll
+            for (int a = 0; a < RI; ++a) {
+                const int i = ti * RI + a;
+#pragma unroll
+                for (int q = 0; q < RJ / 4; ++q) {
+                    const float m = split ? g[a] : 1.0f;
+                    *reinterpret_cast<float4*>(sS + i * DV + tj * RJ + 4 * q) =
+                        make_float4(m * acc[a][4 * q], m * acc[a][4 * q + 1], m * acc[a][4 * q + 2],
+                                    m * acc[a][4 * q + 3]);
+                }
             }
             if (tid < D) {
-                const float lend = sL[(n - 1) * D + tid];
+                const float lend = LT[tid * LDT + n - 1];
                 const float gz = expf(lend);
-                float zz = sz[tid] * gz;
-                for (int j = 0; j < n; ++j)
-                    zz = fmaf(sk[j * D + tid], split ? gz : __expf(lend - sL[j * D + tid]), zz);
-                sz[tid] = zz;
+                float zz = split ? sz[tid] : gz * sz[tid];
+                for (int j = 0; j < kSub; ++j)
+                    zz += split ? kT[tid * LDT + j]
+                                : kT[tid * LDT + j] * __expf(lend - LT[tid * LDT + j]);
+                sz[tid] = split ? gz * zz : zz;
             }
         }
     }
@@ -339,10 +466,15 @@ cudaError_t run_gla(const GlaArgs& a)
     const T* q = static_cast<const T*>(a.q);
     const T* k = static_cast<const T*>(a.k);
     const T* v = static_cast<const T*>(a.v);
-    k_gla_state<D, DV, T><<<(unsigned)(BH * nblk), kThreads, 0, a.stream>>>(k, v, a.alpha, ws, dec,
-                                                                           a.N, nblk, a.fm);
+    const size_t st_smem = sizeof(float) * ((size_t)kSub * (2 * D + DV) + D);
+    cudaError_t err = cudaFuncSetAttribute(k_gla_state<D, DV, T>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st_smem);
+    if (err != cudaSuccess)
+        return err;
+    k_gla_state<D, DV, T><<<(unsigned)(BH * nblk), kThreads, st_smem, a.stream>>>(
+        k, v, a.alpha, ws, dec, a.N, nblk, a.fm);
     count_launches(1);
-    cudaError_t err = cudaGetLastError();
+    err = cudaGetLastError();
     if (err != cudaSuccess)
         return err;
     const int per_seq = (E + kThreads - 1) / kThreads;
@@ -351,7 +483,7 @@ cudaError_t run_gla(const GlaArgs& a)
     err = cudaGetLastError();
     if (err != cudaSuccess)
         return err;
-    const size_t smem = GlaSmem<D, DV>::bytes;
+    const size_t smem = GlaOut<D, DV>::bytes;
     auto kern = k_gla_out<D, DV, T>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess)
