@@ -212,19 +212,24 @@ struct GlaOut {
                             oA = oV + (size_t)kSub * DV, oDen = oA + (size_t)kSub * LDT,
                             floats = oDen + kSub;
     static constexpr size_t bytes = floats * sizeof(float);
-    // output tile of a thread: ORI tokens x 4 value columns
-    static constexpr int OJ = DV / 4, OI = kThreads / OJ, ORI = kSub / OI;
-    static_assert(OI * OJ == kThreads && ORI * OI == kSub, "output tile");
+    // output tiles of 4 tokens x 4 value columns (OT threads); state-update
+    // tiles of UR channels x 8 value columns (UT threads)
+    static constexpr int OJ = DV / 4, OI = kSub / 4, OT = OI * OJ;
+    static constexpr int UR = D * DV / 8 >= 4 * kThreads ? 4 : D * DV / 8 >= 2 * kThreads ? 2 : 1;
+    static constexpr int UJ = DV / 8, UI = D / UR, UT = UI * UJ;
+    static_assert(OT <= kThreads && UT <= kThreads && DV % 8 == 0, "tiles");
 };
 
 template <int D, int DV, typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
     k_gla_out(const T* __restrict__ qp, const T* __restrict__ kp, const T* __restrict__ vp,
               const float* __restrict__ ap, float* __restrict__ out, const float* __restrict__ ws,
               int64_t N, int nblk, int fm)
 {
-    using G = GlaOut<D, DV>;
-    using TL = StateTile<D, DV>;
+    // a CTA takes DVC of the DV value columns (two CTAs per block with
+    // DV = 128: half the state in shared memory, two CTAs per SM)
+    constexpr int DVC = DV > 64 ? 64 : DV, NH = DV / DVC;
+    using G = GlaOut<D, DVC>;
     constexpr int LDT = G::LDT, E = D * DV + D;
     extern __shared__ __align__(16) float smem[];
     float* sS = smem;
@@ -232,32 +237,38 @@ __global__ void __launch_bounds__(kThreads)
     float* qT = smem + G::oQ;  // qT[i * LDT + t]
     float* kT = smem + G::oK;
     float* LT = smem + G::oL;
-    float* sv = smem + G::oV;  // sv[t * DV + c]
+    float* sv = smem + G::oV;  // sv[t * DVC + c]
     float* AT = smem + G::oA;  // AT[j * LDT + t]
     float* sden = smem + G::oDen;
 
-    const int64_t gb = blockIdx.x;
+    const int64_t gb = blockIdx.x / NH;
+    const int c_off = (int)(blockIdx.x % NH) * DVC;
     const int64_t seq = gb / nblk;
     const int blk = (int)(gb % nblk);
     const int64_t t0 = (int64_t)blk * kBlockL;
     const int len = (int)min((int64_t)kBlockL, N - t0);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const bool norm = fm_normalised(fm);
-    for (int e = tid; e < E; e += kThreads)
-        sS[e] = ws[gb * E + e];  // sz follows sS
+    for (int e = tid; e < D * DVC; e += kThreads)
+        sS[e] = ws[gb * E + (e / DVC) * DV + c_off + e % DVC];
+    for (int i = tid; i < D; i += kThreads)
+        sz[i] = ws[gb * E + D * DV + i];
     const T* qb = qp + (seq * N + t0) * D;
     const T* kb = kp + (seq * N + t0) * D;
-    const T* vb = vp + (seq * N + t0) * DV;
+    const T* vb = vp + (seq * N + t0) * DV + c_off;
     const float* ab = ap + (seq * N + t0) * D;
-    float* ob = out + (seq * N + t0) * DV;
+    float* ob = out + (seq * N + t0) * DV + c_off;
 
     for (int s0 = 0; s0 < len; s0 += kSub) {
         const int n = min(kSub, len - s0);
         __syncthreads();  // the previous sub-chunk is consumed
         // log alpha, phi(q), phi(k) of the sub-chunk (coalesced, every thread),
         // then channel tid < D turns its log alphas into the running sum L
+        // (a warp takes 8 channels x 4 tokens: the transposed stores hit 32
+        // different banks)
         for (int e = tid; e < kSub * D; e += kThreads) {
-            const int t = e / D, i = e % D;
+            const int wt = e >> 5, cg = wt % (D / 8), tg = wt / (D / 8);
+            const int i = 8 * cg + (e & 7), t = 4 * tg + ((e >> 3) & 3);
             float la = 0.f, fq = 0.f, fk = 0.f;
             if (t < n) {
                 const int64_t o = (int64_t)(s0 + t) * D + i;
@@ -269,8 +280,8 @@ __global__ void __launch_bounds__(kThreads)
             qT[i * LDT + t] = fq;
             kT[i * LDT + t] = fk;
         }
-        for (int e = tid; e < kSub * DV; e += kThreads) {
-            const int t = e / DV, c = e % DV;
+        for (int e = tid; e < kSub * DVC; e += kThreads) {
+            const int t = e / DVC, c = e % DVC;
             sv[e] = t < n ? ldf(vb + (int64_t)(s0 + t) * DV + c) : 0.f;
         }
         __syncthreads();
@@ -300,18 +311,42 @@ __global__ void __launch_bounds__(kThreads)
         }
         // intra weights A_tj = sum_i q_ti k_ji exp(L_ti - L_ji), j <= t:
         // thread (ty, tx) takes tokens 4 ty .. 4 ty + 3 and key token tx
-        {
-            const int ty = tid >> 5, tx = lane;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            if (split) {
+        if (split) {
+            // 64 threads, 4 tokens x 4 key tokens each (two 16-byte loads per
+            // 16 FMAs)
+            if (tid < (kSub / 4) * (kSub / 4)) {
+                const int ty = tid / (kSub / 4), jx = tid % (kSub / 4);
+                float acc[4][4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.f;
 #pragma unroll 8
                 for (int i = 0; i < D; ++i) {
                     const float4 q4 = *reinterpret_cast<const float4*>(qT + i * LDT + 4 * ty);
-                    const float kk = kT[i * LDT + tx];
-                    acc[0] = fmaf(q4.x, kk, acc[0]), acc[1] = fmaf(q4.y, kk, acc[1]);
-                    acc[2] = fmaf(q4.z, kk, acc[2]), acc[3] = fmaf(q4.w, kk, acc[3]);
+                    const float4 k4 = *reinterpret_cast<const float4*>(kT + i * LDT + 4 * jx);
+                    const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        acc[r][0] = fmaf(qv[r], k4.x, acc[r][0]);
+                        acc[r][1] = fmaf(qv[r], k4.y, acc[r][1]);
+                        acc[r][2] = fmaf(qv[r], k4.z, acc[r][2]);
+                        acc[r][3] = fmaf(qv[r], k4.w, acc[r][3]);
+                    }
                 }
-            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int j = 4 * jx + c;
+                    float w[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        w[r] = j <= 4 * ty + r ? acc[r][c] : 0.f;
+                    *reinterpret_cast<float4*>(AT + j * LDT + 4 * ty) = make_float4(w[0], w[1], w[2], w[3]);
+                }
+            }
+        } else {
+            const int ty = tid >> 5, tx = lane;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            {
                 for (int i = 0; i < D; ++i) {
                     const float kk = kT[i * LDT + tx], lj = LT[i * LDT + tx];
 #pragma unroll
@@ -345,9 +380,9 @@ __global__ void __launch_bounds__(kThreads)
             }
             __syncthreads();
         }
-        // outputs: thread (oi, oj) takes ORI tokens x 4 columns
-        {
-            constexpr int ORI = G::ORI;
+        // outputs: thread (oi, oj) < OT takes 4 tokens x 4 columns
+        if (tid < G::OT) {
+            constexpr int ORI = 4;
             const int oj = tid % G::OJ, oi = tid / G::OJ;
             const int tb = oi * ORI, c0 = 4 * oj;
             float acc[ORI][4];
@@ -362,7 +397,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
                     for (int r = 0; r < ORI; ++r)
                         qv[r] *= expf(LT[i * LDT + tb + r]);
-                const float4 s4 = *reinterpret_cast<const float4*>(sS + i * DV + c0);
+                const float4 s4 = *reinterpret_cast<const float4*>(sS + i * DVC + c0);
 #pragma unroll
                 for (int r = 0; r < ORI; ++r) {
                     acc[r][0] = fmaf(qv[r], s4.x, acc[r][0]);
@@ -375,7 +410,7 @@ __global__ void __launch_bounds__(kThreads)
             for (int j = 0; j < kSub; ++j) {
                 float av[ORI];
                 lds_row(AT + j * LDT + tb, av);
-                const float4 v4 = *reinterpret_cast<const float4*>(sv + j * DV + c0);
+                const float4 v4 = *reinterpret_cast<const float4*>(sv + j * DVC + c0);
 #pragma unroll
                 for (int r = 0; r < ORI; ++r) {
                     acc[r][0] = fmaf(av[r], v4.x, acc[r][0]);
@@ -399,16 +434,16 @@ __global__ void __launch_bounds__(kThreads)
         }
         __syncthreads();  // every read of S, z for this sub-chunk is done
         // S <- diag(exp(L_end)) S + sum_j (phi(k_j) o exp(L_end - L_j)) v_j^T ; z alike
-        {
-            constexpr int RI = TL::RI, RJ = TL::RJ;
-            const int tj = tid % TL::TJ, ti = tid / TL::TJ;
+        if (tid < G::UT) {
+            constexpr int RI = G::UR, RJ = 8;
+            const int tj = tid % G::UJ, ti = tid / G::UJ;
             float g[RI], acc[RI][RJ];
 #pragma unroll
             for (int a = 0; a < RI; ++a) {
                 const int i = ti * RI + a;
                 g[a] = expf(LT[i * LDT + n - 1]);
                 float row[RJ];
-                lds_row(sS + i * DV + tj * RJ, row);
+                lds_row(sS + i * DVC + tj * RJ, row);
 #pragma unroll
                 for (int b = 0; b < RJ; ++b)
                     acc[a][b] = split ? row[b] : g[a] * row[b];
@@ -422,7 +457,7 @@ __global__ void __launch_bounds__(kThreads)
                     kr[a] = split ? kT[i * LDT + j]
                                   : kT[i * LDT + j] * __expf(LT[i * LDT + n - 1] - LT[i * LDT + j]);
                 }
-                lds_row(sv + j * DV + tj * RJ, vr);
+                lds_row(sv + j * DVC + tj * RJ, vr);
 #pragma unroll
                 for (int a = 0; a < RI; ++a)
 #pragma unroll
@@ -435,11 +470,13 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
                 for (int q = 0; q < RJ / 4; ++q) {
                     const float m = split ? g[a] : 1.0f;
-                    *reinterpret_cast<float4*>(sS + i * DV + tj * RJ + 4 * q) =
+                    *reinterpret_cast<float4*>(sS + i * DVC + tj * RJ + 4 * q) =
                         make_float4(m * acc[a][4 * q], m * acc[a][4 * q + 1], m * acc[a][4 * q + 2],
                                     m * acc[a][4 * q + 3]);
                 }
             }
+        }
+        {
             if (tid < D) {
                 const float lend = LT[tid * LDT + n - 1];
                 const float gz = expf(lend);
@@ -483,12 +520,13 @@ cudaError_t run_gla(const GlaArgs& a)
     err = cudaGetLastError();
     if (err != cudaSuccess)
         return err;
-    const size_t smem = GlaOut<D, DV>::bytes;
+    constexpr int NH = DV > 64 ? DV / 64 : 1;
+    const size_t smem = GlaOut<D, DV / NH>::bytes;
     auto kern = k_gla_out<D, DV, T>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess)
         return err;
-    kern<<<(unsigned)(BH * nblk), kThreads, smem, a.stream>>>(q, k, v, a.alpha, a.out, ws, a.N,
+    kern<<<(unsigned)(BH * nblk * NH), kThreads, smem, a.stream>>>(q, k, v, a.alpha, a.out, ws, a.N,
                                                               nblk, a.fm);
     count_launches(1);
     return cudaGetLastError();
