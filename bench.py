@@ -78,14 +78,16 @@ def job_throughput(units_per_step: int, world: int, steps: int, ms_total: float)
 
 
 # summary file name under profiles/ for the kernels of a path
-PROFILE_NAME = {"k_tg_state+k_tg_scan+k_tg_out": "k_tg"}
+PROFILE_NAME = {"k_tg_state+k_tg_scan+k_tg_out": "k_tg",
+                "k_favor+k_tg_state+k_tg_scan+k_tg_out": "k_favor_tg",
+                "k_gla_state+k_gla_scan+k_gla_out": "k_gla"}
 
 
 def profiled_traffic(kernel: str, workload: str):
     """DRAM bytes per launch (read + write) of `kernel` on `workload`, from the
-    ncu summary under profiles/, or None when there is none or the kernel's
+    ncu summary under profiles/, or None when there is none or a kernel
     source has changed since it was taken (the summary records the SHA-256 of
-    the source file it measured)."""
+    every source file it measured)."""
     import hashlib
     import re
 
@@ -93,13 +95,14 @@ def profiled_traffic(kernel: str, workload: str):
     if not path.exists():
         return None
     text = path.read_text()
-    m_src = re.search(r"^source: (\S+) sha256 ([0-9a-f]{64})$", text, re.M)
+    srcs = re.findall(r"^source: (\S+) sha256 ([0-9a-f]{64})$", text, re.M)
     m_tr = re.search(r"^traffic_bytes_per_launch: (\d+)$", text, re.M)
-    if not m_src or not m_tr:
+    if not srcs or not m_tr:
         return None
-    src = ROOT / m_src.group(1)
-    if not src.exists() or hashlib.sha256(src.read_bytes()).hexdigest() != m_src.group(2):
-        return None
+    for name, digest in srcs:  # every source the summary measured is unchanged
+        src = ROOT / name
+        if not src.exists() or hashlib.sha256(src.read_bytes()).hexdigest() != digest:
+            return None
     return int(m_tr.group(1))
 
 

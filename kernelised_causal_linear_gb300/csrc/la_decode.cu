@@ -34,7 +34,8 @@ struct DecodeTile {
     static_assert(D % TI == 0 && TJ <= kThreads, "tile");
 };
 
-template <int D, int DV, typename T>
+// ALPHA: per-key-channel decay (GLA); else one gamma per head
+template <int D, int DV, typename T, bool ALPHA>
 __global__ void __launch_bounds__(kThreads)
     k_decode_step(float* __restrict__ S, float* __restrict__ z, const T* __restrict__ q,
                   const T* __restrict__ k, const T* __restrict__ v,
@@ -65,7 +66,8 @@ __global__ void __launch_bounds__(kThreads)
     if (tid < D) {
         sfq[tid] = phi_f32(to_f32<T>(q[seq * D + tid]), fm);
         sfk[tid] = phi_f32(to_f32<T>(k[seq * D + tid]), fm);
-        sal[tid] = alpha ? alpha[seq * D + tid] : gm;
+        if (ALPHA)
+            sal[tid] = alpha[seq * D + tid];
     }
     if (tid < DV)
         sv[tid] = to_f32<T>(v[seq * DV + tid]);
@@ -74,7 +76,7 @@ __global__ void __launch_bounds__(kThreads)
     // z update and phi(q).z on the first D threads (whole warps)
     if (tid < D) {
         float* zp = z + seq * D + tid;
-        const float zn = fmaf(sal[tid], *zp, sfk[tid]);
+        const float zn = fmaf(ALPHA ? sal[tid] : gm, *zp, sfk[tid]);
         *zp = zn;
         float part = sfq[tid] * zn;
 #pragma unroll
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int a = 0; a < TL::RI; ++a) {
         const int i = ti + a * TL::TI;
-        const float f = sfk[i], ga = sal[i];
+        const float f = sfk[i], ga = ALPHA ? sal[i] : gm;
         float4 x = s[a];
         x.x = fmaf(ga, x.x, f * vv.x);
         x.y = fmaf(ga, x.y, f * vv.y);
@@ -125,7 +127,8 @@ __global__ void __launch_bounds__(kThreads)
 template <int D, int DV, typename T>
 cudaError_t run_decode(const DecodeArgs& a)
 {
-    k_decode_step<D, DV, T><<<(unsigned)a.BH, kThreads, 0, a.stream>>>(
+    auto kern = a.alpha ? k_decode_step<D, DV, T, true> : k_decode_step<D, DV, T, false>;
+    kern<<<(unsigned)a.BH, kThreads, 0, a.stream>>>(
         a.S, a.z, static_cast<const T*>(a.q), static_cast<const T*>(a.k),
         static_cast<const T*>(a.v), a.alpha, a.out, (int)a.H, a.fm, *a.gamma);
     count_launches(1);
