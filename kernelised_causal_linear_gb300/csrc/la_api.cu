@@ -437,7 +437,7 @@ la_status la_favor_features(const void* x, const float* w, void* out, int64_t ro
         return LA_OK;
     if (!x || !w || !out || !aligned16(x) || !aligned16(w) || !aligned16(out))
         return LA_ERR_INVALID_ARG;
-    return from_cuda(favor_features(x, w, out, rows, d, r, in_dtype, out_dtype,
+    return from_cuda(favor_features(x, w, out, rows, d, r, in_dtype, out_dtype, status_ptr(),
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -138,7 +138,7 @@ cudaError_t state_prefix(const float* S, const float* z, int nparts, const int64
 // positive random features (la_favor_features)
 bool favor_shape_ok(int d, int r);
 cudaError_t favor_features(const void* x, const float* w, void* out, int64_t rows, int d, int r,
-                           int in_dtype, int out_dtype, cudaStream_t st);
+                           int in_dtype, int out_dtype, int* status, cudaStream_t st);
 
 struct DecodeArgs {
     float* S;
