@@ -44,6 +44,16 @@ def test_features_match_oracle(orc, d, r, in_dtype):
     assert relb <= 2.0 ** -8, relb
 
 
+def test_features_many_tiles(orc):
+    """Enough rows for every CTA of the tensor-core form to reuse its x stages
+    and both accumulators several times (128k rows, 1000 tiles of 128)."""
+    x = synth.normal((8, 16, 1000, 64), seed=93, scale=0.7, dtype=torch.bfloat16, device="cuda")
+    w = synth.gaussian_rows(128, 64, seed=94, device="cuda")
+    f = la.la_favor_features(x, w)
+    ref = orc.favor(to_np(x), to_np(w))
+    assert np.max(np.abs(to_np(f) - ref) / ref) < 3e-5
+
+
 @pytest.mark.parametrize("causal", [True, False])
 def test_performer_attention(orc, causal):
     """The Performer workload: features of q and k (r = 128), then the
