@@ -107,7 +107,7 @@ constexpr uint32_t kMiscBytes = 2048;
 constexpr uint32_t OFF_ONES = OFF_MISC + kMiscBytes;   // 2 KiB: the e rows of [V | e]
 constexpr int kMaxL = 8;       // largest segment (chunks)
 #ifndef LA_TC_SEG_DIV
-#define LA_TC_SEG_DIV 12       // segments per CTA the segment length aims at
+#define LA_TC_SEG_DIV 8        // segments per CTA the segment length aims at
 #endif
 constexpr int NPH = 4;         // phi(K) scratch ring depth, in segments
 constexpr uint32_t SMEM_BYTES = OFF_ONES + 2048 + 1024;  // + alignment slack
