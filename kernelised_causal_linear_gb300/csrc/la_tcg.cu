@@ -61,7 +61,6 @@ using namespace tcc;
 
 constexpr int kC = 128;        // tokens per chunk
 constexpr int kT = 64;         // value channels per output tile
-constexpr int kPrefetch = 4;   // chunks the L2 prefetch runs ahead of the loads
 constexpr uint64_t kWaitNs = 2000000000ull;  // any single wait gives up after 2 s
 
 // Rows of the [S^T; z] operand image of one value tile: 64 value channels,
@@ -326,32 +325,11 @@ __global__ void __launch_bounds__(kStThreads, 1) k_tg_state(const __grid_constan
             int u = 0;
             int last_ph[4] = {-1, -1, -1, -1};
             bool ok = true;
-            // L2 prefetch kPrefetch chunks ahead of the loads (walks the same
-            // items and chunks)
-            int pf_it = blockIdx.x, pf_k = 0;
-            auto prefetch_next = [&]() {
-                if (pf_it >= items)
-                    return;
-                const int s = pf_it / p.nseg, g = pf_it % p.nseg;
-                const int c0 = g * p.L, n = min(p.L, p.nchunk - c0);
-                const int row = (c0 + pf_k) * kC;
-                for (int kb = 0; kb < KB; ++kb)
-                    tma_prefetch_l2_3d(&p.mk, 64 * kb, row, s);
-                for (int vb = 0; vb < VB; ++vb)
-                    tma_prefetch_l2_3d(&p.mv, 64 * vb, row, s);
-                if (++pf_k == n) {
-                    pf_k = 0;
-                    pf_it += gridDim.x;
-                }
-            };
-            for (int i = 0; i < kPrefetch; ++i)
-                prefetch_next();
             for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
                 const int s = it / p.nseg, g = it % p.nseg;
                 const int c0 = g * p.L, n = min(p.L, p.nchunk - c0);
                 for (int k = 0; k < n; ++k, ++u) {
                     const int st = u % NST;
-                    prefetch_next();
                     if (u >= NST && !tg_wait(&m->free_[st], ((u / NST) & 1) ^ 1, abort)) {
                         ok = false;
                         break;
@@ -834,7 +812,7 @@ struct OutParams {
 template <int D>
 struct OutLayout {
     static constexpr int KB = D / 64;
-    static constexpr int NQ = D == 64 ? 2 : 1;  // Q stages (Q is reloaded from L2 after a prefetch)
+    static constexpr int NQ = D == 64 ? 2 : 1;  // Q stages
     static constexpr int NKV = D == 64 ? 3 : 2;
     static constexpr uint32_t OFF_ZB = 0, OFF_EB = 2048;       // Z, E below every tile
     static constexpr uint32_t OFF_Q = 4096;                     // NQ x KB x 16 KiB
@@ -930,7 +908,7 @@ __device__ __forceinline__ void decay_row(const unsigned char* v, unsigned char*
 // The CTA is warp-specialised; work flows through shared-memory stages and
 // tensor-memory buffers, synchronised by mbarriers:
 //   warp 0      producer (one thread): the state image of each item, Q, K, V
-//               of each chunk, and an L2 prefetch a few chunks ahead
+//               of each chunk
 //   warp 1      output MMAs (one thread): scores, P [V | 1]
 //   warp 2      state MMAs (one thread): phi(Q) [S^T; z], the state increment
 //   warp 3      decayed values V' = gamma^(C-1-t) V as bf16 hi/lo (decay only)
@@ -1007,28 +985,11 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
         if (lane == 0) {
             const uint64_t stream = policy_evict_first();
             const uint64_t keep = policy_evict_last();
-            Iter iq, ikv, ipf;
+            Iter iq, ikv;
             iq.start(p);
             ikv.start(p);
-            ipf.start(p);
             if (!causal)
                 ikv.done = true;
-            // L2 prefetch of the chunk kPrefetch ahead of the Q stream: the
-            // tiled loads then wait on L2, not on HBM
-            auto prefetch = [&](const Iter& c) {
-                const int row = (c.c0 + c.k) * kC;
-                for (int kb = 0; kb < KB; ++kb)
-                    tma_prefetch_l2_3d(&p.mq, 64 * kb, row, c.s);
-                if (causal) {
-                    for (int kb = 0; kb < KB; ++kb)
-                        tma_prefetch_l2_3d(&p.mk, 64 * kb, row, c.s);
-                    tma_prefetch_l2_3d(&p.mv, kT * c.h, row, c.s);
-                }
-            };
-            for (int i = 0; i < kPrefetch && !ipf.done; ++i) {
-                prefetch(ipf);
-                ipf.advance(p);
-            }
             int jimg = 0;
             bool img_done = false;
             int q_ph[2] = {-1, -1}, kv_ph[3] = {-1, -1, -1}, img_ph = -1;
@@ -1065,10 +1026,6 @@ __global__ void __launch_bounds__(512, 1) k_tg_out(const __grid_constant__ OutPa
                         q_ph[qs] = (iq.u / NQ) & 1;
                         TG_TRACE(iq.u, 0);
                         iq.advance(p);
-                        if (!ipf.done) {
-                            prefetch(ipf);
-                            ipf.advance(p);
-                        }
                         prog = true;
                     }
                 }
@@ -1906,7 +1863,7 @@ cudaError_t tg_run(const FwdArgs& a)
         (causal && !tma_map_bf16_3d(&op.mk, a.k, a.d, a.N, BH)) ||
         (causal && !tma_map_bf16_3d(&op.mv, a.v, a.dv, a.N, BH)))
         return cudaErrorInvalidValue;
-    if (!causal) {  // unused maps still need valid descriptors for the prefetch
+    if (!causal) {  // unused maps still need valid descriptors
         op.mk = op.mq;
         op.mv = op.mq;
     }
