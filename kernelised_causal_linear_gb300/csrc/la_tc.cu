@@ -106,6 +106,7 @@ constexpr uint32_t OFF_MISC = OFF_A + NA * 32768;
 constexpr uint32_t kMiscBytes = 2048;
 constexpr uint32_t OFF_ONES = OFF_MISC + kMiscBytes;   // 2 KiB: the e rows of [V | e]
 constexpr int kMaxL = 8;       // largest segment (chunks)
+constexpr int kMinL = 4;       // smallest segment (chunks), unless the sequence is shorter
 #ifndef LA_TC_SEG_DIV
 #define LA_TC_SEG_DIV 8        // segments per CTA the segment length aims at
 #endif
@@ -1144,9 +1145,11 @@ TcGeom tc_geom(int64_t BH, int64_t N, int sms)
         sms = 148;
     g.nchunk = (int)((N + kC - 1) / kC);
     const int64_t chunks = BH * g.nchunk;
-    // about a dozen segments per CTA keeps the tail short; long segments make
-    // the look-back rare
-    g.L = (int)std::max<int64_t>(1, std::min<int64_t>(kMaxL, chunks / ((int64_t)sms * LA_TC_SEG_DIV)));
+    // about eight segments per CTA keeps the tail short; long segments make
+    // the look-back rare, and below four chunks a segment's own work (phase
+    // A, its slot, the look-back) costs more than the parallelism it buys
+    g.L = (int)std::max<int64_t>(kMinL, std::min<int64_t>(kMaxL, chunks / ((int64_t)sms * LA_TC_SEG_DIV)));
+    g.L = std::min(g.L, g.nchunk);
     g.nseg = (g.nchunk + g.L - 1) / g.L;
     g.total = (int)(BH * g.nseg);
     int G = sms;

@@ -216,7 +216,7 @@ def test_tensor_core_few_sequences_long(orc, B, H, N):
 @pytest.mark.parametrize("B,H,N", [(1, 16, 32768 + 3 * 128), (2, 12, 32700), (5, 8, 32768),
                                    (8, 8, 32768)])
 def test_tensor_core_segment_lengths(orc, B, H, N):
-    """Enough chunks that a segment holds 2, 3, 5 and 8 chunks on a 152-SM GPU
+    """Enough chunks that a segment holds 4, 5 and 8 chunks on a 152-SM GPU
     (one output group then runs a segment's chunks in order, carrying S_prev
     from chunk to chunk), with ragged and short last segments."""
     w = synth.Workload("seglen", B, H, N, 64, 64, torch.bfloat16, seed_id=46)
