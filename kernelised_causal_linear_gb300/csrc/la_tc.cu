@@ -88,7 +88,13 @@ constexpr int NS = 4;          // segment-ticket ring
 constexpr int NSIN = 4;        // S_in image ring (an image lives until its segment's phase C is done)
 constexpr int kStateFloats = kD * kD + kD;         // S^T (dv x d) then z (d)
 constexpr int kSlotFloats = 2 * kStateFloats;      // aggregate, exclusive prefix
-constexpr int kMaxList = 128;                      // look-back entries
+constexpr int kMaxList = 256;                      // look-back entries
+// A look-back walks over the segments of its sequence whose exclusive prefix
+// is not yet out, plus two entries.  A CTA holds at most NS segment tickets
+// whose phase C has not finished (the ticket ring), and a segment's prefix is
+// out before its phase C starts, so at most NS such segments per CTA working
+// on the sequence: 40 CTAs per sequence need at most 40 NS + 2 = 162 entries.
+constexpr int kMaxCtasPerSeq = 40;
 constexpr uint32_t kImgPart = 65 * 128;            // rows 0..64 of one bf16 part (hi or lo)
 constexpr uint32_t kImgBytes = 2 * kImgPart;       // one state operand image: hi, then lo
 constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s for any single wait
@@ -1154,7 +1160,7 @@ TcGeom tc_geom(int64_t BH, int64_t N, int sms)
     g.total = (int)(BH * g.nseg);
     int G = sms;
     G = (int)std::min<int64_t>(G, g.total);
-    G = (int)std::min<int64_t>(G, BH * 20);  // bounds the ring and the look-back list
+    G = (int)std::min<int64_t>(G, BH * kMaxCtasPerSeq);  // bounds the look-back list
     if (G < 1)
         G = 1;
     g.G = G;
@@ -1177,13 +1183,14 @@ TcGeom tc_geom(int64_t BH, int64_t N, int sms)
 
 bool tc_forward_eligible(const FwdArgs& a)
 {
-    // the look-back list bounds this kernel to 20 CTAs per sequence; with
-    // fewer sequences than that needs to fill the GPU, the chunked path
-    // (which splits each sequence over the whole GPU) serves the call
+    // the look-back list bounds this kernel to kMaxCtasPerSeq CTAs per
+    // sequence; with fewer sequences than that needs to fill the GPU, the
+    // chunked path (which splits each sequence over the whole GPU) serves the
+    // call
     const int64_t BH = a.B * a.H;
     const int sms = sm_count() > 0 ? sm_count() : 148;
     return a.dtype == LA_BF16 && a.d == 64 && a.dv == 64 && a.causal == 1 && !a.gamma->has_decay &&
-           a.N >= 1 && a.N <= (int64_t)INT32_MAX - kC && BH * 20 >= sms;
+           a.N >= 1 && a.N <= (int64_t)INT32_MAX - kC && BH * kMaxCtasPerSeq >= sms;
 }
 
 size_t tc_forward_workspace(int64_t BH, int64_t N)

@@ -200,10 +200,10 @@ def test_tensor_core_feature_maps(orc, fm):
 
 
 @pytest.mark.parametrize("B,H,N", [(1, 1, 40000), (3, 1, 5000), (1, 7, 3000), (1, 8, 60000),
-                                   (2, 5, 20000)])
+                                   (2, 5, 20000), (1, 4, 65536)])
 def test_tensor_core_few_sequences_long(orc, B, H, N):
     """Few sequences: with fewer than a GPU's worth the chunked path splits
-    each sequence over every SM; from eight sequences on the single-pass
+    each sequence over every SM; from four sequences on the single-pass
     kernel runs them, with many chunks of one sequence in flight at once and
     deep look-backs."""
     w = synth.Workload("few", B, H, N, 64, 64, torch.bfloat16, seed_id=45)
