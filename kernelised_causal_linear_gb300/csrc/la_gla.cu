@@ -266,23 +266,43 @@ __global__ void __launch_bounds__(kThreads, 2)
         // then channel tid < D turns its log alphas into the running sum L
         // (a warp takes 8 channels x 4 tokens: the transposed stores hit 32
         // different banks)
-        for (int e = tid; e < kSub * D; e += kThreads) {
-            const int wt = e >> 5, cg = wt % (D / 8), tg = wt / (D / 8);
-            const int i = 8 * cg + (e & 7), t = 4 * tg + ((e >> 3) & 3);
-            float la = 0.f, fq = 0.f, fk = 0.f;
-            if (t < n) {
-                const int64_t o = (int64_t)(s0 + t) * D + i;
-                la = logf(ab[o]);
-                fq = phi_f32(ldf(qb + o), fm);
-                fk = phi_f32(ldf(kb + o), fm);
+        // (all of a thread's loads are issued before any is used: the
+        // staging is bound by global-load latency otherwise)
+        {
+            constexpr int NE = kSub * D / kThreads, NVE = kSub * DVC / kThreads;
+            float ra[NE], rq[NE], rk[NE], rv[NVE];
+#pragma unroll
+            for (int x = 0; x < NE; ++x) {
+                const int e = tid + x * kThreads;
+                const int wt = e >> 5, cg = wt % (D / 8), tg = wt / (D / 8);
+                const int i = 8 * cg + (e & 7), t = 4 * tg + ((e >> 3) & 3);
+                ra[x] = 1.f, rq[x] = 0.f, rk[x] = 0.f;
+                if (t < n) {
+                    const int64_t o = (int64_t)(s0 + t) * D + i;
+                    ra[x] = __ldg(ab + o);
+                    rq[x] = ldf(qb + o);
+                    rk[x] = ldf(kb + o);
+                }
             }
-            LT[i * LDT + t] = la;
-            qT[i * LDT + t] = fq;
-            kT[i * LDT + t] = fk;
-        }
-        for (int e = tid; e < kSub * DVC; e += kThreads) {
-            const int t = e / DVC, c = e % DVC;
-            sv[e] = t < n ? ldf(vb + (int64_t)(s0 + t) * DV + c) : 0.f;
+#pragma unroll
+            for (int x = 0; x < NVE; ++x) {
+                const int e = tid + x * kThreads;
+                const int t = e / DVC, c = e % DVC;
+                rv[x] = t < n ? ldf(vb + (int64_t)(s0 + t) * DV + c) : 0.f;
+            }
+#pragma unroll
+            for (int x = 0; x < NE; ++x) {
+                const int e = tid + x * kThreads;
+                const int wt = e >> 5, cg = wt % (D / 8), tg = wt / (D / 8);
+                const int i = 8 * cg + (e & 7), t = 4 * tg + ((e >> 3) & 3);
+                const bool in = t < n;
+                LT[i * LDT + t] = in ? logf(ra[x]) : 0.f;
+                qT[i * LDT + t] = in ? phi_f32(rq[x], fm) : 0.f;
+                kT[i * LDT + t] = in ? phi_f32(rk[x], fm) : 0.f;
+            }
+#pragma unroll
+            for (int x = 0; x < NVE; ++x)
+                sv[tid + x * kThreads] = rv[x];
         }
         __syncthreads();
         if (tid < D) {
