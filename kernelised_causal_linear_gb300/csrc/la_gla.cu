@@ -116,11 +116,31 @@ __global__ void __launch_bounds__(kThreads)
     float zacc = 0.f;
     for (int s0 = 0; s0 < len; s0 += kSub) {
         const int n = min(kSub, len - s0);
-        for (int e = tid; e < kSub * D; e += kThreads) {
-            const int t = e / D, i = e % D;
-            const bool in = t < n;
-            sl[t][i] = in ? logf(ab[(int64_t)(s0 + t) * D + i]) : 0.f;
-            sk[t][i] = in ? phi_f32(ldf(kb + (int64_t)(s0 + t) * D + i), fm) : 0.f;
+        {
+            // loads issued in batches of up to eight elements before use
+            constexpr int NE = kSub * D / kThreads, NB = NE < 8 ? NE : 8;
+#pragma unroll 1
+            for (int x0 = 0; x0 < NE; x0 += NB) {
+                float ra[NB], rk[NB];
+#pragma unroll
+                for (int x = 0; x < NB; ++x) {
+                    const int e = tid + (x0 + x) * kThreads;
+                    const int t = e / D, i = e % D;
+                    ra[x] = 1.f, rk[x] = 0.f;
+                    if (t < n) {
+                        ra[x] = __ldg(ab + (int64_t)(s0 + t) * D + i);
+                        rk[x] = ldf(kb + (int64_t)(s0 + t) * D + i);
+                    }
+                }
+#pragma unroll
+                for (int x = 0; x < NB; ++x) {
+                    const int e = tid + (x0 + x) * kThreads;
+                    const int t = e / D, i = e % D;
+                    const bool in = t < n;
+                    sl[t][i] = in ? logf(ra[x]) : 0.f;
+                    sk[t][i] = in ? phi_f32(rk[x], fm) : 0.f;
+                }
+            }
         }
         __syncthreads();
         if (tid < D)  // the running log-sum, and the weight exp(L_end - L_t)
