@@ -148,9 +148,23 @@ __global__ void __launch_bounds__(kThreads)
                 run += sl[t][tid];
                 sk[t][tid] *= expf(slog[tid] - run);
             }
-        for (int e = tid; e < kSub * DV; e += kThreads) {
-            const int t = e / DV, c = e % DV;
-            sv[t][c] = t < n ? ldf(vb + (int64_t)(s0 + t) * DV + c) : 0.f;
+        {
+            constexpr int NVE = kSub * DV / kThreads, NB = NVE < 8 ? NVE : 8;
+#pragma unroll 1
+            for (int x0 = 0; x0 < NVE; x0 += NB) {
+                float rv[NB];
+#pragma unroll
+                for (int x = 0; x < NB; ++x) {
+                    const int e = tid + (x0 + x) * kThreads;
+                    const int t = e / DV, c = e % DV;
+                    rv[x] = t < n ? ldf(vb + (int64_t)(s0 + t) * DV + c) : 0.f;
+                }
+#pragma unroll
+                for (int x = 0; x < NB; ++x) {
+                    const int e = tid + (x0 + x) * kThreads;
+                    sv[e / DV][e % DV] = rv[x];
+                }
+            }
         }
         __syncthreads();
 #pragma unroll 4
