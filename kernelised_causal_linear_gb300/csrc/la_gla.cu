@@ -234,6 +234,80 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // ------------------------------------------------------------- step 3 ----
+// Warp-level bf16 tensor-core products (mma.sync m16n8k16, fp32
+// accumulate) for the output kernel's sub-chunk products with bf16 inputs.
+// Fragment layouts (lane = 4 g + q): A 16 x 16 row-major, registers
+// {A[g][2q..2q+1]}, {A[g+8][2q..]}, {A[g][2q+8..]}, {A[g+8][2q+8..]}; B 16 x 8,
+// {B[2q..2q+1][g]}, {B[2q+8..2q+9][g]}; C 16 x 8, C[g][2q], C[g][2q+1],
+// C[g+8][2q], C[g+8][2q+1].
+__device__ __forceinline__ uint32_t bf2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// two fp32 -> packed bf16 hi and lo parts (hi + lo = x to ~2^-17)
+__device__ __forceinline__ void bf2_split(float a, float b, uint32_t& hi, uint32_t& lo)
+{
+    hi = bf2(a, b);
+    const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&hi);
+    lo = bf2(a - __low2float(h), b - __high2float(h));
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// A[m][k] = X[k * ld + m] (X stored transposed), tile rows m0.., k0.., as hi and lo
+// parts
+__device__ __forceinline__ void frag_a_t_split(const float* X, int ld, int m0, int k0, int g,
+                                               int q, uint32_t (&ah)[4], uint32_t (&al)[4])
+{
+    const float* p = X + (k0 + 2 * q) * ld + m0 + g;
+    bf2_split(p[0], p[ld], ah[0], al[0]);
+    bf2_split(p[8], p[ld + 8], ah[1], al[1]);
+    bf2_split(p[8 * ld], p[9 * ld], ah[2], al[2]);
+    bf2_split(p[8 * ld + 8], p[9 * ld + 8], ah[3], al[3]);
+}
+
+// A[m][k] = X[m * ld + k] (row-major, ld and k0 even), as hi and lo parts
+__device__ __forceinline__ void frag_a_r_split(const float* X, int ld, int m0, int k0, int g, int q,
+                                               uint32_t (&ah)[4], uint32_t (&al)[4])
+{
+    const float* p = X + (m0 + g) * ld + k0 + 2 * q;
+    const float2 x0 = *reinterpret_cast<const float2*>(p);
+    const float2 x1 = *reinterpret_cast<const float2*>(p + 8 * ld);
+    const float2 x2 = *reinterpret_cast<const float2*>(p + 8);
+    const float2 x3 = *reinterpret_cast<const float2*>(p + 8 * ld + 8);
+    bf2_split(x0.x, x0.y, ah[0], al[0]);
+    bf2_split(x1.x, x1.y, ah[1], al[1]);
+    bf2_split(x2.x, x2.y, ah[2], al[2]);
+    bf2_split(x3.x, x3.y, ah[3], al[3]);
+}
+
+// B[k][n] = X[k * ld + n], tile k0.., n0..
+__device__ __forceinline__ void frag_b(const float* X, int ld, int k0, int n0, int g, int q,
+                                       uint32_t& b0, uint32_t& b1)
+{
+    const float* p = X + (k0 + 2 * q) * ld + n0 + g;
+    b0 = bf2(p[0], p[ld]);
+    b1 = bf2(p[8 * ld], p[9 * ld]);
+}
+
+__device__ __forceinline__ void frag_b_split(const float* X, int ld, int k0, int n0, int g, int q,
+                                             uint32_t (&bh)[2], uint32_t (&bl)[2])
+{
+    const float* p = X + (k0 + 2 * q) * ld + n0 + g;
+    bf2_split(p[0], p[ld], bh[0], bl[0]);
+    bf2_split(p[8 * ld], p[9 * ld], bh[1], bl[1]);
+}
+
 // Shared memory of the output kernel (floats): the running state S [D][DV]
 // and z [D]; phi(q), phi(k) and the running log-sums L of the sub-chunk,
 // transposed ([D][LDT], token fastest); v [kSub][DV]; the intra weights
@@ -241,9 +315,12 @@ __global__ void __launch_bounds__(kThreads)
 template <int D, int DV>
 struct GlaOut {
     static constexpr int LDT = kSub + 4;
-    static constexpr size_t oZ = (size_t)D * DV, oQ = oZ + D, oK = oQ + (size_t)D * LDT,
+    // row strides of the state and value tiles: 4 floats of padding put
+    // rows 2q (q = 0..3) of a tensor-core operand fragment in different banks
+    static constexpr int SS = DV + 4, SV = DV + 4;
+    static constexpr size_t oZ = (size_t)D * SS, oQ = oZ + D, oK = oQ + (size_t)D * LDT,
                             oL = oK + (size_t)D * LDT, oV = oL + (size_t)D * LDT,
-                            oA = oV + (size_t)kSub * DV, oDen = oA + (size_t)kSub * LDT,
+                            oA = oV + (size_t)kSub * SV, oDen = oA + (size_t)kSub * LDT,
                             floats = oDen + kSub;
     static constexpr size_t bytes = floats * sizeof(float);
     // output tiles of 4 tokens x 4 value columns (OT threads); state-update
@@ -264,14 +341,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     // DV = 128: half the state in shared memory, two CTAs per SM)
     constexpr int DVC = DV > 64 ? 64 : DV, NH = DV / DVC;
     using G = GlaOut<D, DVC>;
-    constexpr int LDT = G::LDT, E = D * DV + D;
+    constexpr int LDT = G::LDT, SS = G::SS, SV = G::SV, E = D * DV + D;
+    // bf16 inputs at d = 128 with 64 value columns per CTA: the products of
+    // a sub-chunk whose decay factors split run on the tensor cores (bf16
+    // operands, fp32 accumulation).  The rescaled features, the state and the
+    // intra weights are fp32 and enter as bf16 hi/lo pairs (hi*hi + hi*lo +
+    // lo*hi, ~2^-16 relative: a single rounding of the features showed in
+    // the unnormalised outputs, whose sums cancel); v is exact in bf16.
+    constexpr bool kMma = sizeof(T) == 2 && D == 128 && DVC == 64;
     extern __shared__ __align__(16) float smem[];
     float* sS = smem;
     float* sz = smem + G::oZ;
     float* qT = smem + G::oQ;  // qT[i * LDT + t]
     float* kT = smem + G::oK;
     float* LT = smem + G::oL;
-    float* sv = smem + G::oV;  // sv[t * DVC + c]
+    float* sv = smem + G::oV;  // sv[t * SV + c]
     float* AT = smem + G::oA;  // AT[j * LDT + t]
     float* sden = smem + G::oDen;
 
@@ -284,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const bool norm = fm_normalised(fm);
     for (int e = tid; e < D * DVC; e += kThreads)
-        sS[e] = ws[gb * E + (e / DVC) * DV + c_off + e % DVC];
+        sS[(e / DVC) * SS + e % DVC] = ws[gb * E + (e / DVC) * DV + c_off + e % DVC];
     for (int i = tid; i < D; i += kThreads)
         sz[i] = ws[gb * E + D * DV + i];
     const T* qb = qp + (seq * N + t0) * D;
@@ -336,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
 #pragma unroll
             for (int x = 0; x < NVE; ++x)
-                sv[tid + x * kThreads] = rv[x];
+                sv[((tid + x * kThreads) / DVC) * SV + (tid + x * kThreads) % DVC] = rv[x];
         }
         __syncthreads();
         if (tid < D) {
@@ -365,7 +449,25 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         // intra weights A_tj = sum_i q_ti k_ji exp(L_ti - L_ji), j <= t:
         // thread (ty, tx) takes tokens 4 ty .. 4 ty + 3 and key token tx
-        if (split) {
+        if (kMma && split) {
+            // warp w: tokens 16 (w & 1) .. + 15, keys 8 (w >> 1) .. + 7
+            const int g = lane >> 2, q = lane & 3, m0 = 16 * (warp & 1), n0 = 8 * (warp >> 1);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k0 = 0; k0 < D; k0 += 16) {
+                uint32_t ah[4], al[4], bh[2], bl[2];
+                frag_a_t_split(qT, LDT, m0, k0, g, q, ah, al);
+                frag_b_split(kT, LDT, k0, n0, g, q, bh, bl);
+                mma16816(acc, ah, bh[0], bh[1]);
+                mma16816(acc, ah, bl[0], bl[1]);
+                mma16816(acc, al, bh[0], bh[1]);
+            }
+            const int t0 = m0 + g, j0 = n0 + 2 * q;
+            AT[j0 * LDT + t0] = j0 <= t0 ? acc[0] : 0.f;
+            AT[(j0 + 1) * LDT + t0] = j0 + 1 <= t0 ? acc[1] : 0.f;
+            AT[j0 * LDT + t0 + 8] = j0 <= t0 + 8 ? acc[2] : 0.f;
+            AT[(j0 + 1) * LDT + t0 + 8] = j0 + 1 <= t0 + 8 ? acc[3] : 0.f;
+        } else if (split) {
             // 64 threads, 4 tokens x 4 key tokens each (two 16-byte loads per
             // 16 FMAs)
             if (tid < (kSub / 4) * (kSub / 4)) {
@@ -435,7 +537,50 @@ __global__ void __launch_bounds__(kThreads, 2)
             __syncthreads();
         }
         // outputs: thread (oi, oj) < OT takes 4 tokens x 4 columns
-        if (tid < G::OT) {
+        if (kMma && split) {
+            // warp w: value columns 8 w .. 8 w + 7 of all 32 tokens
+            const int g = lane >> 2, q = lane & 3, n0 = 8 * warp;
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 2
+            for (int k0 = 0; k0 < D; k0 += 16) {
+                uint32_t bh[2], bl[2];
+                frag_b_split(sS, SS, k0, n0, g, q, bh, bl);
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    uint32_t ah[4], al[4];
+                    frag_a_t_split(qT, LDT, 16 * mt, k0, g, q, ah, al);
+                    mma16816(acc[mt], ah, bh[0], bh[1]);
+                    mma16816(acc[mt], ah, bl[0], bl[1]);
+                    mma16816(acc[mt], al, bh[0], bh[1]);
+                }
+            }
+#pragma unroll
+            for (int k0 = 0; k0 < kSub; k0 += 16) {
+                uint32_t b0, b1;
+                frag_b(sv, SV, k0, n0, g, q, b0, b1);
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    uint32_t ah[4], al[4];
+                    frag_a_t_split(AT, LDT, 16 * mt, k0, g, q, ah, al);
+                    mma16816(acc[mt], ah, b0, b1);
+                    mma16816(acc[mt], al, b0, b1);
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int t = 16 * mt + g + 8 * h;
+                    if (t < n) {
+                        float2 o = make_float2(acc[mt][2 * h], acc[mt][2 * h + 1]);
+                        if (norm) {
+                            const float inv = 1.0f / fmaxf(sden[t], FLT_MIN);
+                            o.x *= inv, o.y *= inv;
+                        }
+                        *reinterpret_cast<float2*>(ob + (int64_t)(s0 + t) * DV + n0 + 2 * q) = o;
+                    }
+                }
+        } else if (tid < G::OT) {
             constexpr int ORI = 4;
             const int oj = tid % G::OJ, oi = tid / G::OJ;
             const int tb = oi * ORI, c0 = 4 * oj;
@@ -451,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                     for (int r = 0; r < ORI; ++r)
                         qv[r] *= expf(LT[i * LDT + tb + r]);
-                const float4 s4 = *reinterpret_cast<const float4*>(sS + i * DVC + c0);
+                const float4 s4 = *reinterpret_cast<const float4*>(sS + i * SS + c0);
 #pragma unroll
                 for (int r = 0; r < ORI; ++r) {
                     acc[r][0] = fmaf(qv[r], s4.x, acc[r][0]);
@@ -464,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int j = 0; j < kSub; ++j) {
                 float av[ORI];
                 lds_row(AT + j * LDT + tb, av);
-                const float4 v4 = *reinterpret_cast<const float4*>(sv + j * DVC + c0);
+                const float4 v4 = *reinterpret_cast<const float4*>(sv + j * SV + c0);
 #pragma unroll
                 for (int r = 0; r < ORI; ++r) {
                     acc[r][0] = fmaf(av[r], v4.x, acc[r][0]);
@@ -488,7 +633,39 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         __syncthreads();  // every read of S, z for this sub-chunk is done
         // S <- diag(exp(L_end)) S + sum_j (phi(k_j) o exp(L_end - L_j)) v_j^T ; z alike
-        if (tid < G::UT) {
+        if (kMma && split) {
+            // warp w: channels 16 w .. 16 w + 15, all 64 value columns; the
+            // accumulators start from S and end scaled by exp(L_end)
+            const int g = lane >> 2, q = lane & 3, m0 = 16 * warp;
+            float acc[8][4];
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                const float2 x0 = *reinterpret_cast<const float2*>(sS + (m0 + g) * SS + 8 * nt + 2 * q);
+                const float2 x1 =
+                    *reinterpret_cast<const float2*>(sS + (m0 + g + 8) * SS + 8 * nt + 2 * q);
+                acc[nt][0] = x0.x, acc[nt][1] = x0.y, acc[nt][2] = x1.x, acc[nt][3] = x1.y;
+            }
+#pragma unroll
+            for (int k0 = 0; k0 < kSub; k0 += 16) {
+                uint32_t ah[4], al[4];
+                frag_a_r_split(kT, LDT, m0, k0, g, q, ah, al);
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt) {
+                    uint32_t b0, b1;
+                    frag_b(sv, SV, k0, 8 * nt, g, q, b0, b1);
+                    mma16816(acc[nt], ah, b0, b1);
+                    mma16816(acc[nt], al, b0, b1);
+                }
+            }
+            const float g0 = expf(LT[(m0 + g) * LDT + n - 1]), g1 = expf(LT[(m0 + g + 8) * LDT + n - 1]);
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                *reinterpret_cast<float2*>(sS + (m0 + g) * SS + 8 * nt + 2 * q) =
+                    make_float2(g0 * acc[nt][0], g0 * acc[nt][1]);
+                *reinterpret_cast<float2*>(sS + (m0 + g + 8) * SS + 8 * nt + 2 * q) =
+                    make_float2(g1 * acc[nt][2], g1 * acc[nt][3]);
+            }
+        } else if (tid < G::UT) {
             constexpr int RI = G::UR, RJ = 8;
             const int tj = tid % G::UJ, ti = tid / G::UJ;
             float g[RI], acc[RI][RJ];
@@ -497,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int i = ti * RI + a;
                 g[a] = expf(LT[i * LDT + n - 1]);
                 float row[RJ];
-                lds_row(sS + i * DVC + tj * RJ, row);
+                lds_row(sS + i * SS + tj * RJ, row);
 #pragma unroll
                 for (int b = 0; b < RJ; ++b)
                     acc[a][b] = split ? row[b] : g[a] * row[b];
@@ -511,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     kr[a] = split ? kT[i * LDT + j]
                                   : kT[i * LDT + j] * __expf(LT[i * LDT + n - 1] - LT[i * LDT + j]);
                 }
-                lds_row(sv + j * DVC + tj * RJ, vr);
+                lds_row(sv + j * SV + tj * RJ, vr);
 #pragma unroll
                 for (int a = 0; a < RI; ++a)
 #pragma unroll
@@ -524,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int q = 0; q < RJ / 4; ++q) {
                     const float m = split ? g[a] : 1.0f;
-                    *reinterpret_cast<float4*>(sS + i * DVC + tj * RJ + 4 * q) =
+                    *reinterpret_cast<float4*>(sS + i * SS + tj * RJ + 4 * q) =
                         make_float4(m * acc[a][4 * q], m * acc[a][4 * q + 1], m * acc[a][4 * q + 2],
                                     m * acc[a][4 * q + 3]);
                 }

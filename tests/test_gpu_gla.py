@@ -69,6 +69,25 @@ def test_gla_decode_continues_forward(orc):
     for t in range(N):
         o = la.la_decode_step_gla(S, z, q[:, :, t].contiguous(), k[:, :, t].contiguous(),
                                   v[:, :, t].contiguous(), a[:, :, t].contiguous())
-        assert rel_err_rows(o, to_np(full[:, :, t])) <= 1e-5
+        # bf16 inputs at d = 128: the forward's sub-chunk products run on the
+        # tensor cores (bf16 operands, the bf16 tolerance); the decode step is
+        # fp32 throughout and meets 1e-5 against the oracle below
+        assert rel_err_rows(o, to_np(full[:, :, t])) <= TOL[torch.bfloat16]
     ref = orc.forward(to_np(q), to_np(k), to_np(v), alpha=to_np(a))
     assert rel_err_rows(o, ref[:, :, -1]) <= 1e-5
+
+
+@pytest.mark.parametrize("lo", [0.5, 0.01])
+def test_gla_tensor_core_sub_chunks(orc, lo):
+    """bf16 inputs at d = dv = 128 take the tensor-core products in every
+    sub-chunk whose decay splits (gates >= 0.5 over 32 tokens) and the fp32
+    products where it does not (gates down to 0.01); both forms in one call,
+    several blocks and a ragged tail."""
+    w = synth.Workload("gla4", 2, 2, 777, 128, 128, torch.bfloat16, q_scale=0.5, k_scale=0.5,
+                       feature_map="none", seed_id=103)
+    q, k, v = synth.qkv(w, device="cuda")
+    a = synth.gates((2, 2, 777, 128), seed=104, lo=lo, hi=1.0, device="cuda")
+    for fm in ("none", "elu1"):
+        out = la.la_forward_gla(q, k, v, a, feature_map=fm)
+        ref = orc.forward(to_np(q), to_np(k), to_np(v), fm=fm, alpha=to_np(a))
+        assert rel_err_rows(out, ref) <= TOL[torch.bfloat16], fm
