@@ -41,202 +41,9 @@ __device__ __forceinline__ float ldf(const T* p)
     return to_f32<T>(*p);
 }
 
-// ------------------------------------------------------------- step 1 ----
-// Thread (ti, tj) owns RI consecutive rows (channels) x RJ consecutive value
-// columns of the D x DV block state: per token, RI + RJ shared loads (16-byte
-// where they line up) feed RI x RJ FMAs.  The running log-sum of each channel
-// is kept by thread i < D.
-template <int D, int DV>
-struct StateTile {
-    static constexpr int RJ = (D * DV / kThreads >= 8) ? 8 : 4;
-    static constexpr int TJ = DV / RJ;
-    static constexpr int TI = kThreads / TJ;
-    static constexpr int RI = D / TI;
-    static_assert(RI >= 1 && TI * TJ == kThreads && RI * TI == D, "state tile");
-};
-
-template <int N>
-__device__ __forceinline__ void lds_row(const float* p, float (&x)[N])
-{
-    if constexpr (N % 4 == 0) {
-#pragma unroll
-        for (int q = 0; q < N / 4; ++q) {
-            const float4 v = reinterpret_cast<const float4*>(p)[q];
-            x[4 * q] = v.x, x[4 * q + 1] = v.y, x[4 * q + 2] = v.z, x[4 * q + 3] = v.w;
-        }
-    } else {
-#pragma unroll
-        for (int q = 0; q < N; ++q)
-            x[q] = p[q];
-    }
-}
-
-template <int D, int DV, typename T>
-__global__ void __launch_bounds__(kThreads)
-    k_gla_state(const T* __restrict__ kp, const T* __restrict__ vp, const float* __restrict__ ap,
-                float* __restrict__ ws, float* __restrict__ dec, int64_t N, int nblk, int fm)
-{
-    using TL = StateTile<D, DV>;
-    constexpr int TJ = TL::TJ, RI = TL::RI, RJ = TL::RJ;
-    // dynamic shared memory (more than the 48 KiB of static arrays with
-    // D = DV = 128): phi(k) o exp(L_end - L_t), v, log alpha, L_end
-    extern __shared__ __align__(16) float st_smem[];
-    float(*sk)[D] = reinterpret_cast<float(*)[D]>(st_smem);
-    float(*sv)[DV] = reinterpret_cast<float(*)[DV]>(st_smem + kSub * D);
-    float(*sl)[D] = reinterpret_cast<float(*)[D]>(st_smem + kSub * (D + DV));
-    float* slog = st_smem + kSub * (2 * D + DV);
-    const int64_t gb = blockIdx.x;
-    const int64_t seq = gb / nblk;
-    const int blk = (int)(gb % nblk);
-    const int64_t t0 = (int64_t)blk * kBlockL;
-    const int len = (int)min((int64_t)kBlockL, N - t0);
-    const T* kb = kp + (seq * N + t0) * D;
-    const T* vb = vp + (seq * N + t0) * DV;
-    const float* ab = ap + (seq * N + t0) * D;
-    const int tid = threadIdx.x, tj = tid % TJ, ti = tid / TJ;
-
-    // total log decay of the block per channel, summed in token order like
-    // the running sums below (so that the last weight is exactly 1); the
-    // loads do not depend on the sum and stay in flight
-    if (tid < D) {
-        float l = 0.f;
-#pragma unroll 8
-        for (int t = 0; t < len; ++t)
-            l += logf(ab[(int64_t)t * D + tid]);
-        slog[tid] = l;
-    }
-    float run = 0.f;  // L_t of channel tid (tid < D), running
-    __syncthreads();
-    float acc[RI][RJ];
-#pragma unroll
-    for (int a = 0; a < RI; ++a)
-#pragma unroll
-        for (int b = 0; b < RJ; ++b)
-            acc[a][b] = 0.f;
-    float zacc = 0.f;
-    for (int s0 = 0; s0 < len; s0 += kSub) {
-        const int n = min(kSub, len - s0);
-        {
-            // loads issued in batches of up to eight elements before use
-            constexpr int NE = kSub * D / kThreads, NB = NE < 8 ? NE : 8;
-#pragma unroll 1
-            for (int x0 = 0; x0 < NE; x0 += NB) {
-                float ra[NB], rk[NB];
-#pragma unroll
-                for (int x = 0; x < NB; ++x) {
-                    const int e = tid + (x0 + x) * kThreads;
-                    const int t = e / D, i = e % D;
-                    ra[x] = 1.f, rk[x] = 0.f;
-                    if (t < n) {
-                        ra[x] = __ldg(ab + (int64_t)(s0 + t) * D + i);
-                        rk[x] = ldf(kb + (int64_t)(s0 + t) * D + i);
-                    }
-                }
-#pragma unroll
-                for (int x = 0; x < NB; ++x) {
-                    const int e = tid + (x0 + x) * kThreads;
-                    const int t = e / D, i = e % D;
-                    const bool in = t < n;
-                    sl[t][i] = in ? logf(ra[x]) : 0.f;
-                    sk[t][i] = in ? phi_f32(rk[x], fm) : 0.f;
-                }
-            }
-        }
-        __syncthreads();
-        if (tid < D)  // the running log-sum, and the weight exp(L_end - L_t)
-            for (int t = 0; t < n; ++t) {
-                run += sl[t][tid];
-                sk[t][tid] *= expf(slog[tid] - run);
-            }
-        {
-            constexpr int NVE = kSub * DV / kThreads, NB = NVE < 8 ? NVE : 8;
-#pragma unroll 1
-            for (int x0 = 0; x0 < NVE; x0 += NB) {
-                float rv[NB];
-#pragma unroll
-                for (int x = 0; x < NB; ++x) {
-                    const int e = tid + (x0 + x) * kThreads;
-                    const int t = e / DV, c = e % DV;
-                    rv[x] = t < n ? ldf(vb + (int64_t)(s0 + t) * DV + c) : 0.f;
-                }
-#pragma unroll
-                for (int x = 0; x < NB; ++x) {
-                    const int e = tid + (x0 + x) * kThreads;
-                    sv[e / DV][e % DV] = rv[x];
-                }
-            }
-        }
-        __syncthreads();
-#pragma unroll 4
-        for (int t = 0; t < kSub; ++t) {
-            float kr[RI], vr[RJ];
-            lds_row(&sk[t][ti * RI], kr);
-            lds_row(&sv[t][tj * RJ], vr);
-#pragma unroll
-            for (int a = 0; a < RI; ++a)
-#pragma unroll
-                for (int b = 0; b < RJ; ++b)
-                    acc[a][b] = fmaf(kr[a], vr[b], acc[a][b]);
-            if (tid < D)
-                zacc += sk[t][tid];
-        }
-        __syncthreads();
-    }
-    float* dst = ws + gb * (int64_t)(D * DV + D);
-#pragma unroll
-    for (int a = 0; a < RI; ++a) {
-        const int i = ti * RI + a;
-#pragma unroll
-        for (int q = 0; q < RJ / 4; ++q)
-            *reinterpret_cast<float4*>(dst + i * DV + tj * RJ + 4 * q) =
-                make_float4(acc[a][4 * q], acc[a][4 * q + 1], acc[a][4 * q + 2], acc[a][4 * q + 3]);
-    }
-    if (tid < D) {
-        dst[D * DV + tid] = zacc;
-        dec[gb * D + tid] = expf(slog[tid]);
-    }
-}
-
-// ------------------------------------------------------------- step 2 ----
-// Exclusive prefix over the blocks of each sequence, in place: element e of
-// the state (row i = e / DV, or the normaliser entry i) decays by the block's
-// exp(L_end) of channel i.
-__global__ void __launch_bounds__(kThreads)
-    k_gla_scan(float* __restrict__ ws, const float* __restrict__ dec, int nblk, int D, int DV)
-{
-    const int E = D * DV + D;
-    const int per_seq = (E + kThreads - 1) / kThreads;
-    const int64_t seq = blockIdx.x / per_seq;
-    const int e = (int)(blockIdx.x % per_seq) * kThreads + threadIdx.x;
-    if (e >= E)
-        return;
-    const int row = e < D * DV ? e / DV : e - D * DV;
-    float* base = ws + seq * (int64_t)nblk * E + e;
-    const float* db = dec + seq * (int64_t)nblk * D + row;
-    // kAhead blocks' values and decays in flight at a time
-    constexpr int kAhead = 8;
-    float acc = 0.f;
-    for (int b0 = 0; b0 < nblk; b0 += kAhead) {
-        float x[kAhead], dd[kAhead];
-#pragma unroll
-        for (int i = 0; i < kAhead; ++i)
-            if (b0 + i < nblk) {
-                x[i] = __ldcg(base + (int64_t)(b0 + i) * E);
-                dd[i] = __ldg(db + (int64_t)(b0 + i) * D);
-            }
-#pragma unroll
-        for (int i = 0; i < kAhead; ++i)
-            if (b0 + i < nblk) {
-                base[(int64_t)(b0 + i) * E] = acc;
-                acc = fmaf(acc, dd[i], x[i]);
-            }
-    }
-}
-
-// ------------------------------------------------------------- step 3 ----
 // Warp-level bf16 tensor-core products (mma.sync m16n8k16, fp32
-// accumulate) for the output kernel's sub-chunk products with bf16 inputs.
-// Fragment layouts (lane = 4 g + q): A 16 x 16 row-major, registers
+// accumulate) for the sub-chunk products of the block-state and output
+// kernels with bf16 inputs.  Fragment layouts (lane = 4 g + q): A 16 x 16 row-major, registers
 // {A[g][2q..2q+1]}, {A[g+8][2q..]}, {A[g][2q+8..]}, {A[g+8][2q+8..]}; B 16 x 8,
 // {B[2q..2q+1][g]}, {B[2q+8..2q+9][g]}; C 16 x 8, C[g][2q], C[g][2q+1],
 // C[g+8][2q], C[g+8][2q+1].
@@ -308,6 +115,239 @@ __device__ __forceinline__ void frag_b_split(const float* X, int ld, int k0, int
     bf2_split(p[8 * ld], p[9 * ld], bh[1], bl[1]);
 }
 
+// ------------------------------------------------------------- step 1 ----
+// Thread (ti, tj) owns RI consecutive rows (channels) x RJ consecutive value
+// columns of the D x DV block state: per token, RI + RJ shared loads (16-byte
+// where they line up) feed RI x RJ FMAs.  The running log-sum of each channel
+// is kept by thread i < D.
+template <int D, int DV>
+struct StateTile {
+    static constexpr int RJ = (D * DV / kThreads >= 8) ? 8 : 4;
+    static constexpr int TJ = DV / RJ;
+    static constexpr int TI = kThreads / TJ;
+    static constexpr int RI = D / TI;
+    static_assert(RI >= 1 && TI * TJ == kThreads && RI * TI == D, "state tile");
+};
+
+template <int N>
+__device__ __forceinline__ void lds_row(const float* p, float (&x)[N])
+{
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < N / 4; ++q) {
+            const float4 v = reinterpret_cast<const float4*>(p)[q];
+            x[4 * q] = v.x, x[4 * q + 1] = v.y, x[4 * q + 2] = v.z, x[4 * q + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < N; ++q)
+            x[q] = p[q];
+    }
+}
+
+template <int D, int DV, typename T>
+__global__ void __launch_bounds__(kThreads)
+    k_gla_state(const T* __restrict__ kp, const T* __restrict__ vp, const float* __restrict__ ap,
+                float* __restrict__ ws, float* __restrict__ dec, int64_t N, int nblk, int fm)
+{
+    using TL = StateTile<D, DV>;
+    constexpr int TJ = TL::TJ, RI = TL::RI, RJ = TL::RJ;
+    // bf16 inputs at d = 128: the block state is a tensor-core product
+    // (mma.sync m16n8k16, fp32 accumulation) of phi(k) o exp(L_end - L_t),
+    // an fp32 bf16 hi/lo pair, and v, exact in bf16; warp w owns state rows
+    // 16 w .. 16 w + 15
+    constexpr bool kMma = sizeof(T) == 2 && D == 128 && (DV == 128 || DV == 64);
+    constexpr int NT = DV / 8;  // 8-column tiles of a warp's rows
+    // dynamic shared memory (more than the 48 KiB of static arrays with
+    // D = DV = 128): phi(k) o exp(L_end - L_t), v (rows padded by 4 floats,
+    // so that the operand fragments hit different banks), log alpha, L_end
+    extern __shared__ __align__(16) float st_smem[];
+    float(*sk)[D + 4] = reinterpret_cast<float(*)[D + 4]>(st_smem);
+    float(*sv)[DV + 4] = reinterpret_cast<float(*)[DV + 4]>(st_smem + kSub * (D + 4));
+    float(*sl)[D] = reinterpret_cast<float(*)[D]>(st_smem + kSub * (D + DV + 8));
+    float* slog = st_smem + kSub * (2 * D + DV + 8);
+    const int64_t gb = blockIdx.x;
+    const int64_t seq = gb / nblk;
+    const int blk = (int)(gb % nblk);
+    const int64_t t0 = (int64_t)blk * kBlockL;
+    const int len = (int)min((int64_t)kBlockL, N - t0);
+    const T* kb = kp + (seq * N + t0) * D;
+    const T* vb = vp + (seq * N + t0) * DV;
+    const float* ab = ap + (seq * N + t0) * D;
+    const int tid = threadIdx.x, tj = tid % TJ, ti = tid / TJ;
+
+    // total log decay of the block per channel, summed in token order like
+    // the running sums below (so that the last weight is exactly 1); the
+    // loads do not depend on the sum and stay in flight
+    if (tid < D) {
+        float l = 0.f;
+#pragma unroll 8
+        for (int t = 0; t < len; ++t)
+            l += logf(ab[(int64_t)t * D + tid]);
+        slog[tid] = l;
+    }
+    float run = 0.f;  // L_t of channel tid (tid < D), running
+    __syncthreads();
+    float acc[RI][RJ];
+#pragma unroll
+    for (int a = 0; a < RI; ++a)
+#pragma unroll
+        for (int b = 0; b < RJ; ++b)
+            acc[a][b] = 0.f;
+    float macc[kMma ? NT : 1][4];
+#pragma unroll
+    for (int nt = 0; nt < (kMma ? NT : 1); ++nt)
+        macc[nt][0] = macc[nt][1] = macc[nt][2] = macc[nt][3] = 0.f;
+    const int lane = tid & 31, warp = tid >> 5, g = lane >> 2, q = lane & 3;
+    float zacc = 0.f;
+    for (int s0 = 0; s0 < len; s0 += kSub) {
+        const int n = min(kSub, len - s0);
+        {
+            // loads issued in batches of up to eight elements before use
+            constexpr int NE = kSub * D / kThreads, NB = NE < 8 ? NE : 8;
+#pragma unroll 1
+            for (int x0 = 0; x0 < NE; x0 += NB) {
+                float ra[NB], rk[NB];
+#pragma unroll
+                for (int x = 0; x < NB; ++x) {
+                    const int e = tid + (x0 + x) * kThreads;
+                    const int t = e / D, i = e % D;
+                    ra[x] = 1.f, rk[x] = 0.f;
+                    if (t < n) {
+                        ra[x] = __ldg(ab + (int64_t)(s0 + t) * D + i);
+                        rk[x] = ldf(kb + (int64_t)(s0 + t) * D + i);
+                    }
+                }
+#pragma unroll
+                for (int x = 0; x < NB; ++x) {
+                    const int e = tid + (x0 + x) * kThreads;
+                    const int t = e / D, i = e % D;
+                    const bool in = t < n;
+                    sl[t][i] = in ? logf(ra[x]) : 0.f;
+                    sk[t][i] = in ? phi_f32(rk[x], fm) : 0.f;
+                }
+            }
+        }
+        __syncthreads();
+        if (tid < D)  // the running log-sum, and the weight exp(L_end - L_t)
+            for (int t = 0; t < n; ++t) {
+                run += sl[t][tid];
+                sk[t][tid] *= expf(slog[tid] - run);
+            }
+        {
+            constexpr int NVE = kSub * DV / kThreads, NB = NVE < 8 ? NVE : 8;
+#pragma unroll 1
+            for (int x0 = 0; x0 < NVE; x0 += NB) {
+                float rv[NB];
+#pragma unroll
+                for (int x = 0; x < NB; ++x) {
+                    const int e = tid + (x0 + x) * kThreads;
+                    const int t = e / DV, c = e % DV;
+                    rv[x] = t < n ? ldf(vb + (int64_t)(s0 + t) * DV + c) : 0.f;
+                }
+#pragma unroll
+                for (int x = 0; x < NB; ++x) {
+                    const int e = tid + (x0 + x) * kThreads;
+                    sv[e / DV][e % DV] = rv[x];
+                }
+            }
+        }
+        __syncthreads();
+        if constexpr (kMma) {
+#pragma unroll
+            for (int k0 = 0; k0 < kSub; k0 += 16) {
+                uint32_t ah[4], al[4];
+                frag_a_t_split(&sk[0][0], D + 4, 16 * warp, k0, g, q, ah, al);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    uint32_t b0, b1;
+                    frag_b(&sv[0][0], DV + 4, k0, 8 * nt, g, q, b0, b1);
+                    mma16816(macc[nt], ah, b0, b1);
+                    mma16816(macc[nt], al, b0, b1);
+                }
+            }
+            if (tid < D)
+                for (int t = 0; t < kSub; ++t)
+                    zacc += sk[t][tid];
+        } else {
+#pragma unroll 4
+            for (int t = 0; t < kSub; ++t) {
+                float kr[RI], vr[RJ];
+                lds_row(&sk[t][ti * RI], kr);
+                lds_row(&sv[t][tj * RJ], vr);
+#pragma unroll
+                for (int a = 0; a < RI; ++a)
+#pragma unroll
+                    for (int b = 0; b < RJ; ++b)
+                        acc[a][b] = fmaf(kr[a], vr[b], acc[a][b]);
+                if (tid < D)
+                    zacc += sk[t][tid];
+            }
+        }
+        __syncthreads();
+    }
+    float* dst = ws + gb * (int64_t)(D * DV + D);
+    if constexpr (kMma) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int i = 16 * warp + g, c = 8 * nt + 2 * q;
+            *reinterpret_cast<float2*>(dst + i * DV + c) = make_float2(macc[nt][0], macc[nt][1]);
+            *reinterpret_cast<float2*>(dst + (i + 8) * DV + c) = make_float2(macc[nt][2], macc[nt][3]);
+        }
+    } else {
+#pragma unroll
+        for (int a = 0; a < RI; ++a) {
+            const int i = ti * RI + a;
+#pragma unroll
+            for (int qq = 0; qq < RJ / 4; ++qq)
+                *reinterpret_cast<float4*>(dst + i * DV + tj * RJ + 4 * qq) =
+                    make_float4(acc[a][4 * qq], acc[a][4 * qq + 1], acc[a][4 * qq + 2],
+                                acc[a][4 * qq + 3]);
+        }
+    }
+    if (tid < D) {
+        dst[D * DV + tid] = zacc;
+        dec[gb * D + tid] = expf(slog[tid]);
+    }
+}
+
+// ------------------------------------------------------------- step 2 ----
+// Exclusive prefix over the blocks of each sequence, in place: element e of
+// the state (row i = e / DV, or the normaliser entry i) decays by the block's
+// exp(L_end) of channel i.
+__global__ void __launch_bounds__(kThreads)
+    k_gla_scan(float* __restrict__ ws, const float* __restrict__ dec, int nblk, int D, int DV)
+{
+    const int E = D * DV + D;
+    const int per_seq = (E + kThreads - 1) / kThreads;
+    const int64_t seq = blockIdx.x / per_seq;
+    const int e = (int)(blockIdx.x % per_seq) * kThreads + threadIdx.x;
+    if (e >= E)
+        return;
+    const int row = e < D * DV ? e / DV : e - D * DV;
+    float* base = ws + seq * (int64_t)nblk * E + e;
+    const float* db = dec + seq * (int64_t)nblk * D + row;
+    // kAhead blocks' values and decays in flight at a time
+    constexpr int kAhead = 8;
+    float acc = 0.f;
+    for (int b0 = 0; b0 < nblk; b0 += kAhead) {
+        float x[kAhead], dd[kAhead];
+#pragma unroll
+        for (int i = 0; i < kAhead; ++i)
+            if (b0 + i < nblk) {
+                x[i] = __ldcg(base + (int64_t)(b0 + i) * E);
+                dd[i] = __ldg(db + (int64_t)(b0 + i) * D);
+            }
+#pragma unroll
+        for (int i = 0; i < kAhead; ++i)
+            if (b0 + i < nblk) {
+                base[(int64_t)(b0 + i) * E] = acc;
+                acc = fmaf(acc, dd[i], x[i]);
+            }
+    }
+}
+
+// ------------------------------------------------------------- step 3 ----
 // Shared memory of the output kernel (floats): the running state S [D][DV]
 // and z [D]; phi(q), phi(k) and the running log-sums L of the sub-chunk,
 // transposed ([D][LDT], token fastest); v [kSub][DV]; the intra weights
@@ -734,7 +774,7 @@ cudaError_t run_gla(const GlaArgs& a)
     const T* q = static_cast<const T*>(a.q);
     const T* k = static_cast<const T*>(a.k);
     const T* v = static_cast<const T*>(a.v);
-    const size_t st_smem = sizeof(float) * ((size_t)kSub * (2 * D + DV) + D);
+    const size_t st_smem = sizeof(float) * ((size_t)kSub * (2 * D + DV + 8) + D);
     cudaError_t err = cudaFuncSetAttribute(k_gla_state<D, DV, T>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st_smem);
     if (err != cudaSuccess)
