@@ -747,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
         }
-        {
+        if (norm) {  // z is read by the normalised map only
             if (tid < D) {
                 const float lend = LT[tid * LDT + n - 1];
                 const float gz = expf(lend);
