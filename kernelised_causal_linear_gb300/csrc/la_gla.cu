@@ -159,13 +159,15 @@ __global__ void __launch_bounds__(kThreads)
     constexpr bool kMma = sizeof(T) == 2 && D == 128 && (DV == 128 || DV == 64);
     constexpr int NT = DV / 8;  // 8-column tiles of a warp's rows
     // dynamic shared memory (more than the 48 KiB of static arrays with
-    // D = DV = 128): phi(k) o exp(L_end - L_t), v (rows padded by 4 floats,
-    // so that the operand fragments hit different banks), log alpha, L_end
+    // D = DV = 128): phi(k) o exp(L_e - L_t) with L_e the sub-chunk's last
+    // L, v (rows padded by 4 floats, so that the operand fragments hit
+    // different banks), log alpha, the sub-chunk's decay exp(L_e - L_s)
+    // per channel (L_s: L before the sub-chunk)
     extern __shared__ __align__(16) float st_smem[];
     float(*sk)[D + 4] = reinterpret_cast<float(*)[D + 4]>(st_smem);
     float(*sv)[DV + 4] = reinterpret_cast<float(*)[DV + 4]>(st_smem + kSub * (D + 4));
     float(*sl)[D] = reinterpret_cast<float(*)[D]>(st_smem + kSub * (D + DV + 8));
-    float* slog = st_smem + kSub * (2 * D + DV + 8);
+    float* sdec = st_smem + kSub * (2 * D + DV + 8);
     const int64_t gb = blockIdx.x;
     const int64_t seq = gb / nblk;
     const int blk = (int)(gb % nblk);
@@ -176,18 +178,12 @@ __global__ void __launch_bounds__(kThreads)
     const float* ab = ap + (seq * N + t0) * D;
     const int tid = threadIdx.x, tj = tid % TJ, ti = tid / TJ;
 
-    // total log decay of the block per channel, summed in token order like
-    // the running sums below (so that the last weight is exactly 1); the
-    // loads do not depend on the sum and stay in flight
-    if (tid < D) {
-        float l = 0.f;
-#pragma unroll 8
-        for (int t = 0; t < len; ++t)
-            l += logf(ab[(int64_t)t * D + tid]);
-        slog[tid] = l;
-    }
+    // The state so far is kept relative to the end of the tokens folded in:
+    // before each sub-chunk it decays by the sub-chunk's exp(L_e - L_s) per
+    // channel, and the sub-chunk's tokens enter with exp(L_e - L_t), so that
+    // the last token of the block has weight exactly 1 and no pass over the
+    // block's gates is needed before the first sub-chunk.
     float run = 0.f;  // L_t of channel tid (tid < D), running
-    __syncthreads();
     float acc[RI][RJ];
 #pragma unroll
     for (int a = 0; a < RI; ++a)
@@ -229,11 +225,16 @@ __global__ void __launch_bounds__(kThreads)
             }
         }
         __syncthreads();
-        if (tid < D)  // the running log-sum, and the weight exp(L_end - L_t)
+        if (tid < D) {  // the running log-sum, then the weights exp(L_e - L_t)
+            const float start = run;
             for (int t = 0; t < n; ++t) {
                 run += sl[t][tid];
-                sk[t][tid] *= expf(slog[tid] - run);
+                sl[t][tid] = run;
             }
+            for (int t = 0; t < n; ++t)
+                sk[t][tid] *= expf(run - sl[t][tid]);
+            sdec[tid] = expf(run - start);
+        }
         {
             constexpr int NVE = kSub * DV / kThreads, NB = NVE < 8 ? NVE : 8;
 #pragma unroll 1
@@ -254,6 +255,14 @@ __global__ void __launch_bounds__(kThreads)
         }
         __syncthreads();
         if constexpr (kMma) {
+            {
+                const float f0 = sdec[16 * warp + g], f1 = sdec[16 * warp + g + 8];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    macc[nt][0] *= f0, macc[nt][1] *= f0;
+                    macc[nt][2] *= f1, macc[nt][3] *= f1;
+                }
+            }
 #pragma unroll
             for (int k0 = 0; k0 < kSub; k0 += 16) {
                 uint32_t ah[4], al[4];
@@ -266,10 +275,21 @@ __global__ void __launch_bounds__(kThreads)
                     mma16816(macc[nt], al, b0, b1);
                 }
             }
-            if (tid < D)
+            if (tid < D) {
+                zacc *= sdec[tid];
                 for (int t = 0; t < kSub; ++t)
                     zacc += sk[t][tid];
+            }
         } else {
+#pragma unroll
+            for (int a = 0; a < RI; ++a) {
+                const float f = sdec[ti * RI + a];
+#pragma unroll
+                for (int b = 0; b < RJ; ++b)
+                    acc[a][b] *= f;
+            }
+            if (tid < D)
+                zacc *= sdec[tid];
 #pragma unroll 4
             for (int t = 0; t < kSub; ++t) {
                 float kr[RI], vr[RJ];
@@ -307,7 +327,7 @@ __global__ void __launch_bounds__(kThreads)
     }
     if (tid < D) {
         dst[D * DV + tid] = zacc;
-        dec[gb * D + tid] = expf(slog[tid]);
+        dec[gb * D + tid] = expf(run);
     }
 }
 
