@@ -166,6 +166,10 @@ __global__ void __launch_bounds__(kThreads)
     extern __shared__ __align__(16) float st_smem[];
     float(*sk)[D + 4] = reinterpret_cast<float(*)[D + 4]>(st_smem);
     float(*sv)[DV + 4] = reinterpret_cast<float(*)[DV + 4]>(st_smem + kSub * (D + 4));
+    // the tensor-core form keeps v as bf16 pairs of consecutive tokens, word
+    // (t / 2) * (DV + 8) + c, in the same space
+    __nv_bfloat16* v2h = reinterpret_cast<__nv_bfloat16*>(&sv[0][0]);
+    const uint32_t* v2w = reinterpret_cast<const uint32_t*>(&sv[0][0]);
     float(*sl)[D] = reinterpret_cast<float(*)[D]>(st_smem + kSub * (D + DV + 8));
     float* sdec = st_smem + kSub * (2 * D + DV + 8);
     const int64_t gb = blockIdx.x;
@@ -249,7 +253,11 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
                 for (int x = 0; x < NB; ++x) {
                     const int e = tid + (x0 + x) * kThreads;
-                    sv[e / DV][e % DV] = rv[x];
+                    if constexpr (kMma)  // bf16 pairs of consecutive tokens (exact)
+                        v2h[((e / DV) >> 1) * (2 * (DV + 8)) + 2 * (e % DV) + ((e / DV) & 1)] =
+                            __float2bfloat16_rn(rv[x]);
+                    else
+                        sv[e / DV][e % DV] = rv[x];
                 }
             }
         }
@@ -269,8 +277,8 @@ __global__ void __launch_bounds__(kThreads)
                 frag_a_t_split(&sk[0][0], D + 4, 16 * warp, k0, g, q, ah, al);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    uint32_t b0, b1;
-                    frag_b(&sv[0][0], DV + 4, k0, 8 * nt, g, q, b0, b1);
+                    const uint32_t b0 = v2w[(k0 / 2 + q) * (DV + 8) + 8 * nt + g];
+                    const uint32_t b1 = v2w[(k0 / 2 + q + 4) * (DV + 8) + 8 * nt + g];
                     mma16816(macc[nt], ah, b0, b1);
                     mma16816(macc[nt], al, b0, b1);
                 }
