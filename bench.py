@@ -390,7 +390,9 @@ def main():
     if w.extra.get("favor_r"):
         kernel = "k_favor+" + kernel
     if w.extra.get("gla_gates"):
-        path, kernel = "gla_simt", "k_gla_state+k_gla_scan+k_gla_out"
+        # bf16 at d = 128: warp-level tensor-core products; fp32 products otherwise
+        path = "gla_mma" if (w.dtype == torch.bfloat16 and w.d == 128) else "gla_fp32"
+        kernel = "k_gla_state+k_gla_scan+k_gla_out"
     if decode:
         metric = "batched decode step token*heads/s, d=dv=128"
     elif w.name == "causal_n32768_d64_bf16":
@@ -444,8 +446,11 @@ def main():
 
 def la_path_dtype(w) -> str:
     """Arithmetic type of the path that runs: bf16 tensor-core operands with
-    fp32 accumulation on the tcgen05 kernel, fp32 on the CUDA-core paths."""
-    if w.steps > 0 or w.extra.get("gla_gates"):
+    fp32 accumulation on the tcgen05 kernels and on the GLA products for bf16
+    inputs at d = 128, fp32 on the CUDA-core paths."""
+    if w.extra.get("gla_gates"):
+        return "bf16" if (w.dtype == torch.bfloat16 and w.d == 128) else "f32"
+    if w.steps > 0:
         return "f32"
     import kernelised_causal_linear_gb300 as la
 
