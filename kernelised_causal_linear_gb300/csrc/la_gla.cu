@@ -83,6 +83,18 @@ __device__ __forceinline__ void frag_a_t_split(const float* X, int ld, int m0, i
     bf2_split(p[8 * ld + 8], p[9 * ld + 8], ah[3], al[3]);
 }
 
+// A[m][k] from packed pairs along k: word (k / 2) * ld + m holds
+// (A[m][k], A[m][k + 1]) (k even)
+__device__ __forceinline__ void frag_a_p(const uint32_t* P, int ld, int m0, int k0, int g, int q,
+                                         uint32_t (&a)[4])
+{
+    const uint32_t* p = P + (k0 / 2 + q) * ld + m0 + g;
+    a[0] = p[0];
+    a[1] = p[8];
+    a[2] = p[4 * ld];
+    a[3] = p[4 * ld + 8];
+}
+
 // A[m][k] = X[m * ld + k] (row-major, ld and k0 even), as hi and lo parts
 __device__ __forceinline__ void frag_a_r_split(const float* X, int ld, int m0, int k0, int g, int q,
                                                uint32_t (&ah)[4], uint32_t (&al)[4])
@@ -515,6 +527,30 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             __syncthreads();
         }
+        // tensor-core form: phi(q) o exp(L_t) as bf16 hi and lo parts of pairs
+        // of consecutive channels, word (i / 2) * LDT + t of the hi plane and
+        // the same word of the lo plane after it, in place of qT (the
+        // fragments of every warp then load words instead of splitting)
+        uint32_t* q2 = reinterpret_cast<uint32_t*>(qT);
+        const uint32_t* q2h = q2;
+        const uint32_t* q2l = q2 + (D / 2) * LDT;
+        if (kMma && split) {
+            constexpr int NP = (D / 2) * kSub / kThreads;
+            uint32_t ph[NP], pl[NP];
+#pragma unroll
+            for (int x = 0; x < NP; ++x) {
+                const int e = tid + x * kThreads, ip = e / kSub, t = e % kSub;
+                bf2_split(qT[2 * ip * LDT + t], qT[(2 * ip + 1) * LDT + t], ph[x], pl[x]);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int x = 0; x < NP; ++x) {
+                const int e = tid + x * kThreads, ip = e / kSub, t = e % kSub;
+                q2[ip * LDT + t] = ph[x];
+                q2[(D / 2) * LDT + ip * LDT + t] = pl[x];
+            }
+            __syncthreads();
+        }
         // intra weights A_tj = sum_i q_ti k_ji exp(L_ti - L_ji), j <= t:
         // thread (ty, tx) takes tokens 4 ty .. 4 ty + 3 and key token tx
         if (kMma && split) {
@@ -524,7 +560,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int k0 = 0; k0 < D; k0 += 16) {
                 uint32_t ah[4], al[4], bh[2], bl[2];
-                frag_a_t_split(qT, LDT, m0, k0, g, q, ah, al);
+                frag_a_p(q2h, LDT, m0, k0, g, q, ah);
+                frag_a_p(q2l, LDT, m0, k0, g, q, al);
                 frag_b_split(kT, LDT, k0, n0, g, q, bh, bl);
                 mma16816(acc, ah, bh[0], bh[1]);
                 mma16816(acc, ah, bl[0], bl[1]);
@@ -593,7 +630,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int t = 4 * warp; t < 4 * warp + 4; ++t) {
                 float part = lane <= t ? AT[lane * LDT + t] : 0.f;
                 for (int i = lane; i < D; i += 32) {
-                    const float qi = split ? qT[i * LDT + t] : qT[i * LDT + t] * expf(LT[i * LDT + t]);
+                    float qi;
+                    if (kMma && split) {
+                        const __nv_bfloat16* hh = reinterpret_cast<const __nv_bfloat16*>(q2h);
+                        const __nv_bfloat16* ll = reinterpret_cast<const __nv_bfloat16*>(q2l);
+                        const int w2 = 2 * ((i >> 1) * LDT + t) + (i & 1);
+                        qi = __bfloat162float(hh[w2]) + __bfloat162float(ll[w2]);
+                    } else {
+                        qi = split ? qT[i * LDT + t] : qT[i * LDT + t] * expf(LT[i * LDT + t]);
+                    }
                     part = fmaf(qi, sz[i], part);
                 }
 #pragma unroll
@@ -616,7 +661,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
                     uint32_t ah[4], al[4];
-                    frag_a_t_split(qT, LDT, 16 * mt, k0, g, q, ah, al);
+                    frag_a_p(q2h, LDT, 16 * mt, k0, g, q, ah);
+                    frag_a_p(q2l, LDT, 16 * mt, k0, g, q, al);
                     mma16816(acc[mt], ah, bh[0], bh[1]);
                     mma16816(acc[mt], ah, bl[0], bl[1]);
                     mma16816(acc[mt], al, bh[0], bh[1]);
