@@ -518,15 +518,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         // by itself.)
         const bool split =
             __syncthreads_and(tid >= D || LT[tid * LDT + n - 1] >= -60.0f) != 0;
-        if (split) {
-            if (tid < D)
-                for (int t = 0; t < kSub; ++t) {
-                    const float l = LT[tid * LDT + t];
-                    qT[tid * LDT + t] *= expf(l);
-                    kT[tid * LDT + t] *= expf(-l);
-                }
-            __syncthreads();
-        }
         // tensor-core form: phi(q) o exp(L_t) as bf16 hi and lo parts of pairs
         // of consecutive channels, word (i / 2) * LDT + t of the hi plane and
         // the same word of the lo plane after it, in place of qT (the
@@ -535,12 +526,19 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t* q2h = q2;
         const uint32_t* q2l = q2 + (D / 2) * LDT;
         if (kMma && split) {
+            // every thread rescales pairs of channels at one token, packs
+            // phi(q) in registers, and writes the planes once every read of
+            // the fp32 tile is done
             constexpr int NP = (D / 2) * kSub / kThreads;
             uint32_t ph[NP], pl[NP];
 #pragma unroll
             for (int x = 0; x < NP; ++x) {
                 const int e = tid + x * kThreads, ip = e / kSub, t = e % kSub;
-                bf2_split(qT[2 * ip * LDT + t], qT[(2 * ip + 1) * LDT + t], ph[x], pl[x]);
+                const int o0 = 2 * ip * LDT + t, o1 = o0 + LDT;
+                const float l0 = LT[o0], l1 = LT[o1];
+                bf2_split(qT[o0] * expf(l0), qT[o1] * expf(l1), ph[x], pl[x]);
+                kT[o0] *= expf(-l0);
+                kT[o1] *= expf(-l1);
             }
             __syncthreads();
 #pragma unroll
@@ -549,6 +547,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                 q2[ip * LDT + t] = ph[x];
                 q2[(D / 2) * LDT + ip * LDT + t] = pl[x];
             }
+            __syncthreads();
+        } else if (split) {
+            if (tid < D)
+                for (int t = 0; t < kSub; ++t) {
+                    const float l = LT[tid * LDT + t];
+                    qT[tid * LDT + t] *= expf(l);
+                    kT[tid * LDT + t] *= expf(-l);
+                }
             __syncthreads();
         }
         // intra weights A_tj = sum_i q_ti k_ji exp(L_ti - L_ji), j <= t:
