@@ -184,6 +184,7 @@ __global__ void __launch_bounds__(kThreads)
     const uint32_t* v2w = reinterpret_cast<const uint32_t*>(&sv[0][0]);
     float(*sl)[D] = reinterpret_cast<float(*)[D]>(st_smem + kSub * (D + DV + 8));
     float* sdec = st_smem + kSub * (2 * D + DV + 8);
+    float* sle = sdec + D;  // L_e per channel
     const int64_t gb = blockIdx.x;
     const int64_t seq = gb / nblk;
     const int blk = (int)(gb % nblk);
@@ -241,15 +242,14 @@ __global__ void __launch_bounds__(kThreads)
             }
         }
         __syncthreads();
-        if (tid < D) {  // the running log-sum, then the weights exp(L_e - L_t)
+        if (tid < D) {  // the running log-sum
             const float start = run;
             for (int t = 0; t < n; ++t) {
                 run += sl[t][tid];
                 sl[t][tid] = run;
             }
-            for (int t = 0; t < n; ++t)
-                sk[t][tid] *= expf(run - sl[t][tid]);
             sdec[tid] = expf(run - start);
+            sle[tid] = run;
         }
         {
             constexpr int NVE = kSub * DV / kThreads, NB = NVE < 8 ? NVE : 8;
@@ -272,6 +272,12 @@ __global__ void __launch_bounds__(kThreads)
                         sv[e / DV][e % DV] = rv[x];
                 }
             }
+        }
+        __syncthreads();
+        // the weights exp(L_e - L_t), spread over every thread
+        for (int e = tid; e < n * D; e += kThreads) {
+            const int t = e / D, i = e % D;
+            sk[t][i] *= expf(sle[i] - sl[t][i]);
         }
         __syncthreads();
         if constexpr (kMma) {
@@ -854,7 +860,7 @@ cudaError_t run_gla(const GlaArgs& a)
     const T* q = static_cast<const T*>(a.q);
     const T* k = static_cast<const T*>(a.k);
     const T* v = static_cast<const T*>(a.v);
-    const size_t st_smem = sizeof(float) * ((size_t)kSub * (2 * D + DV + 8) + D);
+    const size_t st_smem = sizeof(float) * ((size_t)kSub * (2 * D + DV + 8) + 2 * D);
     cudaError_t err = cudaFuncSetAttribute(k_gla_state<D, DV, T>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st_smem);
     if (err != cudaSuccess)
