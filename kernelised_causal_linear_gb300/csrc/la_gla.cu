@@ -509,12 +509,23 @@ __global__ void __launch_bounds__(kThreads, 2)
                 sv[((tid + x * kThreads) / DVC) * SV + (tid + x * kThreads) % DVC] = rv[x];
         }
         __syncthreads();
-        if (tid < D) {
+        if (tid < D) {  // channel tid's 32 log gates in registers, summed in token order
+            float4* row = reinterpret_cast<float4*>(LT + tid * LDT);
+            float4 x[kSub / 4];
+#pragma unroll
+            for (int u = 0; u < kSub / 4; ++u)
+                x[u] = row[u];
             float run = 0.f;
-            for (int t = 0; t < kSub; ++t) {
-                run += LT[tid * LDT + t];
-                LT[tid * LDT + t] = run;
+#pragma unroll
+            for (int u = 0; u < kSub / 4; ++u) {
+                run += x[u].x, x[u].x = run;
+                run += x[u].y, x[u].y = run;
+                run += x[u].z, x[u].z = run;
+                run += x[u].w, x[u].w = run;
             }
+#pragma unroll
+            for (int u = 0; u < kSub / 4; ++u)
+                row[u] = x[u];
         }
         // When the sub-chunk's decay stays above e^-60 in every channel,
         // exp(L_t - L_j) = exp(L_t) exp(-L_j) with both factors in fp32 range:
