@@ -9,9 +9,11 @@
 // M_{s-1} + k_s^T v_s).  The gates are inputs (data dependent, drawn or
 // computed by the caller).
 //
-// Chunked on CUDA cores in fp32, in three launches like the scalar-decay
-// path, with every decay factor taken as exp of a difference of running
-// log-sums, so that no factor exceeds 1 (no ratio of small products):
+// Chunked in three launches like the scalar-decay path, in fp32, with every
+// decay factor taken as exp of a difference of running log-sums, so that no
+// factor exceeds 1 (no ratio of small products); with bf16 inputs at d = 128
+// the products of steps 1 and 3 run on the tensor cores (warp-level bf16
+// MMAs with fp32 accumulation, fp32 operands as bf16 hi/lo pairs):
 //   1. block state   dS_b = sum_t exp(L_end - L_t) o phi(k_t) v_t^T, with L the
 //                    running sum of log alpha inside the block; the block's
 //                    total decay exp(L_end) per channel is stored beside it
