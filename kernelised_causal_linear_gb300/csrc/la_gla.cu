@@ -166,10 +166,11 @@ __global__ void __launch_bounds__(kThreads)
 {
     using TL = StateTile<D, DV>;
     constexpr int TJ = TL::TJ, RI = TL::RI, RJ = TL::RJ;
-    // bf16 inputs at d = 128: the block state is a tensor-core product
-    // (mma.sync m16n8k16, fp32 accumulation) of phi(k) o exp(L_end - L_t),
-    // an fp32 bf16 hi/lo pair, and v, exact in bf16; warp w owns state rows
-    // 16 w .. 16 w + 15
+    // bf16 inputs at d = 128: each sub-chunk's part of the block state is a
+    // tensor-core product (mma.sync m16n8k16, fp32 accumulation) of the
+    // weighted phi(k), an fp32 bf16 hi/lo pair, and v, exact in bf16; warp w
+    // owns state rows 16 w .. 16 w + 15 (the log gates use the hardware
+    // logarithm, as in the output kernel)
     constexpr bool kMma = sizeof(T) == 2 && D == 128 && (DV == 128 || DV == 64);
     constexpr int NT = DV / 8;  // 8-column tiles of a warp's rows
     // dynamic shared memory (more than the 48 KiB of static arrays with
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(kThreads)
                     const int e = tid + (x0 + x) * kThreads;
                     const int t = e / D, i = e % D;
                     const bool in = t < n;
-                    sl[t][i] = in ? logf(ra[x]) : 0.f;
+                    sl[t][i] = in ? (kMma ? __logf(ra[x]) : logf(ra[x])) : 0.f;
                     sk[t][i] = in ? phi_f32(rk[x], fm) : 0.f;
                 }
             }
@@ -435,7 +436,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     // operands, fp32 accumulation).  The rescaled features, the state and the
     // intra weights are fp32 and enter as bf16 hi/lo pairs (hi*hi + hi*lo +
     // lo*hi, ~2^-16 relative: a single rounding of the features showed in
-    // the unnormalised outputs, whose sums cancel); v is exact in bf16.
+    // the unnormalised outputs, whose sums cancel); v is exact in bf16.  The
+    // log gates use the hardware logarithm (absolute error below 2^-21 on
+    // [0.5, 2], three ulp elsewhere), far inside the bf16 tolerance.
     constexpr bool kMma = sizeof(T) == 2 && D == 128 && DVC == 64;
     extern __shared__ __align__(16) float smem[];
     float* sS = smem;
@@ -502,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int wt = e >> 5, cg = wt % (D / 8), tg = wt / (D / 8);
                 const int i = 8 * cg + (e & 7), t = 4 * tg + ((e >> 3) & 3);
                 const bool in = t < n;
-                LT[i * LDT + t] = in ? logf(ra[x]) : 0.f;
+                LT[i * LDT + t] = in ? (kMma ? __logf(ra[x]) : logf(ra[x])) : 0.f;
                 qT[i * LDT + t] = in ? phi_f32(rq[x], fm) : 0.f;
                 kT[i * LDT + t] = in ? phi_f32(rk[x], fm) : 0.f;
             }
